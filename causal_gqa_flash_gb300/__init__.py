@@ -1,1 +1,164 @@
-"""Causal grouped-query flash attention (forward and backward) for GB300 / sm_103a."""
+"""Causal grouped-query flash attention (forward and backward) for GB300 / sm_103a.
+
+A thin ctypes binding over the C ABI declared in ``include/gqa_attn.h``. The
+functions below only marshal arguments: torch provides device memory and the
+current stream, and every step of the computation runs in the library's CUDA
+kernels. There is no CPU fallback: if the compiled library is missing, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import build, library_path
+
+__all__ = [
+    "AttnError", "build", "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
+    "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_last_error", "attn_version",
+    "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
+    "GQA_ERR_TIMEOUT",
+]
+
+GQA_OK = 0
+GQA_ERR_INVALID_ARG = 1
+GQA_ERR_UNSUPPORTED_DEVICE = 2
+GQA_ERR_LAUNCH = 3
+GQA_ERR_TIMEOUT = 4
+
+# Every function include/gqa_attn.h declares.
+EXPORTED_SYMBOLS = (
+    "attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_last_error", "attn_sync_status",
+    "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_version",
+)
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[{code}] {message}")
+        self.code = code
+
+
+def load():
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built ({path} missing): call causal_gqa_flash_gb300.build()")
+    lib = ctypes.CDLL(path)
+    vp, i, sz, ull = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_ulonglong
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+    lib.attn_fwd.restype = i
+    lib.attn_bwd_workspace_bytes.argtypes = [i, i, i]
+    lib.attn_bwd_workspace_bytes.restype = sz
+    lib.attn_bwd.argtypes = [vp] * 10 + [sz, i, i, i, i, i, i, vp]
+    lib.attn_bwd.restype = i
+    lib.attn_last_error.argtypes = []
+    lib.attn_last_error.restype = ctypes.c_char_p
+    lib.attn_sync_status.argtypes = [vp]
+    lib.attn_sync_status.restype = i
+    lib.attn_selftest_timeout.argtypes = [ull, vp]
+    lib.attn_selftest_timeout.restype = i
+    lib.attn_set_wait_budget_ns.argtypes = [ull]
+    lib.attn_set_wait_budget_ns.restype = None
+    lib.attn_version.argtypes = []
+    lib.attn_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def attn_last_error() -> str:
+    return load().attn_last_error().decode()
+
+
+def attn_version() -> str:
+    return load().attn_version().decode()
+
+
+def _check(code: int):
+    if code != GQA_OK:
+        raise AttnError(code, attn_last_error())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _dims(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k, v must be [B, T, H, d]")
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    return B, T, Hq, Hkv, d
+
+
+def attn_fwd(q, k, v, causal: bool = True, o=None, lse=None, stream=None):
+    """O, LSE = attention(q, k, v). q [B,T,Hq,d], k/v [B,T,Hkv,d] bf16 CUDA tensors, contiguous.
+
+    Returns (o bf16 [B,T,Hq,d], lse fp32 [B,Hq,T]). Output buffers may be passed in.
+    """
+    import torch
+    lib = load()
+    B, T, Hq, Hkv, d = _dims(q, k)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    _check(lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, T, Hq, Hkv, d, int(bool(causal)),
+                        _stream_handle(stream)))
+    return o, lse
+
+
+def attn_bwd_workspace_bytes(B: int, T: int, Hq: int) -> int:
+    return int(load().attn_bwd_workspace_bytes(B, T, Hq))
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool = True, dq=None, dk=None, dv=None, workspace=None,
+             stream=None):
+    """dQ, dK, dV of sum(O * dO). Returns (dq, dk, dv) bf16 with the shapes of q, k, v."""
+    import torch
+    lib = load()
+    B, T, Hq, Hkv, d = _dims(q, k)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dout)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    need = attn_bwd_workspace_bytes(B, T, Hq)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                        _ptr(workspace), ws_bytes, B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
+    return dq, dk, dv
+
+
+def attn_sync_status(stream=None) -> int:
+    """Synchronise the stream and return the device status code (0 = OK, 4 = a wait timed out)."""
+    return int(load().attn_sync_status(_stream_handle(stream)))
+
+
+def attn_selftest_timeout(budget_ns: int, stream=None):
+    _check(load().attn_selftest_timeout(int(budget_ns), _stream_handle(stream)))
+
+
+def attn_set_wait_budget_ns(budget_ns: int):
+    load().attn_set_wait_budget_ns(int(budget_ns))

@@ -1,0 +1,301 @@
+// api.cu — the C ABI (include/gqa_attn.h): argument checks, TMA tensor maps,
+// the per-device status word, and kernel launches on the caller's stream.
+//
+// Error convention after "Talking to the GPU", §One macro for every call: every
+// CUDA call is checked, and a failure is reported with the call's name and the
+// runtime's own words — here as a return code plus attn_last_error(), never by
+// exiting the process.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/gqa_attn.h"
+#include "attn_common.cuh"
+
+namespace gqa {
+
+__device__ DevStatusWord g_status_word;
+
+__global__ void selftest_timeout_kernel(DevStatusWord* status, unsigned long long budget_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_sh;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtx ctx{&abort_sh, status, budget_ns, kKidSelfTest};
+  // Nobody arrives on `bar`: the wait must run out and record a timeout.
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, ctx, 1);
+  __syncthreads();
+}
+
+cudaError_t launch_selftest_timeout(DevStatusWord* status, unsigned long long budget_ns, cudaStream_t stream) {
+  selftest_timeout_kernel<<<1, 32, 0, stream>>>(status, budget_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace gqa
+
+using namespace gqa;
+
+namespace {
+
+thread_local std::string t_last_error;
+std::atomic<unsigned long long> g_budget_ns{2000000000ull};
+constexpr unsigned long long kDefaultBudgetNs = 2000000000ull;
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  DevStatusWord* status = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+gqa_status_t fail(gqa_status_t code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return code;
+}
+
+gqa_status_t cuda_fail(const char* fn, const char* what, cudaError_t e) {
+  return fail(GQA_ERR_LAUNCH, "%s: %s failed: %s (%s)", fn, what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+// Per-device setup: capability check, status-word address, tensor-map encoder.
+gqa_status_t device_state(const char* fn, DeviceState** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(fn, "cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxDevices) return fail(GQA_ERR_UNSUPPORTED_DEVICE, "%s: device %d out of range", fn, dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e != cudaSuccess) return cuda_fail(fn, "cudaDeviceGetAttribute", e);
+    e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_fail(fn, "cudaDeviceGetAttribute", e);
+    st.supported = (major == 10 && minor == 3);
+    if (st.supported) {
+      void* addr = nullptr;
+      e = cudaGetSymbolAddress(&addr, g_status_word);
+      if (e != cudaSuccess) return cuda_fail(fn, "cudaGetSymbolAddress(status word)", e);
+      st.status = static_cast<DevStatusWord*>(addr);
+      if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f)
+          return fail(GQA_ERR_LAUNCH, "%s: cannot resolve cuTensorMapEncodeTiled", fn);
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+      }
+    }
+    st.ready = true;
+  }
+  if (!st.supported)
+    return fail(GQA_ERR_UNSUPPORTED_DEVICE, "%s: device %d is not compute capability 10.3 (GB300)", fn, dev);
+  *out = &st;
+  return GQA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gqa_status_t check_shape(const char* fn, int B, int T, int Hq, int Hkv, int d) {
+  if (B <= 0 || T <= 0 || Hq <= 0 || Hkv <= 0)
+    return fail(GQA_ERR_INVALID_ARG, "%s: B, T, Hq, Hkv must be positive (got %d, %d, %d, %d)", fn, B, T, Hq, Hkv);
+  if (d != 64 && d != 128) return fail(GQA_ERR_INVALID_ARG, "%s: d must be 64 or 128 (got %d)", fn, d);
+  if (Hq % Hkv != 0) return fail(GQA_ERR_INVALID_ARG, "%s: Hq (%d) must be a multiple of Hkv (%d)", fn, Hq, Hkv);
+  // Index arithmetic inside the kernels uses 32-bit tile coordinates and
+  // 64-bit element offsets; keep every TMA coordinate and grid size in range.
+  const long long tiles = (long long)B * Hq * ((T + kTile - 1) / kTile);
+  if (tiles > 0x7fffffffLL || (long long)T > (1LL << 30))
+    return fail(GQA_ERR_INVALID_ARG, "%s: problem too large (B*Hq*ceil(T/128) = %lld)", fn, tiles);
+  return GQA_OK;
+}
+
+gqa_status_t check_ptr(const char* fn, const char* name, const void* p) {
+  if (!p) return fail(GQA_ERR_INVALID_ARG, "%s: %s is NULL", fn, name);
+  if (!aligned16(p)) return fail(GQA_ERR_INVALID_ARG, "%s: %s is not 16-byte aligned", fn, name);
+  return GQA_OK;
+}
+
+// 4D tiled map over a [B, T, H, d] bf16 tensor: box = 64 (d) x 1 (head) x 128 (rows) x 1 (batch),
+// 128-byte swizzle; rows past T read as zero.
+gqa_status_t make_map(const char* fn, const char* name, CUtensorMap* m, const void* ptr, int B, int T, int H,
+                      int d) {
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)T * H * d * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GQA_ERR_INVALID_ARG, "%s: cuTensorMapEncodeTiled(%s) failed (%d)", fn, name, (int)r);
+  return GQA_OK;
+}
+
+size_t round_up_tile(int T) { return ((size_t)T + kTile - 1) / kTile * kTile; }
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_version(void) { return "0.1.0"; }
+
+const char* attn_last_error(void) { return t_last_error.c_str(); }
+
+void attn_set_wait_budget_ns(unsigned long long budget_ns) {
+  g_budget_ns.store(budget_ns ? budget_ns : kDefaultBudgetNs);
+}
+
+size_t attn_bwd_workspace_bytes(int B, int T, int Hq) {
+  if (B <= 0 || T <= 0 || Hq <= 0) return 0;
+  return 2 * (size_t)B * (size_t)Hq * round_up_tile(T) * sizeof(float);
+}
+
+gqa_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int Hq,
+                      int Hkv, int d, int causal, void* stream) {
+  const char* fn = "attn_fwd";
+  t_last_error.clear();
+  gqa_status_t s;
+  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
+  if ((s = check_ptr(fn, "q", q)) || (s = check_ptr(fn, "k", k)) || (s = check_ptr(fn, "v", v)) ||
+      (s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)))
+    return s;
+  DeviceState* ds = nullptr;
+  if ((s = device_state(fn, &ds))) return s;
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  if ((s = make_map(fn, "q", &p.tmap_q, q, B, T, Hq, d)) || (s = make_map(fn, "k", &p.tmap_k, k, B, T, Hkv, d)) ||
+      (s = make_map(fn, "v", &p.tmap_v, v, B, T, Hkv, d)))
+    return s;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.nT = (T + kTile - 1) / kTile;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
+  p.status = ds->status;
+  p.budget_ns = g_budget_ns.load();
+  cudaError_t e = launch_fwd(p, d, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(fn, "kernel launch", e);
+  return GQA_OK;
+}
+
+gqa_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int T, int Hq,
+                      int Hkv, int d, int causal, void* stream) {
+  const char* fn = "attn_bwd";
+  t_last_error.clear();
+  gqa_status_t s;
+  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
+  if ((s = check_ptr(fn, "q", q)) || (s = check_ptr(fn, "k", k)) || (s = check_ptr(fn, "v", v)) ||
+      (s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)) || (s = check_ptr(fn, "dO", dO)) ||
+      (s = check_ptr(fn, "dq", dq)) || (s = check_ptr(fn, "dk", dk)) || (s = check_ptr(fn, "dv", dv)) ||
+      (s = check_ptr(fn, "workspace", workspace)))
+    return s;
+  const size_t need = attn_bwd_workspace_bytes(B, T, Hq);
+  if (workspace_bytes < need)
+    return fail(GQA_ERR_INVALID_ARG, "%s: workspace_bytes %zu < required %zu", fn, workspace_bytes, need);
+  DeviceState* ds = nullptr;
+  if ((s = device_state(fn, &ds))) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int Tpad = (int)round_up_tile(T);
+  float* Dvec = static_cast<float*>(workspace);
+  float* lse2 = Dvec + (size_t)B * Hq * Tpad;
+
+  BwdPreParams pp;
+  pp.o = o;
+  pp.dO = dO;
+  pp.lse = lse;
+  pp.Dvec = Dvec;
+  pp.lse2 = lse2;
+  pp.B = B;
+  pp.T = T;
+  pp.Hq = Hq;
+  pp.Tpad = Tpad;
+  cudaError_t e = launch_bwd_pre(pp, d, st);
+  if (e != cudaSuccess) return cuda_fail(fn, "preprocess launch", e);
+
+  BwdParams p;
+  memset(&p, 0, sizeof(p));
+  if ((s = make_map(fn, "q", &p.tmap_q, q, B, T, Hq, d)) || (s = make_map(fn, "k", &p.tmap_k, k, B, T, Hkv, d)) ||
+      (s = make_map(fn, "v", &p.tmap_v, v, B, T, Hkv, d)) || (s = make_map(fn, "dO", &p.tmap_do, dO, B, T, Hq, d)))
+    return s;
+  p.Dvec = Dvec;
+  p.lse2 = lse2;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = B;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.nT = (T + kTile - 1) / kTile;
+  p.Tpad = Tpad;
+  p.causal = causal ? 1 : 0;
+  p.scale = (float)(1.0 / sqrt((double)d));
+  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
+  p.status = ds->status;
+  p.budget_ns = g_budget_ns.load();
+  e = launch_bwd_dq(p, d, st);
+  if (e != cudaSuccess) return cuda_fail(fn, "dQ kernel launch", e);
+  e = launch_bwd_dkv(p, d, st);
+  if (e != cudaSuccess) return cuda_fail(fn, "dK/dV kernel launch", e);
+  return GQA_OK;
+}
+
+gqa_status_t attn_sync_status(void* stream) {
+  const char* fn = "attn_sync_status";
+  t_last_error.clear();
+  DeviceState* ds = nullptr;
+  gqa_status_t s;
+  if ((s = device_state(fn, &ds))) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(fn, "cudaStreamSynchronize", e);
+  DevStatusWord w;
+  e = cudaMemcpy(&w, ds->status, sizeof(w), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(fn, "cudaMemcpy(status word)", e);
+  if (w.code == kDevOk) return GQA_OK;
+  static const char* names[] = {"?", "attn_fwd", "bwd_preprocess", "bwd_dq", "bwd_dkv", "?", "?", "?", "?",
+                                "selftest"};
+  const char* kname = w.kernel < 10 ? names[w.kernel] : "?";
+  DevStatusWord zero;
+  memset(&zero, 0, sizeof(zero));
+  e = cudaMemcpy(ds->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(fn, "cudaMemcpy(clear status word)", e);
+  return fail(GQA_ERR_TIMEOUT, "%s: kernel %s gave up waiting (wait %u, block %u)", fn, kname, w.where, w.block);
+}
+
+gqa_status_t attn_selftest_timeout(unsigned long long budget_ns, void* stream) {
+  const char* fn = "attn_selftest_timeout";
+  t_last_error.clear();
+  DeviceState* ds = nullptr;
+  gqa_status_t s;
+  if ((s = device_state(fn, &ds))) return s;
+  cudaError_t e = launch_selftest_timeout(ds->status, budget_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(fn, "kernel launch", e);
+  return GQA_OK;
+}
+
+}  // extern "C"

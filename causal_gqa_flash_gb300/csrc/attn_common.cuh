@@ -1,0 +1,81 @@
+// attn_common.cuh — parameters and tile geometry shared by the attention kernels
+// and the host code that launches them.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "sm103_ptx.cuh"
+
+namespace gqa {
+
+// Query and key tiles are 128 rows: one row per TMEM lane, M = 128 MMAs.
+constexpr int kTile = 128;
+// One 128-byte swizzle atom column block: 64 bf16 of the head dim, 128 rows.
+constexpr int kHalfTileBytes = kTile * 128;
+
+enum KernelId : unsigned int {
+  kKidFwd = 1,
+  kKidBwdPre = 2,
+  kKidBwdDq = 3,
+  kKidBwdDkv = 4,
+  kKidSelfTest = 9,
+};
+
+// Forward: one CTA per (128-query tile, query head, batch).
+struct FwdParams {
+  CUtensorMap tmap_q;  // [B,T,Hq,d] bf16, box 64 x 1 x 128 x 1, 128B swizzle
+  CUtensorMap tmap_k;  // [B,T,Hkv,d]
+  CUtensorMap tmap_v;  // [B,T,Hkv,d]
+  void* o;             // [B,T,Hq,d] bf16
+  float* lse;          // [B,Hq,T] fp32, natural log
+  int B, T, Hq, Hkv, G, nT;
+  int causal;
+  float scale_log2;    // (1/sqrt(d)) * log2(e)
+  DevStatusWord* status;
+  unsigned long long budget_ns;
+};
+
+// Backward preprocess: D = rowsum(dO * O), LSE2 = LSE * log2(e), both [B,Hq,Tpad].
+struct BwdPreParams {
+  const void* o;
+  const void* dO;
+  const float* lse;
+  float* Dvec;   // [B,Hq,Tpad]
+  float* lse2;   // [B,Hq,Tpad]
+  int B, T, Hq, Tpad;
+};
+
+// Backward dQ (one CTA per query tile) and dK/dV (one CTA per key tile).
+struct BwdParams {
+  CUtensorMap tmap_q;
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
+  CUtensorMap tmap_do;
+  const float* Dvec;   // [B,Hq,Tpad]
+  const float* lse2;   // [B,Hq,Tpad]
+  void* dq;            // [B,T,Hq,d]
+  void* dk;            // [B,T,Hkv,d]
+  void* dv;            // [B,T,Hkv,d]
+  int B, T, Hq, Hkv, G, nT, Tpad;
+  int causal;
+  float scale;         // 1/sqrt(d)
+  float scale_log2;    // scale * log2(e)
+  DevStatusWord* status;
+  unsigned long long budget_ns;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+// Host-side launchers (defined next to their kernels).
+cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
+cudaError_t launch_bwd_pre(const BwdPreParams& p, int d, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdParams& p, int d, cudaStream_t stream);
+cudaError_t launch_bwd_dkv(const BwdParams& p, int d, cudaStream_t stream);
+cudaError_t launch_selftest_timeout(DevStatusWord* status, unsigned long long budget_ns, cudaStream_t stream);
+
+}  // namespace gqa

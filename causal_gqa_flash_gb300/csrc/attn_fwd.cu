@@ -1,0 +1,332 @@
+// attn_fwd.cu — forward kernel of causal grouped-query flash attention for sm_103a.
+//
+// "A transformer in PTX", §Flash attention: a block of queries walks the key
+// blocks up to the diagonal keeping each row's running max and sum (online
+// softmax); scores are scaled once by log2(e)/sqrt(d) so each probability is
+// 2^(s - max) through the hardware ex2; P never goes to memory; the row's
+// log-sum-exp is saved for the backward.
+//
+// GB300 design (not the page's mma.sync/ldmatrix/cp.async design):
+//  * one CTA = one 128-query tile of one (batch, query head); two CTAs share
+//    an SM so one's softmax overlaps the other's tensor-core work;
+//  * warp 0 issues TMA loads (Q once, a K ring and a V ring, 128B swizzle),
+//    warp 1 issues tcgen05 MMAs from one thread and owns the TMEM allocation,
+//    warps 2-5 are the softmax warpgroup: one thread per query row, which is
+//    one TMEM lane, so row max and row sum need no shuffles;
+//  * S = Q K^T (SS MMA, fp32 in TMEM columns [0,128)), P is written back as
+//    bf16 over S's first 64 columns and O += P V is a TS MMA (A from TMEM,
+//    V as an MN-major smem operand) into TMEM columns [128, 128+d);
+//  * the running max is rescaled lazily: O and l are only rescaled when a
+//    row's max grows by more than 2^8, otherwise p = 2^(s - m_stale) <= 256;
+//  * causal tiles past the diagonal are never visited; only the diagonal tile
+//    is masked; ragged T relies on TMA zero fill plus the causal mask.
+#include "attn_common.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kFwdThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0;     // S fp32 [128 x 128]; P bf16 aliases [0, 64)
+constexpr uint32_t kColO = 128;   // O fp32 [128 x d]
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kTileBytes = kHalves * kHalfTileBytes;  // 128 rows x D bf16
+  static constexpr int kKStages = (D == 64) ? 2 : 1;
+  static constexpr int kVStages = (D == 64) ? 2 : 1;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kSmemBytes = kOffV + kVStages * kTileBytes + 1024;  // + alignment slack
+};
+
+// Wait with a warp-uniform outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& c, unsigned where) {
+  bool ok = mbar_wait(bar, parity, c, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using Cfg = FwdCfg<D>;
+  constexpr int KS = Cfg::kKStages;
+  constexpr int VS = Cfg::kVStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ uint64_t bar_q, bar_kf[KS], bar_ke[KS], bar_vf[VS], bar_ve[VS], bar_s, bar_p, bar_o, bar_drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work item: heaviest query tiles first (causal cost grows with the tile index).
+  const int nbh = p.B * p.Hq;
+  const int qt = p.nT - 1 - static_cast<int>(blockIdx.x) / nbh;
+  const int bh = static_cast<int>(blockIdx.x) % nbh;
+  const int b = bh / p.Hq;
+  const int h = bh % p.Hq;
+  const int kvh = h / p.G;
+  const int n_kv = p.causal ? qt + 1 : p.nT;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_q, 1);
+    for (int s = 0; s < KS; ++s) { mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1); }
+    for (int s = 0; s < VS; ++s) { mbar_init(&bar_vf[s], 1); mbar_init(&bar_ve[s], 1); }
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_p, 128);
+    mbar_init(&bar_o, 1);
+    mbar_init(&bar_drain, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const WaitCtx ctx{&abort_sh, p.status, p.budget_ns, kKidFwd};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tmap_q);
+      tma_prefetch_desc(&p.tmap_k);
+      tma_prefetch_desc(&p.tmap_v);
+      mbar_arrive_expect_tx(&bar_q, Cfg::kTileBytes);
+      for (int hf = 0; hf < Cfg::kHalves; ++hf)
+        tma_load_4d(smem + Cfg::kOffQ + hf * kHalfTileBytes, &p.tmap_q, &bar_q, hf * 64, h, qt * kTile, b);
+      int issued_k[KS] = {}, issued_v[VS] = {};
+      bool ok = true;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int ks = j % KS, kn = j / KS;
+        if (kn > 0) ok = mbar_wait(&bar_ke[ks], (kn - 1) & 1, ctx, 1);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bar_kf[ks], Cfg::kTileBytes);
+        for (int hf = 0; hf < Cfg::kHalves; ++hf)
+          tma_load_4d(smem + Cfg::kOffK + ks * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_k, &bar_kf[ks],
+                      hf * 64, kvh, j * kTile, b);
+        issued_k[ks]++;
+        const int vs = j % VS, vn = j / VS;
+        if (vn > 0) ok = mbar_wait(&bar_ve[vs], (vn - 1) & 1, ctx, 2);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bar_vf[vs], Cfg::kTileBytes);
+        for (int hf = 0; hf < Cfg::kHalves; ++hf)
+          tma_load_4d(smem + Cfg::kOffV + vs * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v, &bar_vf[vs],
+                      hf * 64, kvh, j * kTile, b);
+        issued_v[vs]++;
+      }
+      if (ok) {
+        // Wait for the MMA side to release every stage, so that no commit
+        // arrives on a barrier of this CTA after it has left.
+        for (int s = 0; s < KS && ok; ++s)
+          if (issued_k[s] > 0) ok = mbar_wait(&bar_ke[s], (issued_k[s] - 1) & 1, ctx, 3);
+        for (int s = 0; s < VS && ok; ++s)
+          if (issued_v[s] > 0) ok = mbar_wait(&bar_ve[s], (issued_v[s] - 1) & 1, ctx, 4);
+      }
+      if (!ok) {
+        // Abort path: let every load already issued land before the CTA exits.
+        mbar_wait_drain(&bar_q, 0, p.budget_ns);
+        for (int s = 0; s < KS; ++s)
+          if (issued_k[s] > 0) mbar_wait_drain(&bar_kf[s], (issued_k[s] - 1) & 1, p.budget_ns);
+        for (int s = 0; s < VS; ++s)
+          if (issued_v[s] > 0) mbar_wait_drain(&bar_vf[s], (issued_v[s] - 1) & 1, p.budget_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t sQ = smem_u32(smem + Cfg::kOffQ);
+      const uint32_t sK = smem_u32(smem + Cfg::kOffK);
+      const uint32_t sV = smem_u32(smem + Cfg::kOffV);
+      bool issued = false;
+      auto issue_pv = [&](int jj) -> bool {
+        const int vs = jj % VS;
+        if (!mbar_wait(&bar_p, jj & 1, ctx, 12)) return false;
+        if (!mbar_wait(&bar_vf[vs], (jj / VS) & 1, ctx, 13)) return false;
+        tc_fence_after();
+        const uint32_t vbase = sV + vs * Cfg::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, kHalfTileBytes, 1024);
+          mma_ts(tmem + kColO, tmem + kColS + kk * 8, bdesc, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bar_ve[vs]);
+        return true;
+      };
+      bool ok = mbar_wait(&bar_q, 0, ctx, 10);
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int ks = j % KS;
+        // O += P_{j-1} V_{j-1} must be issued before S_j overwrites P_{j-1}.
+        if (j > 0) {
+          ok = issue_pv(j - 1);
+          if (!ok) break;
+        }
+        ok = mbar_wait(&bar_kf[ks], (j / KS) & 1, ctx, 11);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kbase = sK + ks * Cfg::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
+          mma_ss(tmem + kColS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), idesc_s,
+                 kk > 0 ? 1u : 0u);
+        }
+        issued = true;
+        mma_commit(&bar_s);
+        mma_commit(&bar_ke[ks]);
+      }
+      if (ok) ok = issue_pv(n_kv - 1);
+      if (ok) {
+        mma_commit(&bar_o);
+      } else if (issued) {
+        mma_commit(&bar_drain);
+        mbar_wait_drain(&bar_drain, 0, p.budget_ns);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroup
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int q_idx = qt * kTile + row;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_base + kColS;
+    const uint32_t tO = tmem + lane_base + kColO;
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY;  // running max in log2 units (possibly stale by <= 8)
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = warp_wait(&bar_s, j & 1, ctx, 20);
+      if (!ok) break;
+      tc_fence_after();
+      float s[kTile];
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(tS + c * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+        }
+      }
+      if (p.causal && j == qt) {
+#pragma unroll
+        for (int c = 0; c < kTile; ++c)
+          if (c > row) s[c] = -INFINITY;
+      } else if (!p.causal && (j + 1) * kTile > p.T) {
+        const int lim = p.T - j * kTile;
+#pragma unroll
+        for (int c = 0; c < kTile; ++c)
+          if (c >= lim) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < kTile; ++c) mx = fmaxf(mx, s[c]);
+      const float m_tile = mx * sl2;
+      const bool need = m_tile > m_used + kRescaleThreshold;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2_approx(m_used - m_tile);
+        m_used = m_tile;
+        l *= alpha;
+      }
+      const float neg_m = -m_used;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, neg_m));
+          const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, neg_m));
+          l += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + c * 16, pk);
+      }
+      // Rescale O (already complete: S_j's commit follows PV_{j-1}) when any row of this warp needs it.
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tO + c * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st32(tO + c * 32, r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar_p);
+    }
+    if (ok) ok = warp_wait(&bar_o, 0, ctx, 21);
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const bool valid = q_idx < p.T;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                            ((static_cast<size_t>(b) * p.T + (valid ? q_idx : 0)) * p.Hq + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tO + c * 32, r);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+      if (valid)
+        p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.T + q_idx] = (m_used + log2f(l)) * 0.69314718055994531f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
+  constexpr int smem = FwdCfg<D>::kSmemBytes;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const unsigned grid = static_cast<unsigned>(p.B) * p.Hq * p.nT;
+  attn_fwd_kernel<D><<<grid, kFwdThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
+  return d == 64 ? launch_fwd_d<64>(p, stream) : launch_fwd_d<128>(p, stream);
+}
+
+}  // namespace gqa

@@ -1,0 +1,117 @@
+/*
+ * gqa_attn.h — C ABI of the causal grouped-query flash-attention library for
+ * GB300 (sm_103a): forward and backward, bf16 inputs, fp32 accumulation.
+ *
+ * The operation is the attention of "A transformer in PTX" (mnemonic-site,
+ * 5-transformer):
+ *  - §The model: a causal decoder whose attention is grouped-query — query
+ *    head h reads key/value head h / (Hq/Hkv), several query heads per kv head.
+ *  - §Flash attention: O = softmax(scale * Q K^T, masked so key j is visible to
+ *    query i only when j <= i) V, with scale = 1/sqrt(d), computed block by
+ *    block without writing the T x T score matrix, and the log-sum-exp of each
+ *    row saved so that the backward can recompute the probabilities.
+ *  - §The same bits every time: the backward is a dQ pass per block of
+ *    queries and a dK/dV pass per block of keys that loops over every query
+ *    head sharing the kv head; no float atomics, every sum has one owner and
+ *    one order, so repeated calls give identical bits.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are device pointers, row-major, contiguous, 16-byte aligned:
+ *      q, o, dO, dq     bf16 [B, T, Hq,  d]
+ *      k, v, dk, dv     bf16 [B, T, Hkv, d]
+ *      lse              fp32 [B, Hq, T]   natural-log log-sum-exp of each query row
+ *  - d is 64 or 128; Hq % Hkv == 0; B, T, Hq, Hkv >= 1.
+ *  - The caller owns every buffer. The library never allocates device memory;
+ *    it keeps only a per-device status word and a small host-side cache.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *    asynchronous on it and never synchronise.
+ *  - Outputs are overwritten, never accumulated into.
+ *  - Errors: a non-zero gqa_status_t is returned before anything is launched
+ *    when an argument is invalid; attn_last_error() then describes it.
+ *    Kernels never trap: a pipeline wait that exceeds its time budget makes
+ *    the CTA leave cleanly and records GQA_ERR_TIMEOUT in the device status
+ *    word, which attn_sync_status() reports.
+ *  - Requires a device of compute capability 10.3 (GB300).
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int gqa_status_t;
+
+#define GQA_OK 0
+#define GQA_ERR_INVALID_ARG 1       /* null/misaligned pointer, bad shape, d not 64/128, small workspace */
+#define GQA_ERR_UNSUPPORTED_DEVICE 2 /* current device is not compute capability 10.3 */
+#define GQA_ERR_LAUNCH 3            /* a CUDA runtime/driver call or kernel launch failed */
+#define GQA_ERR_TIMEOUT 4           /* a kernel gave up waiting on its pipeline (device status word) */
+
+/*
+ * Forward pass ("A transformer in PTX", §Flash attention).
+ *   q [B,T,Hq,d], k/v [B,T,Hkv,d] bf16 in; o [B,T,Hq,d] bf16 out;
+ *   lse [B,Hq,T] fp32 out (natural log).
+ *   causal != 0: key j is visible to query i iff j <= i; causal == 0: all keys.
+ *   The score scale is 1/sqrt(d).
+ */
+gqa_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int Hq,
+                      int Hkv, int d, int causal, void* stream);
+
+/*
+ * Bytes of scratch the backward needs: two fp32 arrays [B, Hq, T rounded up
+ * to 128] (D_i = rowsum(dO * O) and the LSE in log2 units). The caller
+ * allocates it; nothing in it needs to be initialised or preserved.
+ */
+size_t attn_bwd_workspace_bytes(int B, int T, int Hq);
+
+/*
+ * Backward pass of L = sum(O * dO) ("A transformer in PTX", §The same bits
+ * every time): a rowsum(dO * O) preprocess, then a dQ kernel per block of
+ * queries and a dK/dV kernel per block of keys that loops over the query heads
+ * of its kv head in ascending order.
+ *   q, k, v, o, lse: as produced/consumed by attn_fwd; dO [B,T,Hq,d] bf16 in;
+ *   dq [B,T,Hq,d], dk/dv [B,T,Hkv,d] bf16 out.
+ *   workspace: device memory of at least attn_bwd_workspace_bytes(B,T,Hq)
+ *   bytes, 16-byte aligned, not shared with a concurrent call.
+ * Results are bit-identical from call to call for the same inputs.
+ */
+gqa_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                      int B, int T, int Hq, int Hkv, int d, int causal, void* stream);
+
+/* Description of the last error returned on this host thread ("" if none). */
+const char* attn_last_error(void);
+
+/*
+ * Synchronise `stream`, then read and clear the device status word of the
+ * current device. Returns GQA_OK, GQA_ERR_TIMEOUT (a kernel gave up waiting;
+ * attn_last_error() names the kernel and wait), or GQA_ERR_LAUNCH if the
+ * synchronisation itself failed.
+ */
+gqa_status_t attn_sync_status(void* stream);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier nobody arrives at, with a budget of `budget_ns` nanoseconds, so
+ * the wait must run out, record GQA_ERR_TIMEOUT in the status word and
+ * return. Nothing faults or hangs. Read the result with attn_sync_status().
+ */
+gqa_status_t attn_selftest_timeout(unsigned long long budget_ns, void* stream);
+
+/*
+ * Time budget of every pipeline wait, in nanoseconds (default 2e9). Applies
+ * to launches made after the call, on every device. 0 restores the default.
+ */
+void attn_set_wait_budget_ns(unsigned long long budget_ns);
+
+/* Library version as "major.minor.patch". */
+const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

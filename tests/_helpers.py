@@ -1,0 +1,49 @@
+"""Shared helpers for the GPU parity tests (comparison metrics and guard buffers)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# Tolerances of the GPU path against the f64 oracle:
+#  O: max |gpu - oracle| over all elements; LSE: max abs; dQ/dK/dV: ||gpu - oracle||_F / ||oracle||_F.
+TOL_O = 1e-2
+TOL_LSE = 1e-3
+TOL_GRAD = 1e-2
+
+
+def f64(t) -> np.ndarray:
+    return t.detach().to("cpu").double().numpy()
+
+
+def max_abs(a, r) -> float:
+    return float(np.max(np.abs(a - r))) if a.size else 0.0
+
+
+def rel_fro(a, r) -> float:
+    n = np.linalg.norm(r)
+    return float(np.linalg.norm(a - r) / n) if n > 0 else float(np.linalg.norm(a))
+
+
+def worst_index(a, r):
+    """(index tuple, gpu value, oracle value) of the largest absolute difference."""
+    idx = np.unravel_index(np.argmax(np.abs(a - r)), a.shape)
+    return tuple(int(i) for i in idx), float(a[idx]), float(r[idx])
+
+
+GUARD = 4096  # bytes of guard on each side of a guarded output
+
+
+class Guarded:
+    """A CUDA tensor embedded in a larger buffer whose edges hold a known byte pattern."""
+
+    def __init__(self, shape, dtype, device):
+        n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        self.raw = torch.empty(n + 2 * GUARD, dtype=torch.uint8, device=device)
+        self.raw.fill_(0xA5)
+        self.tensor = self.raw[GUARD:GUARD + n].view(dtype).view(shape)
+        self.n = n
+
+    def intact(self) -> bool:
+        head = self.raw[:GUARD]
+        tail = self.raw[GUARD + self.n:]
+        return bool((head == 0xA5).all().item()) and bool((tail == 0xA5).all().item())

@@ -1,0 +1,83 @@
+"""CPU checks of the C ABI: the library builds for sm_103a, loads, exports every
+function the header declares, and rejects bad arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import causal_gqa_flash_gb300 as gqa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa_attn.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", src))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gqa.build()
+    return gqa.load()
+
+
+def test_header_matches_binding():
+    assert declared_functions() == set(gqa.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(gqa.library_path())
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+def test_version_and_workspace(lib):
+    assert gqa.attn_version() == "0.1.0"
+    # two fp32 arrays [B, Hq, T rounded up to 128]
+    assert gqa.attn_bwd_workspace_bytes(2, 3000, 6) == 2 * 2 * 6 * 3072 * 4
+    assert gqa.attn_bwd_workspace_bytes(1, 128, 1) == 2 * 128 * 4
+    assert gqa.attn_bwd_workspace_bytes(0, 128, 1) == 0
+
+
+FAKE = ctypes.c_void_p(0x100000)      # aligned, never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p(0x100008)
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,d,needle", [
+    (1, 128, 6, 2, 96, "d must be 64 or 128"),
+    (1, 128, 5, 2, 64, "multiple of Hkv"),
+    (1, 0, 6, 2, 64, "positive"),
+    (0, 128, 6, 2, 64, "positive"),
+    (1, 128, 6, 0, 64, "positive"),
+])
+def test_fwd_rejects_bad_shapes(lib, B, T, Hq, Hkv, d, needle):
+    rc = lib.attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, B, T, Hq, Hkv, d, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG
+    assert needle in gqa.attn_last_error()
+
+
+def test_fwd_rejects_null_and_misaligned(lib):
+    rc = lib.attn_fwd(None, FAKE, FAKE, FAKE, FAKE, 1, 128, 6, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "q is NULL" in gqa.attn_last_error()
+    rc = lib.attn_fwd(FAKE, FAKE, MISALIGNED, FAKE, FAKE, 1, 128, 6, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "v is not 16-byte aligned" in gqa.attn_last_error()
+
+
+def test_bwd_rejects_small_workspace(lib):
+    need = gqa.attn_bwd_workspace_bytes(2, 256, 4)
+    args = [FAKE] * 10 + [need - 1, 2, 256, 4, 2, 64, 1, None]
+    rc = lib.attn_bwd(*args)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "workspace_bytes" in gqa.attn_last_error()
+    args = [FAKE] * 9 + [None, need, 2, 256, 4, 2, 64, 1, None]
+    rc = lib.attn_bwd(*args)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "workspace is NULL" in gqa.attn_last_error()
+
+
+def test_last_error_is_cleared_by_next_call(lib):
+    lib.attn_fwd(None, None, None, None, None, 1, 128, 6, 2, 64, 1, None)
+    assert gqa.attn_last_error()
+    lib.attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 6, 2, 96, 1, None)
+    assert "d must be" in gqa.attn_last_error()
