@@ -1,0 +1,430 @@
+#!/usr/bin/env python3
+"""Benchmark of causal grouped-query flash attention, forward + backward, on GB300.
+
+One step = one forward (attn_fwd) and one backward (preprocess, dQ, dK/dV) over
+one batch of the workload, with inputs resident in HBM. The metric is causal
+TFLOP/s of fwd+bwd with the standard count: fwd = 4*B*Hq*T^2*d/2 and
+bwd = 2.5 * fwd (five matmuls; the dQ and dK/dV kernels actually run seven).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on its
+own GPU (the (batch, kv-head) units are independent: no collective is needed);
+the time is the max over ranks and the value is the work of all ranks over it.
+
+--impl reference times the f64 CPU oracle (the only reference this project has)
+on the host cores, on a bounded sample of the same workload.
+
+Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal GQA flash-attn fwd+bwd TFLOP/s (bf16) and % of GB300 dense bf16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="c2", help="c1..c5 (default c2, the trainer's dev-preset shape)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--profile-run", action="store_true",
+                    help="timed steps only (no clock soak, e2e or oracle leg): the command profiled under ncu")
+    return ap.parse_args()
+
+
+def causal_pairs(T: int, causal: bool) -> float:
+    return T * T / 2.0 if causal else float(T * T)
+
+
+def fwd_flops(w) -> float:
+    return 4.0 * w.B * w.Hq * causal_pairs(w.T, w.causal) * w.d
+
+
+def step_flops(w) -> float:
+    return 3.5 * fwd_flops(w)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def config_dict(w, extra=None):
+    d = {"workload": f"{w.name}: {w.describe()}", "B": w.B, "seq_len": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+         "causal": w.causal, "flop_convention": "fwd=4*B*Hq*T^2*d/2, bwd=2.5*fwd"}
+    if extra:
+        d.update(extra)
+    return d
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the GPU is busy."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.bus_id:
+            cmd += ["-i", self.bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_bus_id(torch, dev):
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- traffic record
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "causal_gqa_flash_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "attn_fwd_kernel": ["attn_fwd.cu", "attn_common.cuh", "sm103_ptx.cuh"],
+    "bwd_pre_kernel": ["attn_bwd.cu", "attn_common.cuh", "sm103_ptx.cuh"],
+    "bwd_dq_kernel": ["attn_bwd.cu", "attn_common.cuh", "sm103_ptx.cuh"],
+    "bwd_dkv_kernel": ["attn_bwd.cu", "attn_common.cuh", "sm103_ptx.cuh"],
+}
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(kernel, {}).get(workload)
+    if not ent or ent.get("source_sha256_16") != kernel_source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+def oracle_sample(w, min_seconds: float, max_seconds: float):
+    """Time the f64 oracle (fwd+bwd) on whole (batch, kv-head) groups of the workload."""
+    import oracle
+    from causal_gqa_flash_gb300.inputs import workload_inputs
+
+    q, k, v, dout = workload_inputs(w)
+    G = w.Hq // w.Hkv
+    groups = [(b, kv) for b in range(w.B) for kv in range(w.Hkv)]
+    sl = []
+    for b, kv in groups:
+        hs = slice(kv * G, (kv + 1) * G)
+        sl.append(tuple(x.double().numpy()[b:b + 1, :, s].copy() for x, s in
+                        ((q, hs), (k, slice(kv, kv + 1)), (v, slice(kv, kv + 1)), (dout, hs))))
+    group_flops = 3.5 * 4.0 * 1 * G * causal_pairs(w.T, w.causal) * w.d
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        qs, ks, vs, ds = sl[done % len(sl)]
+        oracle.bwd(qs, ks, vs, ds, causal=w.causal)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or el >= max_seconds:
+            break
+    return {"value": group_flops * done / el / 1e12, "seconds": el, "groups": done,
+            "cores": oracle.max_threads(),
+            "sample": f"{done} (batch, kv-head) groups of {w.name} (each {G} query heads x T={w.T}), "
+                      f"f64 oracle fwd+bwd, {el:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    from causal_gqa_flash_gb300.inputs import workload_inputs
+    q, k, v, dout = workload_inputs(w)
+    G = w.Hq // w.Hkv
+    qs, ks, vs, ds = (x.double().numpy()[0:1, :, s].copy() for x, s in
+                      ((q, slice(0, G)), (k, slice(0, 1)), (v, slice(0, 1)), (dout, slice(0, G))))
+    sample_flops = 3.5 * 4.0 * G * causal_pairs(w.T, w.causal) * w.d
+    for _ in range(args.warmup):
+        oracle.bwd(qs, ks, vs, ds, causal=w.causal)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.bwd(qs, ks, vs, ds, causal=w.causal)
+    el = time.perf_counter() - t0
+    value = sample_flops * args.steps / el / 1e12
+    sample = (f"each step: one (batch, kv-head) group of {w.name} ({G} query heads x T={w.T}), "
+              f"f64 oracle fwd+bwd on the host cores")
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(w, {"sample": "one (batch, kv-head) group per step"}),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import causal_gqa_flash_gb300 as gqa
+    from causal_gqa_flash_gb300.inputs import workload_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    gqa.build()
+    gqa.load()
+    peaks, peak_src = load_peaks()
+
+    q_h, k_h, v_h, do_h = (x.pin_memory() for x in workload_inputs(w))
+    q, k, v, dout = (x.to(dev) for x in (q_h, k_h, v_h, do_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(gqa.attn_bwd_workspace_bytes(w.B, w.T, w.Hq), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    causal = w.causal
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        gqa.attn_fwd(q, k, v, causal=causal, o=o, lse=lse, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        gqa.attn_bwd_preprocess(o, lse, dout, ws, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        gqa.attn_bwd_dq(q, k, v, dout, dq, ws, causal=causal, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        gqa.attn_bwd_dkv(q, k, v, dout, dk, dv, ws, causal=causal, stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if gqa.attn_sync_status(stream) != gqa.GQA_OK:
+        raise RuntimeError(gqa.attn_last_error())
+
+    sampler = ClockSampler(gpu_bus_id(torch, dev)) if rank == 0 and not args.profile_run else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush between timed steps, outside the events
+        step(events[i])
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    # keep the GPU busy with identical untimed steps so the 100 ms clock sampler sees load
+    t_soak = time.perf_counter()
+    while sampler and time.perf_counter() - t_soak < max(0.0, 1.5 - wall):
+        for _ in range(20):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.stop()
+    if gqa.attn_sync_status(stream) != gqa.GQA_OK:
+        raise RuntimeError(gqa.attn_last_error())
+
+    names = ["attn_fwd_kernel", "bwd_pre_kernel", "bwd_dq_kernel", "bwd_dkv_kernel"]
+    per_kernel = {n: sum(events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps))
+                  for j, n in enumerate(names)}
+    step_ms_total = sum(events[i][0].elapsed_time(events[i][4]) for i in range(args.steps))
+    t = torch.tensor([step_ms_total], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    step_ms_total = float(t.item())
+    ms_per_step = step_ms_total / args.steps
+    value = world * step_flops(w) * args.steps / (step_ms_total * 1e-3) / 1e12
+    per_gpu = value / world
+
+    # roofline of the dominant kernel (largest share of the step)
+    pairs = causal_pairs(w.T, w.causal)
+    mm = 2.0 * w.B * w.Hq * pairs * w.d  # one causal matmul over all heads
+    kflops = {"attn_fwd_kernel": 2 * mm, "bwd_dq_kernel": 3 * mm, "bwd_dkv_kernel": 4 * mm}
+    pre_bytes = 2 * w.B * w.T * w.Hq * w.d * 2 + w.B * w.Hq * w.T * 4 + 2 * w.B * w.Hq * w.T * 4
+    dom = max(per_kernel, key=per_kernel.get)
+    avg_ms = per_kernel[dom] / args.steps
+    if dom == "bwd_pre_kernel":
+        achieved = pre_bytes / (avg_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        achieved = kflops[dom] / (avg_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_src} burst" if roof["bound"] == "tensor" else peak_src
+    roof["traffic"] = recorded_traffic(dom, w.name)
+    kernel_ms = {n: per_kernel[n] / args.steps for n in names}
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    dq_h = torch.empty(dq.shape, dtype=dq.dtype, pin_memory=True)
+    dk_h = torch.empty(dk.shape, dtype=dk.dtype, pin_memory=True)
+    dv_h = torch.empty(dv.shape, dtype=dv.dtype, pin_memory=True)
+    h2d = sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h, do_h))
+    d2h = sum(x.numel() * x.element_size() for x in (o_h, lse_h, dq_h, dk_h, dv_h))
+
+    def e2e_step():
+        q.copy_(q_h, non_blocking=True)
+        k.copy_(k_h, non_blocking=True)
+        v.copy_(v_h, non_blocking=True)
+        dout.copy_(do_h, non_blocking=True)
+        gqa.attn_fwd(q, k, v, causal=causal, o=o, lse=lse, stream=stream)
+        gqa.attn_bwd(q, k, v, o, lse, dout, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        dq_h.copy_(dq, non_blocking=True)
+        dk_h.copy_(dk, non_blocking=True)
+        dv_h.copy_(dv, non_blocking=True)
+
+    for _ in range(0 if args.profile_run else 3):
+        e2e_step()
+    e_steps = 0 if args.profile_run else max(3, args.steps // 2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    te = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = world * step_flops(w) * e_steps / (float(te.item()) * 1e-3) / 1e12 if e_steps else None
+
+    cpu = None
+    if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.profile_run):
+        s = oracle_sample(w, min_seconds=10.0, max_seconds=30.0)
+        cpu = {"value": s["value"], "unit": "TFLOP/s", "cores": s["cores"], "kind": "oracle", "sample": s["sample"]}
+
+    if rank == 0:
+        clocks = sampler.summary() if sampler else None
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_dict(w, {"l2": "flushed between timed steps (256 MB write, outside the events)",
+                                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+            "pct_of_peak": 100.0 * per_gpu / peaks["bf16_tflops"],
+            "peak_tflops": peaks["bf16_tflops"], "peak_source": f"{peak_src} burst",
+            "fwd_tflops": fwd_flops(w) / (kernel_ms["attn_fwd_kernel"] * 1e-3) / 1e12,
+            "bwd_tflops": 2.5 * fwd_flops(w) / ((kernel_ms["bwd_pre_kernel"] + kernel_ms["bwd_dq_kernel"]
+                                                 + kernel_ms["bwd_dkv_kernel"]) * 1e-3) / 1e12,
+            "kernel_ms": kernel_ms,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks,
+            "wall_s_timed": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    from causal_gqa_flash_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

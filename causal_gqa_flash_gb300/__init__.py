@@ -15,6 +15,7 @@ from ._build import build, library_path
 
 __all__ = [
     "AttnError", "build", "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
+    "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv",
     "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_last_error", "attn_version",
     "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
     "GQA_ERR_TIMEOUT",
@@ -28,8 +29,8 @@ GQA_ERR_TIMEOUT = 4
 
 # Every function include/gqa_attn.h declares.
 EXPORTED_SYMBOLS = (
-    "attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_last_error", "attn_sync_status",
-    "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_version",
+    "attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv",
+    "attn_last_error", "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_version",
 )
 
 _lib = None
@@ -57,6 +58,12 @@ def load():
     lib.attn_bwd_workspace_bytes.restype = sz
     lib.attn_bwd.argtypes = [vp] * 10 + [sz, i, i, i, i, i, i, vp]
     lib.attn_bwd.restype = i
+    lib.attn_bwd_preprocess.argtypes = [vp, vp, vp, vp, sz, i, i, i, i, vp]
+    lib.attn_bwd_preprocess.restype = i
+    lib.attn_bwd_dq.argtypes = [vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, vp]
+    lib.attn_bwd_dq.restype = i
+    lib.attn_bwd_dkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, vp]
+    lib.attn_bwd_dkv.restype = i
     lib.attn_last_error.argtypes = []
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_sync_status.argtypes = [vp]
@@ -145,10 +152,38 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = True, dq=None, dk=None, dv=No
     need = attn_bwd_workspace_bytes(B, T, Hq)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    ws_bytes = workspace.numel() * workspace.element_size()
+    ws_bytes = _ws_bytes(workspace)
     _check(lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                         _ptr(workspace), ws_bytes, B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
     return dq, dk, dv
+
+
+def _ws_bytes(workspace):
+    return workspace.numel() * workspace.element_size()
+
+
+def attn_bwd_preprocess(o, lse, dout, workspace, stream=None):
+    """Stage 1 of attn_bwd: workspace <- rowsum(dO * O) and LSE * log2(e)."""
+    lib = load()
+    B, T, Hq, d = o.shape
+    _check(lib.attn_bwd_preprocess(_ptr(o), _ptr(lse), _ptr(dout), _ptr(workspace), _ws_bytes(workspace), B, T,
+                                   Hq, d, _stream_handle(stream)))
+
+
+def attn_bwd_dq(q, k, v, dout, dq, workspace, causal: bool = True, stream=None):
+    """Stage 2 of attn_bwd: dq, one CTA per query tile."""
+    lib = load()
+    B, T, Hq, Hkv, d = _dims(q, k)
+    _check(lib.attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(workspace), _ws_bytes(workspace),
+                           B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
+
+
+def attn_bwd_dkv(q, k, v, dout, dk, dv, workspace, causal: bool = True, stream=None):
+    """Stage 3 of attn_bwd: dk and dv, one CTA per key tile looping over the kv head's query heads."""
+    lib = load()
+    B, T, Hq, Hkv, d = _dims(q, k)
+    _check(lib.attn_bwd_dkv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dk), _ptr(dv), _ptr(workspace),
+                            _ws_bytes(workspace), B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
 
 
 def attn_sync_status(stream=None) -> int:

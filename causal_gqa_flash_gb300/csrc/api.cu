@@ -200,28 +200,61 @@ gqa_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, floa
   return GQA_OK;
 }
 
-gqa_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
-                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int T, int Hq,
-                      int Hkv, int d, int causal, void* stream) {
-  const char* fn = "attn_bwd";
-  t_last_error.clear();
+}  // extern "C"
+
+namespace {
+
+// Checks shared by the backward stages; fills the workspace pointers.
+gqa_status_t check_workspace(const char* fn, const void* workspace, size_t workspace_bytes, int B, int T, int Hq,
+                             float** Dvec, float** lse2, int* Tpad) {
   gqa_status_t s;
-  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
-  if ((s = check_ptr(fn, "q", q)) || (s = check_ptr(fn, "k", k)) || (s = check_ptr(fn, "v", v)) ||
-      (s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)) || (s = check_ptr(fn, "dO", dO)) ||
-      (s = check_ptr(fn, "dq", dq)) || (s = check_ptr(fn, "dk", dk)) || (s = check_ptr(fn, "dv", dv)) ||
-      (s = check_ptr(fn, "workspace", workspace)))
-    return s;
+  if ((s = check_ptr(fn, "workspace", workspace))) return s;
   const size_t need = attn_bwd_workspace_bytes(B, T, Hq);
   if (workspace_bytes < need)
     return fail(GQA_ERR_INVALID_ARG, "%s: workspace_bytes %zu < required %zu", fn, workspace_bytes, need);
+  *Tpad = (int)round_up_tile(T);
+  *Dvec = static_cast<float*>(const_cast<void*>(workspace));
+  *lse2 = *Dvec + (size_t)B * Hq * (*Tpad);
+  return GQA_OK;
+}
+
+// Parameters of the dQ and dK/dV kernels (shape, pointers and tensor maps already checked by the caller).
+gqa_status_t make_bwd_params(const char* fn, BwdParams* p, const void* q, const void* k, const void* v,
+                             const void* dO, float* Dvec, float* lse2, int Tpad, int B, int T, int Hq, int Hkv,
+                             int d, int causal, DeviceState* ds) {
+  memset(p, 0, sizeof(*p));
+  gqa_status_t s;
+  if ((s = make_map(fn, "q", &p->tmap_q, q, B, T, Hq, d)) || (s = make_map(fn, "k", &p->tmap_k, k, B, T, Hkv, d)) ||
+      (s = make_map(fn, "v", &p->tmap_v, v, B, T, Hkv, d)) ||
+      (s = make_map(fn, "dO", &p->tmap_do, dO, B, T, Hq, d)))
+    return s;
+  p->Dvec = Dvec;
+  p->lse2 = lse2;
+  p->B = B;
+  p->T = T;
+  p->Hq = Hq;
+  p->Hkv = Hkv;
+  p->G = Hq / Hkv;
+  p->nT = (T + kTile - 1) / kTile;
+  p->Tpad = Tpad;
+  p->causal = causal ? 1 : 0;
+  p->scale = (float)(1.0 / sqrt((double)d));
+  p->scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
+  p->status = ds->status;
+  p->budget_ns = g_budget_ns.load();
+  return GQA_OK;
+}
+
+gqa_status_t bwd_preprocess_impl(const char* fn, const void* o, const float* lse, const void* dO, void* workspace,
+                                 size_t workspace_bytes, int B, int T, int Hq, int d, cudaStream_t st) {
+  gqa_status_t s;
+  if ((s = check_shape(fn, B, T, Hq, 1, d))) return s;
+  if ((s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)) || (s = check_ptr(fn, "dO", dO))) return s;
+  float *Dvec, *lse2;
+  int Tpad;
+  if ((s = check_workspace(fn, workspace, workspace_bytes, B, T, Hq, &Dvec, &lse2, &Tpad))) return s;
   DeviceState* ds = nullptr;
   if ((s = device_state(fn, &ds))) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int Tpad = (int)round_up_tile(T);
-  float* Dvec = static_cast<float*>(workspace);
-  float* lse2 = Dvec + (size_t)B * Hq * Tpad;
-
   BwdPreParams pp;
   pp.o = o;
   pp.dO = dO;
@@ -234,34 +267,84 @@ gqa_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o
   pp.Tpad = Tpad;
   cudaError_t e = launch_bwd_pre(pp, d, st);
   if (e != cudaSuccess) return cuda_fail(fn, "preprocess launch", e);
+  return GQA_OK;
+}
 
-  BwdParams p;
-  memset(&p, 0, sizeof(p));
-  if ((s = make_map(fn, "q", &p.tmap_q, q, B, T, Hq, d)) || (s = make_map(fn, "k", &p.tmap_k, k, B, T, Hkv, d)) ||
-      (s = make_map(fn, "v", &p.tmap_v, v, B, T, Hkv, d)) || (s = make_map(fn, "dO", &p.tmap_do, dO, B, T, Hq, d)))
+// which: 1 = dQ, 2 = dK/dV
+gqa_status_t bwd_main_impl(const char* fn, int which, const void* q, const void* k, const void* v, const void* dO,
+                           void* dq, void* dk, void* dv, const void* workspace, size_t workspace_bytes, int B, int T,
+                           int Hq, int Hkv, int d, int causal, cudaStream_t st) {
+  gqa_status_t s;
+  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
+  if ((s = check_ptr(fn, "q", q)) || (s = check_ptr(fn, "k", k)) || (s = check_ptr(fn, "v", v)) ||
+      (s = check_ptr(fn, "dO", dO)))
     return s;
-  p.Dvec = Dvec;
-  p.lse2 = lse2;
+  if (which == 1 && (s = check_ptr(fn, "dq", dq))) return s;
+  if (which == 2 && ((s = check_ptr(fn, "dk", dk)) || (s = check_ptr(fn, "dv", dv)))) return s;
+  float *Dvec, *lse2;
+  int Tpad;
+  if ((s = check_workspace(fn, workspace, workspace_bytes, B, T, Hq, &Dvec, &lse2, &Tpad))) return s;
+  DeviceState* ds = nullptr;
+  if ((s = device_state(fn, &ds))) return s;
+  BwdParams p;
+  if ((s = make_bwd_params(fn, &p, q, k, v, dO, Dvec, lse2, Tpad, B, T, Hq, Hkv, d, causal, ds))) return s;
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
-  p.B = B;
-  p.T = T;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.G = Hq / Hkv;
-  p.nT = (T + kTile - 1) / kTile;
-  p.Tpad = Tpad;
-  p.causal = causal ? 1 : 0;
-  p.scale = (float)(1.0 / sqrt((double)d));
-  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
-  p.status = ds->status;
-  p.budget_ns = g_budget_ns.load();
-  e = launch_bwd_dq(p, d, st);
-  if (e != cudaSuccess) return cuda_fail(fn, "dQ kernel launch", e);
-  e = launch_bwd_dkv(p, d, st);
-  if (e != cudaSuccess) return cuda_fail(fn, "dK/dV kernel launch", e);
+  cudaError_t e = which == 1 ? launch_bwd_dq(p, d, st) : launch_bwd_dkv(p, d, st);
+  if (e != cudaSuccess) return cuda_fail(fn, which == 1 ? "dQ kernel launch" : "dK/dV kernel launch", e);
   return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status_t attn_bwd_preprocess(const void* o, const float* lse, const void* dO, void* workspace,
+                                 size_t workspace_bytes, int B, int T, int Hq, int d, void* stream) {
+  t_last_error.clear();
+  return bwd_preprocess_impl("attn_bwd_preprocess", o, lse, dO, workspace, workspace_bytes, B, T, Hq, d,
+                             static_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
+                         const void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                         int causal, void* stream) {
+  t_last_error.clear();
+  return bwd_main_impl("attn_bwd_dq", 1, q, k, v, dO, dq, nullptr, nullptr, workspace, workspace_bytes, B, T, Hq,
+                       Hkv, d, causal, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t attn_bwd_dkv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
+                          const void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                          int causal, void* stream) {
+  t_last_error.clear();
+  return bwd_main_impl("attn_bwd_dkv", 2, q, k, v, dO, nullptr, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv,
+                       d, causal, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int T, int Hq,
+                      int Hkv, int d, int causal, void* stream) {
+  const char* fn = "attn_bwd";
+  t_last_error.clear();
+  gqa_status_t s;
+  // Validate everything before the first launch.
+  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
+  if ((s = check_ptr(fn, "q", q)) || (s = check_ptr(fn, "k", k)) || (s = check_ptr(fn, "v", v)) ||
+      (s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)) || (s = check_ptr(fn, "dO", dO)) ||
+      (s = check_ptr(fn, "dq", dq)) || (s = check_ptr(fn, "dk", dk)) || (s = check_ptr(fn, "dv", dv)))
+    return s;
+  float *Dvec, *lse2;
+  int Tpad;
+  if ((s = check_workspace(fn, workspace, workspace_bytes, B, T, Hq, &Dvec, &lse2, &Tpad))) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = bwd_preprocess_impl(fn, o, lse, dO, workspace, workspace_bytes, B, T, Hq, d, st))) return s;
+  if ((s = bwd_main_impl(fn, 1, q, k, v, dO, dq, nullptr, nullptr, workspace, workspace_bytes, B, T, Hq, Hkv, d,
+                         causal, st)))
+    return s;
+  return bwd_main_impl(fn, 2, q, k, v, dO, nullptr, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv, d, causal,
+                       st);
 }
 
 gqa_status_t attn_sync_status(void* stream) {

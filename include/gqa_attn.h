@@ -82,6 +82,27 @@ gqa_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o
                       const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                       int B, int T, int Hq, int Hkv, int d, int causal, void* stream);
 
+/*
+ * The three stages of attn_bwd, callable one by one (attn_bwd is exactly
+ * these three calls in this order on one stream). dQ and dK/dV only read the
+ * workspace, so after the preprocess they may run on two streams.
+ *
+ * attn_bwd_preprocess: workspace <- D_i = rowsum(dO_i * O_i) and LSE_i*log2(e),
+ *   fp32 [B, Hq, T rounded up to 128] each, rows past T set to 0.
+ * attn_bwd_dq:  dq [B,T,Hq,d] <- scale * sum_j dS_ij k_j, one CTA per query tile.
+ * attn_bwd_dkv: dk, dv [B,T,Hkv,d] <- sums over the query heads sharing each kv
+ *   head, one CTA per key tile, heads and query tiles in ascending order.
+ * Arguments mean what they mean in attn_bwd.
+ */
+gqa_status_t attn_bwd_preprocess(const void* o, const float* lse, const void* dO, void* workspace,
+                                 size_t workspace_bytes, int B, int T, int Hq, int d, void* stream);
+gqa_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
+                         const void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                         int causal, void* stream);
+gqa_status_t attn_bwd_dkv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
+                          const void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                          int causal, void* stream);
+
 /* Description of the last error returned on this host thread ("" if none). */
 const char* attn_last_error(void);
 

@@ -19,6 +19,22 @@ def max_abs(a, r) -> float:
     return float(np.max(np.abs(a - r))) if a.size else 0.0
 
 
+def half_ulp_bf16(r: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers at |r| (8 significant bits): the rounding error any bf16 output may carry."""
+    mag = np.maximum(np.abs(r), 2.0 ** -126)
+    return np.ldexp(1.0, np.floor(np.log2(mag)).astype(np.int64) - 8)
+
+
+def o_err(a, r) -> float:
+    """O error beyond the bf16 output's own rounding: max(|a - r| - half_ulp_bf16(r)).
+
+    For |O| in [4, 8) a bf16 value is only known to +-2^-6 = 0.0156, so a plain
+    max-abs bound of 1e-2 is unattainable by any bf16 output there; the O
+    tolerance applies to the error the computation adds on top of that.
+    """
+    return float(np.max(np.abs(a - r) - half_ulp_bf16(r))) if a.size else 0.0
+
+
 def rel_fro(a, r) -> float:
     n = np.linalg.norm(r)
     return float(np.linalg.norm(a - r) / n) if n > 0 else float(np.linalg.norm(a))
