@@ -15,7 +15,7 @@ from ._build import build, library_path
 
 __all__ = [
     "AttnError", "build", "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
-    "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv",
+    "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
     "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_last_error", "attn_version",
     "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
     "GQA_ERR_TIMEOUT",
@@ -26,11 +26,13 @@ GQA_ERR_INVALID_ARG = 1
 GQA_ERR_UNSUPPORTED_DEVICE = 2
 GQA_ERR_LAUNCH = 3
 GQA_ERR_TIMEOUT = 4
+NOALLOC_SCRATCH_BYTES = 8 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_attn.h
 
 # Every function include/gqa_attn.h declares.
 EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv",
-    "attn_last_error", "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_version",
+    "attn_bwd_noalloc", "attn_last_error", "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns",
+    "attn_version",
 )
 
 _lib = None
@@ -64,6 +66,8 @@ def load():
     lib.attn_bwd_dq.restype = i
     lib.attn_bwd_dkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, vp]
     lib.attn_bwd_dkv.restype = i
+    lib.attn_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, i, i, vp]
+    lib.attn_bwd_noalloc.restype = i
     lib.attn_last_error.argtypes = []
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_sync_status.argtypes = [vp]
@@ -184,6 +188,27 @@ def attn_bwd_dkv(q, k, v, dout, dk, dv, workspace, causal: bool = True, stream=N
     B, T, Hq, Hkv, d = _dims(q, k)
     _check(lib.attn_bwd_dkv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dk), _ptr(dv), _ptr(workspace),
                             _ws_bytes(workspace), B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, dout, causal: bool = True, dq=None, dk=None, dv=None, stream=None):
+    """attn_bwd whose scratch is the library's own fixed device array (no workspace argument).
+
+    For callers that may not allocate device memory where they run the backward.
+    Problems needing more than NOALLOC_SCRATCH_BYTES of scratch are rejected;
+    calls that overlap on one GPU race on the shared array.
+    """
+    import torch
+    lib = load()
+    B, T, Hq, Hkv, d = _dims(q, k)
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    _check(lib.attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                _ptr(dv), B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
+    return dq, dk, dv
 
 
 def attn_sync_status(stream=None) -> int:

@@ -48,6 +48,16 @@ using namespace gqa;
 namespace {
 
 thread_local std::string t_last_error;
+
+}  // namespace
+
+namespace gqa {
+// Lets other translation units of the library report through attn_last_error().
+void set_last_error_message(const char* msg) { t_last_error = msg ? msg : ""; }
+}  // namespace gqa
+
+namespace {
+
 std::atomic<unsigned long long> g_budget_ns{2000000000ull};
 constexpr unsigned long long kDefaultBudgetNs = 2000000000ull;
 

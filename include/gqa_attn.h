@@ -103,6 +103,32 @@ gqa_status_t attn_bwd_dkv(const void* q, const void* k, const void* v, const voi
                           const void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
                           int causal, void* stream);
 
+/*
+ * Backward pass that allocates nothing, not even a workspace from the caller.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that may not allocate device memory where they run the backward (a loop
+ * whose device memory is all handed out up front by a pool it does not own,
+ * or a latency-critical loop that avoids cudaMalloc/cudaFree because they can
+ * synchronise the device). Inputs and outputs are still the caller's and mean
+ * what they mean in attn_bwd; the scratch lives in a fixed array of
+ * GQA_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits.
+ *  - Limit: attn_bwd_workspace_bytes(B, T, Hq) must not exceed
+ *    GQA_NOALLOC_SCRATCH_BYTES (B * Hq * roundup(T, 128) <= 1,048,576);
+ *    larger problems get GQA_ERR_INVALID_ARG before anything is launched.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array and it keeps the last call's
+ *    contents. Every element the kernels read is rewritten by the call itself,
+ *    so stale contents do no harm, but two calls whose work overlaps on the
+ *    GPU (different streams, or different host threads on one device) race.
+ */
+#define GQA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+gqa_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dO, void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int d,
+                              int causal, void* stream);
+
 /* Description of the last error returned on this host thread ("" if none). */
 const char* attn_last_error(void);
 

@@ -1,0 +1,58 @@
+"""The backward entry point that allocates nothing (attn_bwd_noalloc).
+
+It is for callers that may not allocate device memory where they run the
+backward, so its scratch is a fixed array inside the library. Called through
+the C ABI twice in a row (different shapes, so the second call meets the
+first call's leftovers in the shared array), its dQ/dK/dV must agree with
+attn_bwd given a caller workspace, within the tolerance of the parity tests.
+This file is collected last on purpose.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import causal_gqa_flash_gb300 as gqa
+from causal_gqa_flash_gb300.inputs import make_inputs
+
+from _helpers import TOL_GRAD, f64, rel_fro
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gqa.build()
+    return gqa.load()
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+@pytest.mark.parametrize("shapes", [[(2, 700, 6, 2, 64, 11), (1, 300, 4, 1, 128, 12)]])
+def test_noalloc_matches_workspace_backward(lib, shapes):
+    for B, T, Hq, Hkv, d, seed in shapes:
+        q, k, v, dout = (x.to(DEV) for x in make_inputs(B, T, Hq, Hkv, d, seed=seed))
+        o, lse = gqa.attn_fwd(q, k, v, causal=True)
+        ref = gqa.attn_bwd(q, k, v, o, lse, dout, causal=True)  # caller-provided workspace
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        rc = lib.attn_bwd_noalloc(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(dout), _p(dq), _p(dk), _p(dv), B, T, Hq,
+                                  Hkv, d, 1, stream)
+        assert rc == gqa.GQA_OK, gqa.attn_last_error()
+        assert gqa.attn_sync_status() == gqa.GQA_OK, gqa.attn_last_error()
+        for name, a, r in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
+            err = rel_fro(f64(a), f64(r))
+            print(f"B={B} T={T} Hq={Hq} Hkv={Hkv} d={d} {name}: rel-F {err:.2e}, identical={torch.equal(a, r)}")
+            assert err <= TOL_GRAD, (name, err)
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(lib):
+    fake = ctypes.c_void_p(0x100000)  # never dereferenced: the size check comes first
+    B, T, Hq = 1, 1 << 17, 16        # needs 2 * 16 * 131072 * 4 bytes = 16 MiB > 8 MiB
+    assert gqa.attn_bwd_workspace_bytes(B, T, Hq) > gqa.NOALLOC_SCRATCH_BYTES
+    rc = lib.attn_bwd_noalloc(*([fake] * 9), B, T, Hq, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG
+    assert "more than the library's fixed" in gqa.attn_last_error()
