@@ -1,7 +1,8 @@
 #!/usr/bin/env python3
 """Benchmark of causal grouped-query flash attention, forward + backward, on GB300.
 
-One step = one forward (attn_fwd) and one backward (preprocess, dQ, dK/dV) over
+One step = one forward (attn_fwd) and one backward (preprocess, then dQ and dK/dV
+in one launch) over
 one batch of the workload, with inputs resident in HBM. The metric is causal
 TFLOP/s of fwd+bwd with the standard count: fwd = 4*B*Hq*T^2*d/2 and
 bwd = 2.5 * fwd (five matmuls; the dQ and dK/dV kernels actually run seven).
@@ -153,8 +154,7 @@ def kernel_source_hash(files):
 KERNEL_SOURCES = {
     "attn_fwd_kernel": ["attn_fwd.cu", "attn_common.cuh", "sm103_ptx.cuh"],
     "bwd_pre_kernel": ["attn_bwd.cu", "attn_common.cuh", "sm103_ptx.cuh"],
-    "bwd_dq_kernel": ["attn_bwd.cu", "attn_common.cuh", "sm103_ptx.cuh"],
-    "bwd_dkv_kernel": ["attn_bwd.cu", "attn_common.cuh", "sm103_ptx.cuh"],
+    "bwd_main_kernel": ["attn_bwd.cu", "attn_common.cuh", "sm103_ptx.cuh"],
 }
 
 
@@ -273,12 +273,9 @@ def run_ours(args, w):
         gqa.attn_bwd_preprocess(o, lse, dout, ws, stream=stream)
         if ev is not None:
             ev[2].record(stream)
-        gqa.attn_bwd_dq(q, k, v, dout, dq, ws, causal=causal, stream=stream)
+        gqa.attn_bwd_dq_dkv(q, k, v, dout, dq, dk, dv, ws, causal=causal, stream=stream)
         if ev is not None:
             ev[3].record(stream)
-        gqa.attn_bwd_dkv(q, k, v, dout, dk, dv, ws, causal=causal, stream=stream)
-        if ev is not None:
-            ev[4].record(stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -290,7 +287,7 @@ def run_ours(args, w):
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -314,10 +311,10 @@ def run_ours(args, w):
     if gqa.attn_sync_status(stream) != gqa.GQA_OK:
         raise RuntimeError(gqa.attn_last_error())
 
-    names = ["attn_fwd_kernel", "bwd_pre_kernel", "bwd_dq_kernel", "bwd_dkv_kernel"]
+    names = ["attn_fwd_kernel", "bwd_pre_kernel", "bwd_main_kernel"]
     per_kernel = {n: sum(events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps))
                   for j, n in enumerate(names)}
-    step_ms_total = sum(events[i][0].elapsed_time(events[i][4]) for i in range(args.steps))
+    step_ms_total = sum(events[i][0].elapsed_time(events[i][3]) for i in range(args.steps))
     t = torch.tensor([step_ms_total], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -329,7 +326,7 @@ def run_ours(args, w):
     # roofline of the dominant kernel (largest share of the step)
     pairs = causal_pairs(w.T, w.causal)
     mm = 2.0 * w.B * w.Hq * pairs * w.d  # one causal matmul over all heads
-    kflops = {"attn_fwd_kernel": 2 * mm, "bwd_dq_kernel": 3 * mm, "bwd_dkv_kernel": 4 * mm}
+    kflops = {"attn_fwd_kernel": 2 * mm, "bwd_main_kernel": 7 * mm}  # dQ tasks 3 matmuls, dK/dV tasks 4
     pre_bytes = 2 * w.B * w.T * w.Hq * w.d * 2 + w.B * w.Hq * w.T * 4 + 2 * w.B * w.Hq * w.T * 4
     dom = max(per_kernel, key=per_kernel.get)
     avg_ms = per_kernel[dom] / args.steps
@@ -400,13 +397,13 @@ def run_ours(args, w):
             "pct_of_peak": 100.0 * per_gpu / peaks["bf16_tflops"],
             "peak_tflops": peaks["bf16_tflops"], "peak_source": f"{peak_src} burst",
             "fwd_tflops": fwd_flops(w) / (kernel_ms["attn_fwd_kernel"] * 1e-3) / 1e12,
-            "bwd_tflops": 2.5 * fwd_flops(w) / ((kernel_ms["bwd_pre_kernel"] + kernel_ms["bwd_dq_kernel"]
-                                                 + kernel_ms["bwd_dkv_kernel"]) * 1e-3) / 1e12,
+            "bwd_tflops": 2.5 * fwd_flops(w) / ((kernel_ms["bwd_pre_kernel"] + kernel_ms["bwd_main_kernel"]) * 1e-3)
+            / 1e12,
             "kernel_ms": kernel_ms,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 3 * args.steps,
             "clocks": clocks,
             "wall_s_timed": wall,
         }

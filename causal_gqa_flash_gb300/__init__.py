@@ -15,7 +15,8 @@ from ._build import build, library_path
 
 __all__ = [
     "AttnError", "build", "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
-    "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_dq_dkv", "attn_bwd_noalloc",
+    "NOALLOC_SCRATCH_BYTES",
     "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_last_error", "attn_version",
     "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
     "GQA_ERR_TIMEOUT",
@@ -31,7 +32,7 @@ NOALLOC_SCRATCH_BYTES = 8 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_attn
 # Every function include/gqa_attn.h declares.
 EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv",
-    "attn_bwd_noalloc", "attn_last_error", "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns",
+    "attn_bwd_dq_dkv", "attn_bwd_noalloc", "attn_last_error", "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns",
     "attn_version",
 )
 
@@ -66,6 +67,8 @@ def load():
     lib.attn_bwd_dq.restype = i
     lib.attn_bwd_dkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, vp]
     lib.attn_bwd_dkv.restype = i
+    lib.attn_bwd_dq_dkv.argtypes = [vp] * 8 + [sz, i, i, i, i, i, i, vp]
+    lib.attn_bwd_dq_dkv.restype = i
     lib.attn_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, i, i, vp]
     lib.attn_bwd_noalloc.restype = i
     lib.attn_last_error.argtypes = []
@@ -188,6 +191,14 @@ def attn_bwd_dkv(q, k, v, dout, dk, dv, workspace, causal: bool = True, stream=N
     B, T, Hq, Hkv, d = _dims(q, k)
     _check(lib.attn_bwd_dkv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dk), _ptr(dv), _ptr(workspace),
                             _ws_bytes(workspace), B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
+
+
+def attn_bwd_dq_dkv(q, k, v, dout, dq, dk, dv, workspace, causal: bool = True, stream=None):
+    """Stages 2+3 of attn_bwd in one launch: dq, dk and dv (heaviest tasks first)."""
+    lib = load()
+    B, T, Hq, Hkv, d = _dims(q, k)
+    _check(lib.attn_bwd_dq_dkv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                               _ws_bytes(workspace), B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
 
 
 def attn_bwd_noalloc(q, k, v, o, lse, dout, causal: bool = True, dq=None, dk=None, dv=None, stream=None):

@@ -280,7 +280,7 @@ gqa_status_t bwd_preprocess_impl(const char* fn, const void* o, const float* lse
   return GQA_OK;
 }
 
-// which: 1 = dQ, 2 = dK/dV
+// which: 1 = dQ tasks, 2 = dK/dV tasks, 3 = both (one launch)
 gqa_status_t bwd_main_impl(const char* fn, int which, const void* q, const void* k, const void* v, const void* dO,
                            void* dq, void* dk, void* dv, const void* workspace, size_t workspace_bytes, int B, int T,
                            int Hq, int Hkv, int d, int causal, cudaStream_t st) {
@@ -289,8 +289,8 @@ gqa_status_t bwd_main_impl(const char* fn, int which, const void* q, const void*
   if ((s = check_ptr(fn, "q", q)) || (s = check_ptr(fn, "k", k)) || (s = check_ptr(fn, "v", v)) ||
       (s = check_ptr(fn, "dO", dO)))
     return s;
-  if (which == 1 && (s = check_ptr(fn, "dq", dq))) return s;
-  if (which == 2 && ((s = check_ptr(fn, "dk", dk)) || (s = check_ptr(fn, "dv", dv)))) return s;
+  if ((which & 1) && (s = check_ptr(fn, "dq", dq))) return s;
+  if ((which & 2) && ((s = check_ptr(fn, "dk", dk)) || (s = check_ptr(fn, "dv", dv)))) return s;
   float *Dvec, *lse2;
   int Tpad;
   if ((s = check_workspace(fn, workspace, workspace_bytes, B, T, Hq, &Dvec, &lse2, &Tpad))) return s;
@@ -301,8 +301,10 @@ gqa_status_t bwd_main_impl(const char* fn, int which, const void* q, const void*
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
-  cudaError_t e = which == 1 ? launch_bwd_dq(p, d, st) : launch_bwd_dkv(p, d, st);
-  if (e != cudaSuccess) return cuda_fail(fn, which == 1 ? "dQ kernel launch" : "dK/dV kernel launch", e);
+  p.n_dkv_tasks = (which & 2) ? B * Hkv * p.nT : 0;
+  p.n_dq_tasks = (which & 1) ? B * Hq * p.nT : 0;
+  cudaError_t e = launch_bwd_main(p, d, st);
+  if (e != cudaSuccess) return cuda_fail(fn, "backward kernel launch", e);
   return GQA_OK;
 }
 
@@ -350,11 +352,15 @@ gqa_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o
   if ((s = check_workspace(fn, workspace, workspace_bytes, B, T, Hq, &Dvec, &lse2, &Tpad))) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if ((s = bwd_preprocess_impl(fn, o, lse, dO, workspace, workspace_bytes, B, T, Hq, d, st))) return s;
-  if ((s = bwd_main_impl(fn, 1, q, k, v, dO, dq, nullptr, nullptr, workspace, workspace_bytes, B, T, Hq, Hkv, d,
-                         causal, st)))
-    return s;
-  return bwd_main_impl(fn, 2, q, k, v, dO, nullptr, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv, d, causal,
-                       st);
+  return bwd_main_impl(fn, 3, q, k, v, dO, dq, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv, d, causal, st);
+}
+
+gqa_status_t attn_bwd_dq_dkv(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk,
+                             void* dv, const void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv,
+                             int d, int causal, void* stream) {
+  t_last_error.clear();
+  return bwd_main_impl("attn_bwd_dq_dkv", 3, q, k, v, dO, dq, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv, d,
+                       causal, static_cast<cudaStream_t>(stream));
 }
 
 gqa_status_t attn_sync_status(void* stream) {
@@ -370,7 +376,7 @@ gqa_status_t attn_sync_status(void* stream) {
   e = cudaMemcpy(&w, ds->status, sizeof(w), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(fn, "cudaMemcpy(status word)", e);
   if (w.code == kDevOk) return GQA_OK;
-  static const char* names[] = {"?", "attn_fwd", "bwd_preprocess", "bwd_dq", "bwd_dkv", "?", "?", "?", "?",
+  static const char* names[] = {"?", "attn_fwd", "bwd_preprocess", "bwd_main", "?", "?", "?", "?", "?",
                                 "selftest"};
   const char* kname = w.kernel < 10 ? names[w.kernel] : "?";
   DevStatusWord zero;

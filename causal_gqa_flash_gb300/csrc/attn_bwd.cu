@@ -10,13 +10,13 @@
 // recompute backward) writes, per query row, D_i = rowsum(dO_i * O_i) and the
 // LSE in log2 units, into the caller's workspace, padded to whole 128-row tiles.
 //
-// Both main kernels use the forward's warp layout: warp 0 TMA, warp 1 tcgen05
-// MMA issue (one thread) and TMEM owner, warps 2-5 one thread per TMEM lane.
-//   dQ kernel (per 128-query tile of one query head), key tiles in ascending order:
+// The dQ and dK/dV passes are two kinds of task of one launch (ordered so the
+// heaviest tasks start first), each task owning its outputs:
+//   dQ task (per 128-query tile of one query head), key tiles in ascending order:
 //     S = Q K^T, dP = dO V^T                  (SS MMAs into TMEM)
 //     P = 2^(S*scale*log2e - LSE2), dS = P (dP - D)   (per row, bf16 into TMEM)
 //     dQ += dS K                              (TS MMA, K as MN-major operand)
-//   dK/dV kernel (per 128-key tile of one kv head), query heads of the group in
+//   dK/dV task (per 128-key tile of one kv head), query heads of the group in
 //   ascending order, query tiles from the diagonal on:
 //     S^T = K Q^T, dP^T = V dO^T              (SS MMAs)
 //     P^T, dS^T per key row                   (bf16 into TMEM)
@@ -27,7 +27,6 @@
 namespace gqa {
 namespace {
 
-constexpr int kBwdThreads = 192;
 constexpr uint32_t kBwdTmemCols = 512;
 // Requesting at least this much dynamic shared memory keeps one CTA per SM,
 // which the 512-column TMEM allocation needs anyway.
@@ -100,303 +99,110 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
 }
 
 // ============================================================================
-// dQ kernel
+// dQ and dK/dV: one launch, two kinds of task.
+//
+// CTA = 10 warps: warp 0 issues TMA, warp 1 issues tcgen05 MMAs and owns TMEM,
+// warps 2-9 are two compute warpgroups; each thread of a warpgroup owns one
+// TMEM lane (one row) and the warpgroup owns half of the 128 score columns.
+// Blocks [0, n_dkv) are dK/dV tasks (one per key tile, kv head, batch; key tile
+// ascending = causal cost descending), blocks [n_dkv, n_dkv + n_dq) are dQ
+// tasks (one per query tile, head, batch; query tile descending). Both kinds
+// need the 512-column TMEM allocation, so one CTA runs per SM, and the
+// heaviest tasks start first.
+//
+// TMEM columns: [0,128) S (dQ) or S^T (dK/dV), fp32; [128,256) dP or dP^T.
+// Warpgroup g writes its bf16 P/dS (64 columns -> 32 packed) over the first
+// half of its own fp32 columns: [g*64, g*64+32) and [128+g*64, 128+g*64+32).
+// [256, 256+D) dQ or dV; [256+D, 256+2D) dK.
 // ============================================================================
+constexpr int kMainThreads = 320;
+constexpr int kComputeThreads = 256;
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColDP = 128;
+constexpr uint32_t kColAcc = 256;
+
 template <int D>
-struct DqCfg {
+struct MainCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = kHalves * kHalfTileBytes;
-  static constexpr int kKStages = 2;
-  static constexpr int kVStages = 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffDO = kOffQ + kTileBytes;
-  static constexpr int kOffK = kOffDO + kTileBytes;
-  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-  static constexpr int kUsed = kOffV + kVStages * kTileBytes + 1024;
+  // dQ task: [Q][dO] then K ring (2) then V ring (2)
+  static constexpr int kDqOffQ = 0;
+  static constexpr int kDqOffDO = kTileBytes;
+  static constexpr int kDqOffK = 2 * kTileBytes;
+  static constexpr int kDqOffV = 4 * kTileBytes;
+  static constexpr int kDqBytes = 6 * kTileBytes;
+  // dK/dV task: [K][V] then 2 stages of [Q][dO][LSE2 x128][D x128]
+  static constexpr int kStageBytes = 2 * kTileBytes + 1024;
+  static constexpr int kKvOffK = 0;
+  static constexpr int kKvOffV = kTileBytes;
+  static constexpr int kKvOffStage = 2 * kTileBytes;
+  static constexpr int kKvBytes = 2 * kTileBytes + 2 * kStageBytes;
+  static constexpr int kUsed = (kDqBytes > kKvBytes ? kDqBytes : kKvBytes) + 1024;
   static constexpr int kSmemBytes = kUsed > kOneCtaPerSmSmem ? kUsed : kOneCtaPerSmSmem;
 };
 
-constexpr uint32_t kDqColS = 0;     // S fp32; dS bf16 aliases [0, 64)
-constexpr uint32_t kDqColDP = 128;  // dP fp32
-constexpr uint32_t kDqColDQ = 256;  // dQ fp32 [128 x D]
+// TMEM column of the bf16 A operand (P, P^T, dS or dS^T) for K-step kk (16 rows
+// of the reduction each); `base` is kColS or kColDP.
+__device__ __forceinline__ uint32_t packed_col(uint32_t base, int kk) {
+  return base + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+}
 
-template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
-  using Cfg = DqCfg<D>;
-  constexpr int KS = Cfg::kKStages;
-  constexpr int VS = Cfg::kVStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  __shared__ uint64_t bar_qdo, bar_kf[KS], bar_ke[KS], bar_vf[VS], bar_ve[VS], bar_s, bar_ds, bar_fin, bar_drain;
-  __shared__ uint32_t tmem_base_sh;
-  __shared__ int abort_sh;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int nbh = p.B * p.Hq;
-  const int qt = p.nT - 1 - static_cast<int>(blockIdx.x) / nbh;  // heaviest first
-  const int bh = static_cast<int>(blockIdx.x) % nbh;
-  const int b = bh / p.Hq;
-  const int h = bh % p.Hq;
-  const int kvh = h / p.G;
-  const int n_kv = p.causal ? qt + 1 : p.nT;
-
-  if (threadIdx.x == 0) {
-    mbar_init(&bar_qdo, 1);
-    for (int s = 0; s < KS; ++s) { mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1); }
-    for (int s = 0; s < VS; ++s) { mbar_init(&bar_vf[s], 1); mbar_init(&bar_ve[s], 1); }
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_ds, 128);
-    mbar_init(&bar_fin, 1);
-    mbar_init(&bar_drain, 1);
-    abort_sh = 0;
-    fence_mbar_init();
+// Store 32 packed bf16x2 columns (two x16 stores).
+__device__ __forceinline__ void tmem_st_packed32(uint32_t taddr, const uint32_t (&v)[32]) {
+  uint32_t a[16], b[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    a[i] = v[i];
+    b[i] = v[16 + i];
   }
-  if (warp == 1) {
-    tmem_alloc(&tmem_base_sh, kBwdTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_base_sh;
-  const WaitCtx ctx{&abort_sh, p.status, p.budget_ns, kKidBwdDq};
+  tmem_st16(taddr, a);
+  tmem_st16(taddr + 16, b);
+}
 
-  if (warp == 0) {
-    if (lane == 0) {
-      tma_prefetch_desc(&p.tmap_q);
-      tma_prefetch_desc(&p.tmap_k);
-      tma_prefetch_desc(&p.tmap_v);
-      tma_prefetch_desc(&p.tmap_do);
-      mbar_arrive_expect_tx(&bar_qdo, 2 * Cfg::kTileBytes);
-      for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-        tma_load_4d(smem + Cfg::kOffQ + hf * kHalfTileBytes, &p.tmap_q, &bar_qdo, hf * 64, h, qt * kTile, b);
-        tma_load_4d(smem + Cfg::kOffDO + hf * kHalfTileBytes, &p.tmap_do, &bar_qdo, hf * 64, h, qt * kTile, b);
-      }
-      int issued_k[KS] = {}, issued_v[VS] = {};
-      bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int ks = j % KS, kn = j / KS;
-        if (kn > 0) ok = mbar_wait(&bar_ke[ks], (kn - 1) & 1, ctx, 1);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bar_kf[ks], Cfg::kTileBytes);
-        for (int hf = 0; hf < Cfg::kHalves; ++hf)
-          tma_load_4d(smem + Cfg::kOffK + ks * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_k, &bar_kf[ks],
-                      hf * 64, kvh, j * kTile, b);
-        issued_k[ks]++;
-        const int vs = j % VS, vn = j / VS;
-        if (vn > 0) ok = mbar_wait(&bar_ve[vs], (vn - 1) & 1, ctx, 2);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bar_vf[vs], Cfg::kTileBytes);
-        for (int hf = 0; hf < Cfg::kHalves; ++hf)
-          tma_load_4d(smem + Cfg::kOffV + vs * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v, &bar_vf[vs],
-                      hf * 64, kvh, j * kTile, b);
-        issued_v[vs]++;
-      }
-      if (ok) {
-        for (int s = 0; s < KS && ok; ++s)
-          if (issued_k[s] > 0) ok = mbar_wait(&bar_ke[s], (issued_k[s] - 1) & 1, ctx, 3);
-        for (int s = 0; s < VS && ok; ++s)
-          if (issued_v[s] > 0) ok = mbar_wait(&bar_ve[s], (issued_v[s] - 1) & 1, ctx, 4);
-      }
-      if (!ok) {
-        mbar_wait_drain(&bar_qdo, 0, p.budget_ns);
-        for (int s = 0; s < KS; ++s)
-          if (issued_k[s] > 0) mbar_wait_drain(&bar_kf[s], (issued_k[s] - 1) & 1, p.budget_ns);
-        for (int s = 0; s < VS; ++s)
-          if (issued_v[s] > 0) mbar_wait_drain(&bar_vf[s], (issued_v[s] - 1) & 1, p.budget_ns);
-      }
+// Store `ncols` (multiple of 32) fp32 columns of this thread's row as bf16 to dst.
+template <int NCOLS>
+__device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* dst, float scale, bool valid) {
+#pragma unroll
+  for (int c = 0; c < NCOLS / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(taddr + c * 32, r);
+    tmem_wait_ld();
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
+    if (valid) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4) d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t idesc_q = idesc_bf16_f32(128, D, 0, 1);
-      const uint32_t sQ = smem_u32(smem + Cfg::kOffQ);
-      const uint32_t sDO = smem_u32(smem + Cfg::kOffDO);
-      const uint32_t sK = smem_u32(smem + Cfg::kOffK);
-      const uint32_t sV = smem_u32(smem + Cfg::kOffV);
-      bool issued = false;
-      auto issue_dq = [&](int jj) -> bool {
-        if (!mbar_wait(&bar_ds, jj & 1, ctx, 12)) return false;
-        tc_fence_after();
-        const int ks = jj % KS;
-        const uint32_t kbase = sK + ks * Cfg::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t bdesc = sdesc_sw128(kbase + kk * 2048, kHalfTileBytes, 1024);
-          mma_ts(tmem + kDqColDQ, tmem + kDqColS + kk * 8, bdesc, idesc_q, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&bar_ke[ks]);
-        return true;
-      };
-      bool ok = mbar_wait(&bar_qdo, 0, ctx, 10);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        if (j > 0) {
-          ok = issue_dq(j - 1);
-          if (!ok) break;
-        }
-        const int ks = j % KS, vs = j % VS;
-        ok = mbar_wait(&bar_kf[ks], (j / KS) & 1, ctx, 11);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kbase = sK + ks * Cfg::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-          mma_ss(tmem + kDqColS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
-        }
-        issued = true;
-        ok = mbar_wait(&bar_vf[vs], (j / VS) & 1, ctx, 13);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t vbase = sV + vs * Cfg::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-          mma_ss(tmem + kDqColDP, sdesc_sw128(sDO + off, 16, 1024), sdesc_sw128(vbase + off, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bar_ve[vs]);
-        mma_commit(&bar_s);
-      }
-      if (ok) ok = issue_dq(n_kv - 1);
-      if (ok) {
-        mma_commit(&bar_fin);
-      } else if (issued) {
-        mma_commit(&bar_drain);
-        mbar_wait_drain(&bar_drain, 0, p.budget_ns);
-      }
-    }
-  } else {
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const int q_idx = qt * kTile + row;
-    const bool valid = q_idx < p.T;
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_base + kDqColS;
-    const uint32_t tDP = tmem + lane_base + kDqColDP;
-    const uint32_t tDQ = tmem + lane_base + kDqColDQ;
-    const size_t vec_idx = (static_cast<size_t>(b) * p.Hq + h) * p.Tpad + q_idx;  // < B*Hq*Tpad
-    const float lse2_r = p.lse2[vec_idx];
-    const float D_r = p.Dvec[vec_idx];
-    const float sl2 = p.scale_log2;
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      ok = warp_wait(&bar_s, j & 1, ctx, 20);
-      if (!ok) break;
-      tc_fence_after();
-      // Columns visible to this row in tile j: [0, lim).
-      int lim = kTile;
-      if (p.causal && j == qt) lim = row + 1;
-      if (!p.causal && (j + 1) * kTile > p.T) lim = p.T - j * kTile;
-      if (!valid) lim = 0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t rs[32], rp[32];
-        tmem_ld32(tS + c * 32, rs);
-        tmem_ld32(tDP + c * 32, rp);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int col = c * 32 + 2 * i;
-          float p0 = ex2_approx(fmaf(__uint_as_float(rs[2 * i]), sl2, -lse2_r));
-          float p1 = ex2_approx(fmaf(__uint_as_float(rs[2 * i + 1]), sl2, -lse2_r));
-          p0 = col < lim ? p0 : 0.f;
-          p1 = col + 1 < lim ? p1 : 0.f;
-          const float ds0 = p0 * (__uint_as_float(rp[2 * i]) - D_r);
-          const float ds1 = p1 * (__uint_as_float(rp[2 * i + 1]) - D_r);
-          pk[i] = pack_bf16x2(ds0, ds1);
-        }
-        tmem_st16(tS + c * 16, pk);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bar_ds);
-    }
-    if (ok) ok = warp_wait(&bar_fin, 0, ctx, 21);
-    if (ok) {
-      tc_fence_after();
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.dq) +
-                           ((static_cast<size_t>(b) * p.T + (valid ? q_idx : 0)) * p.Hq + h) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tDQ + c * 32, r);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * p.scale, __uint_as_float(r[2 * i + 1]) * p.scale);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) {
-    __syncwarp();
-    tmem_dealloc(tmem, kBwdTmemCols);
   }
 }
 
-// ============================================================================
-// dK / dV kernel
-// ============================================================================
 template <int D>
-struct DkvCfg {
-  static constexpr int kHalves = D / 64;
-  static constexpr int kTileBytes = kHalves * kHalfTileBytes;
-  static constexpr int kQStages = 2;
-  // stage = [Q tile][dO tile][LSE2 x128 fp32][D x128 fp32]
-  static constexpr int kStageBytes = 2 * kTileBytes + 1024;
-  static constexpr int kOffK = 0;
-  static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffStage = kOffV + kTileBytes;
-  static constexpr int kUsed = kOffStage + kQStages * kStageBytes + 1024;
-  static constexpr int kSmemBytes = kUsed > kOneCtaPerSmSmem ? kUsed : kOneCtaPerSmSmem;
-};
-
-constexpr uint32_t kDkvColS = 0;     // S^T fp32; P^T bf16 aliases [0, 64)
-constexpr uint32_t kDkvColDP = 128;  // dP^T fp32; dS^T bf16 aliases [128, 192)
-constexpr uint32_t kDkvColDV = 256;  // dV fp32 [128 x D]
-// dK follows dV at 256 + D
-
-template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_constant__ BwdParams p) {
-  using Cfg = DkvCfg<D>;
-  constexpr int QS = Cfg::kQStages;
-  constexpr uint32_t kColDK = kDkvColDV + D;
+__global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
+  using Cfg = MainCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  __shared__ uint64_t bar_kv, bar_qf[QS], bar_qe[QS], bar_s, bar_pds, bar_fin, bar_drain;
+  // Barriers. dQ task: fixed = Q+dO, ring[0..1] = K full/empty, ring[2..3] = V full/empty.
+  // dK/dV task: fixed = K+V, ring[0..1] = stage full/empty.
+  __shared__ uint64_t bar_fixed, bar_full[4], bar_empty[4], bar_s, bar_p, bar_fin, bar_drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nbk = p.B * p.Hkv;
-  const int kt = static_cast<int>(blockIdx.x) / nbk;  // causal cost falls with the key tile: heaviest first
-  const int bk = static_cast<int>(blockIdx.x) % nbk;
-  const int b = bk / p.Hkv;
-  const int kvh = bk % p.Hkv;
-  const int i0 = p.causal ? kt : 0;
-  const int ni = p.nT - i0;        // query tiles per head
-  const int n_it = p.G * ni;       // (head, query tile) pairs, head-major
+  const int n_dkv = p.n_dkv_tasks;
+  const bool is_dkv = static_cast<int>(blockIdx.x) < n_dkv;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar_kv, 1);
-    for (int s = 0; s < QS; ++s) { mbar_init(&bar_qf[s], 1); mbar_init(&bar_qe[s], 1); }
+    mbar_init(&bar_fixed, 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
     mbar_init(&bar_s, 1);
-    mbar_init(&bar_pds, 128);
+    mbar_init(&bar_p, kComputeThreads);
     mbar_init(&bar_fin, 1);
     mbar_init(&bar_drain, 1);
     abort_sh = 0;
@@ -410,91 +216,187 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const WaitCtx ctx{&abort_sh, p.status, p.budget_ns, kKidBwdDkv};
+  const WaitCtx ctx{&abort_sh, p.status, p.budget_ns, kKidBwdMain};
+  constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: N = 128 keys/queries
+  constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);    // gradient MMAs: N = D, B MN-major
+
+  // ---------------------------------------------------------------- task decode
+  int b, kvh, h = 0, tile, n_it;
+  int i0 = 0, ni = 1;  // dK/dV: first query tile and query tiles per head
+  if (is_dkv) {
+    const int nbk = p.B * p.Hkv;
+    tile = static_cast<int>(blockIdx.x) / nbk;
+    const int bk = static_cast<int>(blockIdx.x) % nbk;
+    b = bk / p.Hkv;
+    kvh = bk % p.Hkv;
+    i0 = p.causal ? tile : 0;
+    ni = p.nT - i0;
+    n_it = p.G * ni;
+  } else {
+    const int t = static_cast<int>(blockIdx.x) - n_dkv;
+    const int nbh = p.B * p.Hq;
+    tile = p.nT - 1 - t / nbh;
+    const int bh = t % nbh;
+    b = bh / p.Hq;
+    h = bh % p.Hq;
+    kvh = h / p.G;
+    n_it = p.causal ? tile + 1 : p.nT;
+  }
 
   if (warp == 0) {
+    // ============================================================ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&p.tmap_q);
       tma_prefetch_desc(&p.tmap_k);
       tma_prefetch_desc(&p.tmap_v);
       tma_prefetch_desc(&p.tmap_do);
-      mbar_arrive_expect_tx(&bar_kv, 2 * Cfg::kTileBytes);
-      for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-        tma_load_4d(smem + Cfg::kOffK + hf * kHalfTileBytes, &p.tmap_k, &bar_kv, hf * 64, kvh, kt * kTile, b);
-        tma_load_4d(smem + Cfg::kOffV + hf * kHalfTileBytes, &p.tmap_v, &bar_kv, hf * 64, kvh, kt * kTile, b);
-      }
-      int issued[QS] = {};
+      int issued[4] = {0, 0, 0, 0};
       bool ok = true;
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int st = it % QS, n = it / QS;
-        if (n > 0) ok = mbar_wait(&bar_qe[st], (n - 1) & 1, ctx, 1);
-        if (!ok) break;
-        const int h = kvh * p.G + it / ni;
-        const int qt = i0 + it % ni;
-        uint8_t* stage = smem + Cfg::kOffStage + st * Cfg::kStageBytes;
-        mbar_arrive_expect_tx(&bar_qf[st], 2 * Cfg::kTileBytes + 1024);
+      if (is_dkv) {
+        mbar_arrive_expect_tx(&bar_fixed, 2 * Cfg::kTileBytes);
         for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-          tma_load_4d(stage + hf * kHalfTileBytes, &p.tmap_q, &bar_qf[st], hf * 64, h, qt * kTile, b);
-          tma_load_4d(stage + Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_do, &bar_qf[st], hf * 64, h,
-                      qt * kTile, b);
+          tma_load_4d(smem + Cfg::kKvOffK + hf * kHalfTileBytes, &p.tmap_k, &bar_fixed, hf * 64, kvh, tile * kTile, b);
+          tma_load_4d(smem + Cfg::kKvOffV + hf * kHalfTileBytes, &p.tmap_v, &bar_fixed, hf * 64, kvh, tile * kTile, b);
         }
-        const size_t vec = (static_cast<size_t>(b) * p.Hq + h) * p.Tpad + static_cast<size_t>(qt) * kTile;
-        bulk_load(stage + 2 * Cfg::kTileBytes, p.lse2 + vec, 512, &bar_qf[st]);
-        bulk_load(stage + 2 * Cfg::kTileBytes + 512, p.Dvec + vec, 512, &bar_qf[st]);
-        issued[st]++;
+        for (int it = 0; it < n_it && ok; ++it) {
+          const int st = it & 1, n = it >> 1;
+          if (n > 0) ok = mbar_wait(&bar_empty[st], (n - 1) & 1, ctx, 1);
+          if (!ok) break;
+          const int hq = kvh * p.G + it / ni;
+          const int qt = i0 + it % ni;
+          uint8_t* stage = smem + Cfg::kKvOffStage + st * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(&bar_full[st], 2 * Cfg::kTileBytes + 1024);
+          for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+            tma_load_4d(stage + hf * kHalfTileBytes, &p.tmap_q, &bar_full[st], hf * 64, hq, qt * kTile, b);
+            tma_load_4d(stage + Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_do, &bar_full[st], hf * 64, hq,
+                        qt * kTile, b);
+          }
+          const size_t vec = (static_cast<size_t>(b) * p.Hq + hq) * p.Tpad + static_cast<size_t>(qt) * kTile;
+          bulk_load(stage + 2 * Cfg::kTileBytes, p.lse2 + vec, 512, &bar_full[st]);
+          bulk_load(stage + 2 * Cfg::kTileBytes + 512, p.Dvec + vec, 512, &bar_full[st]);
+          issued[st]++;
+        }
+      } else {
+        mbar_arrive_expect_tx(&bar_fixed, 2 * Cfg::kTileBytes);
+        for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+          tma_load_4d(smem + Cfg::kDqOffQ + hf * kHalfTileBytes, &p.tmap_q, &bar_fixed, hf * 64, h, tile * kTile, b);
+          tma_load_4d(smem + Cfg::kDqOffDO + hf * kHalfTileBytes, &p.tmap_do, &bar_fixed, hf * 64, h, tile * kTile, b);
+        }
+        for (int j = 0; j < n_it && ok; ++j) {
+          const int st = j & 1, n = j >> 1;
+          if (n > 0) ok = mbar_wait(&bar_empty[st], (n - 1) & 1, ctx, 1);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bar_full[st], Cfg::kTileBytes);
+          for (int hf = 0; hf < Cfg::kHalves; ++hf)
+            tma_load_4d(smem + Cfg::kDqOffK + st * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_k, &bar_full[st],
+                        hf * 64, kvh, j * kTile, b);
+          issued[st]++;
+          if (n > 0) ok = mbar_wait(&bar_empty[2 + st], (n - 1) & 1, ctx, 2);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bar_full[2 + st], Cfg::kTileBytes);
+          for (int hf = 0; hf < Cfg::kHalves; ++hf)
+            tma_load_4d(smem + Cfg::kDqOffV + st * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v,
+                        &bar_full[2 + st], hf * 64, kvh, j * kTile, b);
+          issued[2 + st]++;
+        }
       }
-      if (ok) {
-        for (int s = 0; s < QS && ok; ++s)
-          if (issued[s] > 0) ok = mbar_wait(&bar_qe[s], (issued[s] - 1) & 1, ctx, 3);
-      }
+      // Wait until every stage is released, so no MMA commit arrives after exit.
+      for (int s = 0; s < 4 && ok; ++s)
+        if (issued[s] > 0) ok = mbar_wait(&bar_empty[s], (issued[s] - 1) & 1, ctx, 3);
       if (!ok) {
-        mbar_wait_drain(&bar_kv, 0, p.budget_ns);
-        for (int s = 0; s < QS; ++s)
-          if (issued[s] > 0) mbar_wait_drain(&bar_qf[s], (issued[s] - 1) & 1, p.budget_ns);
+        mbar_wait_drain(&bar_fixed, 0, p.budget_ns);
+        for (int s = 0; s < 4; ++s)
+          if (issued[s] > 0) mbar_wait_drain(&bar_full[s], (issued[s] - 1) & 1, p.budget_ns);
       }
     }
   } else if (warp == 1) {
+    // ============================================================ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);
-      const uint32_t sK = smem_u32(smem + Cfg::kOffK);
-      const uint32_t sV = smem_u32(smem + Cfg::kOffV);
-      const uint32_t sStage = smem_u32(smem + Cfg::kOffStage);
       bool issued = false;
-      bool ok = mbar_wait(&bar_kv, 0, ctx, 10);
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int st = it % QS;
-        ok = mbar_wait(&bar_qf[st], (it / QS) & 1, ctx, 11);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t sQ = sStage + st * Cfg::kStageBytes;
-        const uint32_t sDO = sQ + Cfg::kTileBytes;
+      bool ok = mbar_wait(&bar_fixed, 0, ctx, 10);
+      if (is_dkv) {
+        const uint32_t sK = smem_u32(smem + Cfg::kKvOffK);
+        const uint32_t sV = smem_u32(smem + Cfg::kKvOffV);
+        for (int it = 0; it < n_it && ok; ++it) {
+          const int st = it & 1;
+          ok = mbar_wait(&bar_full[st], (it >> 1) & 1, ctx, 11);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sQ = smem_u32(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes);
+          const uint32_t sDO = sQ + Cfg::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-          mma_ss(tmem + kDkvColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
-        }
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
+            mma_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idesc_s,
+                   kk > 0 ? 1u : 0u);
+          }
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-          mma_ss(tmem + kDkvColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
-        }
-        issued = true;
-        mma_commit(&bar_s);
-        ok = mbar_wait(&bar_pds, it & 1, ctx, 12);
-        if (!ok) break;
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
+            mma_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), idesc_s,
+                   kk > 0 ? 1u : 0u);
+          }
+          issued = true;
+          mma_commit(&bar_s);
+          ok = mbar_wait(&bar_p, it & 1, ctx, 12);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + kDkvColDV, tmem + kDkvColS + kk * 8, sdesc_sw128(sDO + kk * 2048, kHalfTileBytes, 1024),
-                 idesc_g, acc);
-          mma_ts(tmem + kColDK, tmem + kDkvColDP + kk * 8, sdesc_sw128(sQ + kk * 2048, kHalfTileBytes, 1024),
-                 idesc_g, acc);
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+            mma_ts(tmem + kColAcc, tmem + packed_col(kColS, kk),
+                   sdesc_sw128(sDO + kk * 2048, kHalfTileBytes, 1024), idesc_g, acc);
+            mma_ts(tmem + kColAcc + D, tmem + packed_col(kColDP, kk),
+                   sdesc_sw128(sQ + kk * 2048, kHalfTileBytes, 1024), idesc_g, acc);
+          }
+          mma_commit(&bar_empty[st]);
         }
-        mma_commit(&bar_qe[st]);
+      } else {
+        const uint32_t sQ = smem_u32(smem + Cfg::kDqOffQ);
+        const uint32_t sDO = smem_u32(smem + Cfg::kDqOffDO);
+        auto issue_dq = [&](int jj) -> bool {
+          if (!mbar_wait(&bar_p, jj & 1, ctx, 12)) return false;
+          tc_fence_after();
+          const int st = jj & 1;
+          const uint32_t kbase = smem_u32(smem + Cfg::kDqOffK + st * Cfg::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tmem + kColAcc, tmem + packed_col(kColS, kk), sdesc_sw128(kbase + kk * 2048, kHalfTileBytes, 1024),
+                   idesc_g, (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bar_empty[st]);
+          return true;
+        };
+        for (int j = 0; j < n_it && ok; ++j) {
+          if (j > 0) {
+            ok = issue_dq(j - 1);
+            if (!ok) break;
+          }
+          const int st = j & 1;
+          ok = mbar_wait(&bar_full[st], (j >> 1) & 1, ctx, 11);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kbase = smem_u32(smem + Cfg::kDqOffK + st * Cfg::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
+            mma_ss(tmem + kColS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), idesc_s,
+                   kk > 0 ? 1u : 0u);
+          }
+          issued = true;
+          ok = mbar_wait(&bar_full[2 + st], (j >> 1) & 1, ctx, 13);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t vbase = smem_u32(smem + Cfg::kDqOffV + st * Cfg::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
+            mma_ss(tmem + kColDP, sdesc_sw128(sDO + off, 16, 1024), sdesc_sw128(vbase + off, 16, 1024), idesc_s,
+                   kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar_empty[2 + st]);
+          mma_commit(&bar_s);
+        }
+        if (ok) ok = issue_dq(n_it - 1);
       }
       if (ok) {
         mma_commit(&bar_fin);
@@ -504,88 +406,139 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkv_kernel(const __grid_co
       }
     }
   } else {
+    // ============================================================ compute warpgroups
+    const int wg = (warp - 2) >> 2;  // 0 or 1: score columns [wg*64, wg*64+64)
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;   // key row within the tile
-    const int k_idx = kt * kTile + row;
+    const int row = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_base + kDkvColS;
-    const uint32_t tDP = tmem + lane_base + kDkvColDP;
-    const float sl2 = p.scale_log2;
+    const uint32_t tS = tmem + lane_base + kColS + wg * 64;
+    const uint32_t tDP = tmem + lane_base + kColDP + wg * 64;
+    const uint64_t sl2x2 = f2_make(p.scale_log2, p.scale_log2);
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int st = it % QS;
-      const int qt = i0 + it % ni;
-      ok = warp_wait(&bar_s, it & 1, ctx, 20);
-      if (!ok) break;
-      ok = warp_wait(&bar_qf[st], (it / QS) & 1, ctx, 22);  // LSE2/D vectors of this stage
-      if (!ok) break;
-      tc_fence_after();
-      const float* vlse2 = reinterpret_cast<const float*>(smem + Cfg::kOffStage + st * Cfg::kStageBytes +
-                                                          2 * Cfg::kTileBytes);
-      const float* vD = vlse2 + kTile;
-      // Query columns visible to this key row in tile qt: [lo, hi).
-      int lo = 0;
-      int hi = p.T - qt * kTile;
-      if (hi > kTile) hi = kTile;
-      if (p.causal && qt == kt) lo = row;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t rs[32], rp[32];
-        tmem_ld32(tS + c * 32, rs);
-        tmem_ld32(tDP + c * 32, rp);
+    if (is_dkv) {
+      const int k_idx = tile * kTile + row;
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it & 1;
+        const int qt = i0 + it % ni;
+        ok = warp_wait(&bar_s, it & 1, ctx, 20);
+        if (!ok) break;
+        ok = warp_wait(&bar_full[st], (it >> 1) & 1, ctx, 22);  // LSE2 / D vectors of this stage
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t rs[64], rp[64];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
+        tmem_ld32(tDP, *reinterpret_cast<uint32_t(*)[32]>(&rp[0]));
+        tmem_ld32(tDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&rp[32]));
         tmem_wait_ld();
-        uint32_t pk[16], dk[16];
+        const float* vl = reinterpret_cast<const float*>(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes +
+                                                         2 * Cfg::kTileBytes) + wg * 64;
+        const float* vd = vl + kTile;
+        // Query columns visible to this key row: [lo, hi) relative to this warpgroup's 64 columns.
+        const int hi_tile = min(kTile, p.T - qt * kTile);
+        const bool masked = (p.causal && qt == tile) || hi_tile < kTile;
+        const int lo = ((p.causal && qt == tile) ? row : 0) - wg * 64;
+        const int hi = hi_tile - wg * 64;
+        uint32_t pk[32], dk[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int col = c * 32 + 2 * i;
-          float p0 = ex2_approx(fmaf(__uint_as_float(rs[2 * i]), sl2, -vlse2[col]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(rs[2 * i + 1]), sl2, -vlse2[col + 1]));
-          p0 = (col >= lo && col < hi) ? p0 : 0.f;
-          p1 = (col + 1 >= lo && col + 1 < hi) ? p1 : 0.f;
-          const float ds0 = p0 * (__uint_as_float(rp[2 * i]) - vD[col]);
-          const float ds1 = p1 * (__uint_as_float(rp[2 * i + 1]) - vD[col + 1]);
-          pk[i] = pack_bf16x2(p0, p1);
-          dk[i] = pack_bf16x2(ds0, ds1);
+        for (int i = 0; i < 32; i += 2) {
+          const float4 l4 = *reinterpret_cast<const float4*>(vl + 2 * i);
+          const float4 d4 = *reinterpret_cast<const float4*>(vd + 2 * i);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = 2 * (i + u);
+            const float la = u ? l4.z : l4.x, lb = u ? l4.w : l4.y;
+            const float da = u ? d4.z : d4.x, db = u ? d4.w : d4.y;
+            const uint64_t sarg = f2_fma(f2_make(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])), sl2x2,
+                                         f2_make(-la, -lb));
+            float a0, a1;
+            f2_split(sarg, a0, a1);
+            float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            if (masked) {
+              p0 = (c >= lo && c < hi) ? p0 : 0.f;
+              p1 = (c + 1 >= lo && c + 1 < hi) ? p1 : 0.f;
+            }
+            const uint64_t pp = f2_make(p0, p1);
+            const uint64_t ds = f2_mul(pp, f2_sub(f2_make(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])),
+                                                  f2_make(da, db)));
+            float d0, d1;
+            f2_split(ds, d0, d1);
+            pk[i + u] = pack_bf16x2(p0, p1);
+            dk[i + u] = pack_bf16x2(d0, d1);
+          }
         }
-        tmem_st16(tS + c * 16, pk);
-        tmem_st16(tDP + c * 16, dk);
+        tmem_st_packed32(tS, pk);
+        tmem_st_packed32(tDP, dk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar_p);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bar_pds);
-    }
-    if (ok) ok = warp_wait(&bar_fin, 0, ctx, 21);
-    if (ok) {
-      tc_fence_after();
-      const bool valid = k_idx < p.T;
-      const size_t off = ((static_cast<size_t>(b) * p.T + (valid ? k_idx : 0)) * p.Hkv + kvh) * D;
-      __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dv) + off;
-      __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dk) + off;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        uint32_t pk[16];
-        tmem_ld32(tmem + lane_base + kDkvColDV + c * 32, r);
+      if (ok) ok = warp_wait(&bar_fin, 0, ctx, 21);
+      if (ok) {
+        tc_fence_after();
+        const bool valid = k_idx < p.T;
+        const size_t off = ((static_cast<size_t>(b) * p.T + (valid ? k_idx : 0)) * p.Hkv + kvh) * D;
+        if (wg == 0)
+          store_row_bf16<D>(tmem + lane_base + kColAcc, reinterpret_cast<__nv_bfloat16*>(p.dv) + off, 1.f, valid);
+        else
+          store_row_bf16<D>(tmem + lane_base + kColAcc + D, reinterpret_cast<__nv_bfloat16*>(p.dk) + off, p.scale,
+                            valid);
+      }
+    } else {
+      const int q_idx = tile * kTile + row;
+      const bool valid = q_idx < p.T;
+      const size_t vec_idx = (static_cast<size_t>(b) * p.Hq + h) * p.Tpad + q_idx;  // < B*Hq*Tpad
+      const float lse2_r = p.lse2[vec_idx];
+      const float D_r = p.Dvec[vec_idx];
+      const uint64_t neg_l2 = f2_make(-lse2_r, -lse2_r);
+      const uint64_t Dx2 = f2_make(D_r, D_r);
+      for (int j = 0; j < n_it; ++j) {
+        ok = warp_wait(&bar_s, j & 1, ctx, 20);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t rs[64], rp[64];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
+        tmem_ld32(tDP, *reinterpret_cast<uint32_t(*)[32]>(&rp[0]));
+        tmem_ld32(tDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&rp[32]));
         tmem_wait_ld();
+        // Key columns visible to this query row: [0, lim) relative to this warpgroup's 64 columns.
+        int lim_tile = kTile;
+        if (p.causal && j == tile) lim_tile = row + 1;
+        if (!p.causal && (j + 1) * kTile > p.T) lim_tile = p.T - j * kTile;
+        const bool masked = (p.causal && j == tile) || (!p.causal && (j + 1) * kTile > p.T) ||
+                            (tile + 1) * kTile > p.T;
+        const int lim = (valid ? lim_tile : 0) - wg * 64;
+        uint32_t dk[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(dv_row + c * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        for (int i = 0; i < 32; ++i) {
+          const int c = 2 * i;
+          const uint64_t sarg =
+              f2_fma(f2_make(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])), sl2x2, neg_l2);
+          float a0, a1;
+          f2_split(sarg, a0, a1);
+          float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+          if (masked) {
+            p0 = c < lim ? p0 : 0.f;
+            p1 = c + 1 < lim ? p1 : 0.f;
+          }
+          const uint64_t ds =
+              f2_mul(f2_make(p0, p1), f2_sub(f2_make(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])), Dx2));
+          float d0, d1;
+          f2_split(ds, d0, d1);
+          dk[i] = pack_bf16x2(d0, d1);
         }
-        tmem_ld32(tmem + lane_base + kColDK + c * 32, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * p.scale, __uint_as_float(r[2 * i + 1]) * p.scale);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(dk_row + c * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-        }
+        tmem_st_packed32(tS, dk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar_p);
+      }
+      if (ok) ok = warp_wait(&bar_fin, 0, ctx, 21);
+      if (ok) {
+        tc_fence_after();
+        const size_t off = ((static_cast<size_t>(b) * p.T + (valid ? q_idx : 0)) * p.Hq + h) * D;
+        store_row_bf16<D / 2>(tmem + lane_base + kColAcc + wg * (D / 2),
+                              reinterpret_cast<__nv_bfloat16*>(p.dq) + off + wg * (D / 2), p.scale, valid);
       }
     }
   }
@@ -628,28 +581,16 @@ cudaError_t launch_bwd_pre(const BwdPreParams& p, int d, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dq(const BwdParams& p, int d, cudaStream_t stream) {
-  const unsigned grid = static_cast<unsigned>(p.B) * p.Hq * p.nT;
+cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>(p.n_dkv_tasks + p.n_dq_tasks);
+  if (grid == 0) return cudaSuccess;
   cudaError_t e;
   if (d == 64) {
-    if ((e = ensure_smem_attr(bwd_dq_kernel<64>, DqCfg<64>::kSmemBytes, 0)) != cudaSuccess) return e;
-    bwd_dq_kernel<64><<<grid, kBwdThreads, DqCfg<64>::kSmemBytes, stream>>>(p);
+    if ((e = ensure_smem_attr(bwd_main_kernel<64>, MainCfg<64>::kSmemBytes, 0)) != cudaSuccess) return e;
+    bwd_main_kernel<64><<<grid, kMainThreads, MainCfg<64>::kSmemBytes, stream>>>(p);
   } else {
-    if ((e = ensure_smem_attr(bwd_dq_kernel<128>, DqCfg<128>::kSmemBytes, 1)) != cudaSuccess) return e;
-    bwd_dq_kernel<128><<<grid, kBwdThreads, DqCfg<128>::kSmemBytes, stream>>>(p);
-  }
-  return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_dkv(const BwdParams& p, int d, cudaStream_t stream) {
-  const unsigned grid = static_cast<unsigned>(p.B) * p.Hkv * p.nT;
-  cudaError_t e;
-  if (d == 64) {
-    if ((e = ensure_smem_attr(bwd_dkv_kernel<64>, DkvCfg<64>::kSmemBytes, 2)) != cudaSuccess) return e;
-    bwd_dkv_kernel<64><<<grid, kBwdThreads, DkvCfg<64>::kSmemBytes, stream>>>(p);
-  } else {
-    if ((e = ensure_smem_attr(bwd_dkv_kernel<128>, DkvCfg<128>::kSmemBytes, 3)) != cudaSuccess) return e;
-    bwd_dkv_kernel<128><<<grid, kBwdThreads, DkvCfg<128>::kSmemBytes, stream>>>(p);
+    if ((e = ensure_smem_attr(bwd_main_kernel<128>, MainCfg<128>::kSmemBytes, 1)) != cudaSuccess) return e;
+    bwd_main_kernel<128><<<grid, kMainThreads, MainCfg<128>::kSmemBytes, stream>>>(p);
   }
   return cudaGetLastError();
 }

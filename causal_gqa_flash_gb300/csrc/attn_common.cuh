@@ -19,8 +19,7 @@ constexpr int kHalfTileBytes = kTile * 128;
 enum KernelId : unsigned int {
   kKidFwd = 1,
   kKidBwdPre = 2,
-  kKidBwdDq = 3,
-  kKidBwdDkv = 4,
+  kKidBwdMain = 3,
   kKidSelfTest = 9,
 };
 
@@ -61,6 +60,8 @@ struct BwdParams {
   void* dv;            // [B,T,Hkv,d]
   int B, T, Hq, Hkv, G, nT, Tpad;
   int causal;
+  int n_dkv_tasks;     // blocks [0, n_dkv_tasks) compute dK/dV (0 = none)
+  int n_dq_tasks;      // the next n_dq_tasks blocks compute dQ (0 = none)
   float scale;         // 1/sqrt(d)
   float scale_log2;    // scale * log2(e)
   DevStatusWord* status;
@@ -74,8 +75,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // Host-side launchers (defined next to their kernels).
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, int d, cudaStream_t stream);
-cudaError_t launch_bwd_dq(const BwdParams& p, int d, cudaStream_t stream);
-cudaError_t launch_bwd_dkv(const BwdParams& p, int d, cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_selftest_timeout(DevStatusWord* status, unsigned long long budget_ns, cudaStream_t stream);
 
 }  // namespace gqa

@@ -83,9 +83,10 @@ gqa_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o
                       int B, int T, int Hq, int Hkv, int d, int causal, void* stream);
 
 /*
- * The three stages of attn_bwd, callable one by one (attn_bwd is exactly
- * these three calls in this order on one stream). dQ and dK/dV only read the
- * workspace, so after the preprocess they may run on two streams.
+ * The stages of attn_bwd, callable one by one: attn_bwd is exactly
+ * attn_bwd_preprocess followed by attn_bwd_dq_dkv on one stream. The dQ and
+ * dK/dV passes only read the workspace; attn_bwd_dq_dkv runs both in one
+ * launch (heaviest tasks first), attn_bwd_dq and attn_bwd_dkv run one each.
  *
  * attn_bwd_preprocess: workspace <- D_i = rowsum(dO_i * O_i) and LSE_i*log2(e),
  *   fp32 [B, Hq, T rounded up to 128] each, rows past T set to 0.
@@ -102,6 +103,9 @@ gqa_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const void
 gqa_status_t attn_bwd_dkv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
                           const void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
                           int causal, void* stream);
+gqa_status_t attn_bwd_dq_dkv(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk,
+                             void* dv, const void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv,
+                             int d, int causal, void* stream);
 
 /*
  * Backward pass that allocates nothing, not even a workspace from the caller.
