@@ -8,7 +8,8 @@
 //
 // Before them, a preprocess pass (not on the page; the standard companion of a
 // recompute backward) writes, per query row, D_i = rowsum(dO_i * O_i) and the
-// LSE in log2 units, into the caller's workspace, padded to whole 128-row tiles.
+// negated LSE in log2 units, into the caller's workspace, padded to whole
+// 128-row tiles.
 //
 // The dQ and dK/dV passes are two kinds of task of one launch (ordered so the
 // heaviest tasks start first), each task owning its outputs:
@@ -49,7 +50,7 @@ __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x <
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
 // ============================================================================
-// Preprocess: D = rowsum(dO * O), LSE2 = LSE * log2(e); padded rows get 0.
+// Preprocess: D = rowsum(dO * O), -LSE2 = -LSE * log2(e); padded rows get 0.
 // Rows are visited in memory order (b, t, h); D/8 threads read one row with
 // 16-byte loads, so a warp reads contiguous bytes.
 // ============================================================================
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
     const int b = static_cast<int>(bt / p.T);
     const size_t idx = (static_cast<size_t>(b) * p.Hq + h) * p.Tpad + t;
     p.Dvec[idx] = acc;
-    p.lse2[idx] = p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.T + t] * 1.4426950408889634f;
+    p.lse2[idx] = -p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.T + t] * 1.4426950408889634f;
   }
   // Zero the padding rows [T, Tpad) of every (b, h).
   const int pad = p.Tpad - p.T;
@@ -102,62 +103,65 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
 // dQ and dK/dV: one launch, two kinds of task.
 //
 // CTA = 10 warps: warp 0 issues TMA, warp 1 issues tcgen05 MMAs and owns TMEM,
-// warps 2-9 are two compute warpgroups; each thread of a warpgroup owns one
-// TMEM lane (one row) and the warpgroup owns half of the 128 score columns.
-// Blocks [0, n_dkv) are dK/dV tasks (one per key tile, kv head, batch; key tile
-// ascending = causal cost descending), blocks [n_dkv, n_dkv + n_dq) are dQ
-// tasks (one per query tile, head, batch; query tile descending). Both kinds
-// need the 512-column TMEM allocation, so one CTA runs per SM, and the
-// heaviest tasks start first.
+// warps 2-9 are two compute warpgroups. Each compute thread owns one TMEM lane
+// (one row) and its warpgroup owns half of the 128 score columns, processed in
+// four rounds of 16 columns whose TMEM loads are software-pipelined (the next
+// round is in flight while this one is computed).
 //
-// TMEM columns: [0,128) S (dQ) or S^T (dK/dV), fp32; [128,256) dP or dP^T.
-// Warpgroup g writes its bf16 P/dS (64 columns -> 32 packed) over the first
-// half of its own fp32 columns: [g*64, g*64+32) and [128+g*64, 128+g*64+32).
-// [256, 256+D) dQ or dV; [256+D, 256+2D) dK.
+// Blocks [0, n_dkv) are dK/dV tasks (one per key tile, kv head, batch; key tile
+// ascending = causal cost descending); the following n_dq blocks are dQ tasks
+// (query tile descending). Both kinds allocate all 512 TMEM columns, so one CTA
+// runs per SM and the heaviest tasks start first.
+//
+// Pipeline per iteration `it` (one 128x128 score tile):
+//   MMA:     S(it+1) into the other S buffer | dP(it+1) once compute(it) has
+//            read dP(it) | gradient MMAs of `it` once compute(it) is done.
+//   compute: read S(it), dP(it) -> P = 2^(S*scale*log2e - LSE2), dS = P(dP - D)
+//            -> bf16 P and dS written back over the 16 S columns of each round.
+// so the tensor core works on iteration it+1 while iteration it is computed.
+// With one S buffer (dK/dV at d = 128, where dV and dK take 256 columns) only
+// dP(it+1) overlaps compute(it).
+//
+// TMEM columns (S buffers are 128 fp32 columns each):
+//   dQ:        S0 [0,128) S1 [128,256) dP [256,384) dQ [384,384+D)
+//   dK/dV 64:  S0 [0,128) S1 [128,256) dP [256,384) dV [384,448) dK [448,512)
+//   dK/dV 128: S  [0,128)              dP [128,256) dV [256,384) dK [384,512)
+// Round r of warpgroup g covers score columns c0 = 64g + 16r .. c0+15; its bf16
+// P goes to S columns [c0, c0+8) and dS to [c0+8, c0+16) (dQ writes only dS at
+// [c0, c0+8)), so the A operand of K-step kk (16 score columns) is at 16*kk.
 // ============================================================================
 constexpr int kMainThreads = 320;
 constexpr int kComputeThreads = 256;
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColDP = 128;
-constexpr uint32_t kColAcc = 256;
 
 template <int D>
 struct MainCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = kHalves * kHalfTileBytes;
-  // dQ task: [Q][dO] then K ring (2) then V ring (2)
+  // dQ task: [Q][dO], K ring of 3, V ring of 2
+  static constexpr int kDqKStages = 3;
+  static constexpr int kDqVStages = 2;
   static constexpr int kDqOffQ = 0;
   static constexpr int kDqOffDO = kTileBytes;
   static constexpr int kDqOffK = 2 * kTileBytes;
-  static constexpr int kDqOffV = 4 * kTileBytes;
-  static constexpr int kDqBytes = 6 * kTileBytes;
-  // dK/dV task: [K][V] then 2 stages of [Q][dO][LSE2 x128][D x128]
+  static constexpr int kDqOffV = kDqOffK + kDqKStages * kTileBytes;
+  static constexpr int kDqBytes = kDqOffV + kDqVStages * kTileBytes;
+  // dK/dV task: [K][V], stages of [Q][dO][-LSE2 x128][D x128]
+  static constexpr int kKvNS = (D == 64) ? 2 : 1;       // S buffers
+  static constexpr int kKvStages = (D == 64) ? 3 : 2;   // Q/dO stages
   static constexpr int kStageBytes = 2 * kTileBytes + 1024;
   static constexpr int kKvOffK = 0;
   static constexpr int kKvOffV = kTileBytes;
   static constexpr int kKvOffStage = 2 * kTileBytes;
-  static constexpr int kKvBytes = 2 * kTileBytes + 2 * kStageBytes;
+  static constexpr int kKvBytes = kKvOffStage + kKvStages * kStageBytes;
   static constexpr int kUsed = (kDqBytes > kKvBytes ? kDqBytes : kKvBytes) + 1024;
   static constexpr int kSmemBytes = kUsed > kOneCtaPerSmSmem ? kUsed : kOneCtaPerSmSmem;
+  // TMEM columns
+  static constexpr uint32_t kDqColDP = 256;
+  static constexpr uint32_t kDqColAcc = 384;
+  static constexpr uint32_t kKvColDP = kKvNS * 128;
+  static constexpr uint32_t kKvColDV = kKvColDP + 128;
+  static constexpr uint32_t kKvColDK = kKvColDV + D;
 };
-
-// TMEM column of the bf16 A operand (P, P^T, dS or dS^T) for K-step kk (16 rows
-// of the reduction each); `base` is kColS or kColDP.
-__device__ __forceinline__ uint32_t packed_col(uint32_t base, int kk) {
-  return base + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-}
-
-// Store 32 packed bf16x2 columns (two x16 stores).
-__device__ __forceinline__ void tmem_st_packed32(uint32_t taddr, const uint32_t (&v)[32]) {
-  uint32_t a[16], b[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    a[i] = v[i];
-    b[i] = v[16 + i];
-  }
-  tmem_st16(taddr, a);
-  tmem_st16(taddr + 16, b);
-}
 
 // Store `ncols` (multiple of 32) fp32 columns of this thread's row as bf16 to dst.
 template <int NCOLS>
@@ -179,14 +183,103 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* ds
   }
 }
 
+// One 16-column round of a dK/dV tile (row = key, columns = queries).
+// nl2/dv: this round's 16 values of -LSE2 and D (per query). Visible iff lo <= col < hi.
+template <bool MASKED>
+__device__ __forceinline__ void dkv_round(const uint32_t (&s)[16], const uint32_t (&dp)[16], const float* nl2,
+                                          const float* dv, float sl2, int col0, int lo, int hi, uint32_t tS_round) {
+  uint32_t pk[8], dk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * i]), sl2, nl2[2 * i]));
+    float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * i + 1]), sl2, nl2[2 * i + 1]));
+    if (MASKED) {
+      const int c = col0 + 2 * i;
+      p0 = (c >= lo && c < hi) ? p0 : 0.f;
+      p1 = (c + 1 >= lo && c + 1 < hi) ? p1 : 0.f;
+    }
+    const float d0 = p0 * (__uint_as_float(dp[2 * i]) - dv[2 * i]);
+    const float d1 = p1 * (__uint_as_float(dp[2 * i + 1]) - dv[2 * i + 1]);
+    pk[i] = pack_bf16x2(p0, p1);
+    dk[i] = pack_bf16x2(d0, d1);
+  }
+  tmem_st8(tS_round, pk);
+  tmem_st8(tS_round + 8, dk);
+}
+
+// One 16-column round of a dQ tile (row = query, columns = keys). Visible iff col < lim.
+template <bool MASKED>
+__device__ __forceinline__ void dq_round(const uint32_t (&s)[16], const uint32_t (&dp)[16], float nl2_r, float D_r,
+                                         float sl2, int col0, int lim, uint32_t tS_round) {
+  uint32_t dk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * i]), sl2, nl2_r));
+    float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * i + 1]), sl2, nl2_r));
+    if (MASKED) {
+      const int c = col0 + 2 * i;
+      p0 = c < lim ? p0 : 0.f;
+      p1 = c + 1 < lim ? p1 : 0.f;
+    }
+    dk[i] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * i]) - D_r), p1 * (__uint_as_float(dp[2 * i + 1]) - D_r));
+  }
+  tmem_st8(tS_round, dk);
+}
+
+// One round of either kind; DKV rounds read this round's -LSE2 / D vectors from shared memory.
+template <bool DKV, bool MASKED>
+__device__ __forceinline__ void tile_round(int r, const uint32_t (&s)[16], const uint32_t (&dp)[16],
+                                           const float* vnl2, const float* vD, float nl2_r, float D_r, float sl2,
+                                           int lo, int hi, uint32_t tS) {
+  if (DKV) {
+    float nl[16], dv[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 a = *reinterpret_cast<const float4*>(vnl2 + r * 16 + 4 * i);
+      const float4 b = *reinterpret_cast<const float4*>(vD + r * 16 + 4 * i);
+      nl[4 * i] = a.x; nl[4 * i + 1] = a.y; nl[4 * i + 2] = a.z; nl[4 * i + 3] = a.w;
+      dv[4 * i] = b.x; dv[4 * i + 1] = b.y; dv[4 * i + 2] = b.z; dv[4 * i + 3] = b.w;
+    }
+    dkv_round<MASKED>(s, dp, nl, dv, sl2, r * 16, lo, hi, tS + r * 16);
+  } else {
+    dq_round<MASKED>(s, dp, nl2_r, D_r, sl2, r * 16, hi, tS + r * 16);
+  }
+}
+
+// The compute part of one tile for one warpgroup: four rounds of 16 columns with
+// the TMEM load of round r+2 in flight while round r+1 is computed. Signals
+// dp_free as soon as every dP column of this warpgroup is in registers.
+template <bool DKV, bool MASKED>
+__device__ __forceinline__ void compute_tile(uint32_t tS, uint32_t tDP, const float* vnl2, const float* vD,
+                                             float nl2_r, float D_r, float sl2, int lo, int hi, uint64_t* bar_dpfree) {
+  uint32_t sa[16], da[16], sb[16], db[16];
+  tmem_ld16(tS, sa);
+  tmem_ld16(tDP, da);
+  tmem_ld16(tS + 16, sb);
+  tmem_ld16(tDP + 16, db);
+  tmem_wait_ld();
+  tile_round<DKV, MASKED>(0, sa, da, vnl2, vD, nl2_r, D_r, sl2, lo, hi, tS);
+  tmem_ld16(tS + 32, sa);
+  tmem_ld16(tDP + 32, da);
+  tile_round<DKV, MASKED>(1, sb, db, vnl2, vD, nl2_r, D_r, sl2, lo, hi, tS);
+  tmem_wait_ld();
+  tmem_ld16(tS + 48, sb);
+  tmem_ld16(tDP + 48, db);
+  tile_round<DKV, MASKED>(2, sa, da, vnl2, vD, nl2_r, D_r, sl2, lo, hi, tS);
+  tmem_wait_ld();
+  // every dP column of this warpgroup is in registers: the MMA may overwrite dP
+  tc_fence_before();
+  mbar_arrive(bar_dpfree);
+  tile_round<DKV, MASKED>(3, sb, db, vnl2, vD, nl2_r, D_r, sl2, lo, hi, tS);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
   using Cfg = MainCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  // Barriers. dQ task: fixed = Q+dO, ring[0..1] = K full/empty, ring[2..3] = V full/empty.
-  // dK/dV task: fixed = K+V, ring[0..1] = stage full/empty.
-  __shared__ uint64_t bar_fixed, bar_full[4], bar_empty[4], bar_s, bar_p, bar_fin, bar_drain;
+  __shared__ uint64_t bar_fixed, bar_full[3], bar_empty[3], bar_vfull[2], bar_vempty[2];
+  __shared__ uint64_t bar_s, bar_dpfree, bar_p, bar_fin, bar_drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -197,11 +290,16 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_fixed, 1);
-    for (int s = 0; s < 4; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_vfull[s], 1);
+      mbar_init(&bar_vempty[s], 1);
+    }
     mbar_init(&bar_s, 1);
+    mbar_init(&bar_dpfree, kComputeThreads);
     mbar_init(&bar_p, kComputeThreads);
     mbar_init(&bar_fin, 1);
     mbar_init(&bar_drain, 1);
@@ -217,7 +315,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const WaitCtx ctx{&abort_sh, p.status, p.budget_ns, kKidBwdMain};
-  constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: N = 128 keys/queries
+  constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: N = 128
   constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);    // gradient MMAs: N = D, B MN-major
 
   // ---------------------------------------------------------------- task decode
@@ -242,6 +340,8 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
     kvh = h / p.G;
     n_it = p.causal ? tile + 1 : p.nT;
   }
+  const int NS = is_dkv ? Cfg::kKvNS : 2;
+  const int NST = is_dkv ? Cfg::kKvStages : Cfg::kDqKStages;
 
   if (warp == 0) {
     // ============================================================ TMA producer
@@ -250,16 +350,16 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
       tma_prefetch_desc(&p.tmap_k);
       tma_prefetch_desc(&p.tmap_v);
       tma_prefetch_desc(&p.tmap_do);
-      int issued[4] = {0, 0, 0, 0};
+      int issued[3] = {0, 0, 0}, vissued[2] = {0, 0};
       bool ok = true;
+      mbar_arrive_expect_tx(&bar_fixed, 2 * Cfg::kTileBytes);
       if (is_dkv) {
-        mbar_arrive_expect_tx(&bar_fixed, 2 * Cfg::kTileBytes);
         for (int hf = 0; hf < Cfg::kHalves; ++hf) {
           tma_load_4d(smem + Cfg::kKvOffK + hf * kHalfTileBytes, &p.tmap_k, &bar_fixed, hf * 64, kvh, tile * kTile, b);
           tma_load_4d(smem + Cfg::kKvOffV + hf * kHalfTileBytes, &p.tmap_v, &bar_fixed, hf * 64, kvh, tile * kTile, b);
         }
         for (int it = 0; it < n_it && ok; ++it) {
-          const int st = it & 1, n = it >> 1;
+          const int st = it % NST, n = it / NST;
           if (n > 0) ok = mbar_wait(&bar_empty[st], (n - 1) & 1, ctx, 1);
           if (!ok) break;
           const int hq = kvh * p.G + it / ni;
@@ -277,13 +377,12 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
           issued[st]++;
         }
       } else {
-        mbar_arrive_expect_tx(&bar_fixed, 2 * Cfg::kTileBytes);
         for (int hf = 0; hf < Cfg::kHalves; ++hf) {
           tma_load_4d(smem + Cfg::kDqOffQ + hf * kHalfTileBytes, &p.tmap_q, &bar_fixed, hf * 64, h, tile * kTile, b);
           tma_load_4d(smem + Cfg::kDqOffDO + hf * kHalfTileBytes, &p.tmap_do, &bar_fixed, hf * 64, h, tile * kTile, b);
         }
         for (int j = 0; j < n_it && ok; ++j) {
-          const int st = j & 1, n = j >> 1;
+          const int st = j % NST, n = j / NST;
           if (n > 0) ok = mbar_wait(&bar_empty[st], (n - 1) & 1, ctx, 1);
           if (!ok) break;
           mbar_arrive_expect_tx(&bar_full[st], Cfg::kTileBytes);
@@ -291,116 +390,136 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
             tma_load_4d(smem + Cfg::kDqOffK + st * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_k, &bar_full[st],
                         hf * 64, kvh, j * kTile, b);
           issued[st]++;
-          if (n > 0) ok = mbar_wait(&bar_empty[2 + st], (n - 1) & 1, ctx, 2);
+          const int vs = j & 1, vn = j >> 1;
+          if (vn > 0) ok = mbar_wait(&bar_vempty[vs], (vn - 1) & 1, ctx, 2);
           if (!ok) break;
-          mbar_arrive_expect_tx(&bar_full[2 + st], Cfg::kTileBytes);
+          mbar_arrive_expect_tx(&bar_vfull[vs], Cfg::kTileBytes);
           for (int hf = 0; hf < Cfg::kHalves; ++hf)
-            tma_load_4d(smem + Cfg::kDqOffV + st * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v,
-                        &bar_full[2 + st], hf * 64, kvh, j * kTile, b);
-          issued[2 + st]++;
+            tma_load_4d(smem + Cfg::kDqOffV + vs * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v, &bar_vfull[vs],
+                        hf * 64, kvh, j * kTile, b);
+          vissued[vs]++;
         }
       }
       // Wait until every stage is released, so no MMA commit arrives after exit.
-      for (int s = 0; s < 4 && ok; ++s)
+      for (int s = 0; s < 3 && ok; ++s)
         if (issued[s] > 0) ok = mbar_wait(&bar_empty[s], (issued[s] - 1) & 1, ctx, 3);
+      for (int s = 0; s < 2 && ok; ++s)
+        if (vissued[s] > 0) ok = mbar_wait(&bar_vempty[s], (vissued[s] - 1) & 1, ctx, 4);
       if (!ok) {
         mbar_wait_drain(&bar_fixed, 0, p.budget_ns);
-        for (int s = 0; s < 4; ++s)
+        for (int s = 0; s < 3; ++s)
           if (issued[s] > 0) mbar_wait_drain(&bar_full[s], (issued[s] - 1) & 1, p.budget_ns);
+        for (int s = 0; s < 2; ++s)
+          if (vissued[s] > 0) mbar_wait_drain(&bar_vfull[s], (vissued[s] - 1) & 1, p.budget_ns);
       }
     }
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     if (lane == 0) {
-      bool issued = false;
-      bool ok = mbar_wait(&bar_fixed, 0, ctx, 10);
-      if (is_dkv) {
-        const uint32_t sK = smem_u32(smem + Cfg::kKvOffK);
-        const uint32_t sV = smem_u32(smem + Cfg::kKvOffV);
-        for (int it = 0; it < n_it && ok; ++it) {
-          const int st = it & 1;
-          ok = mbar_wait(&bar_full[st], (it >> 1) & 1, ctx, 11);
-          if (!ok) break;
-          tc_fence_after();
+      bool issued_any = false;
+      const uint32_t colDP = is_dkv ? Cfg::kKvColDP : Cfg::kDqColDP;
+      // S (or S^T) of iteration i into S buffer i % NS.
+      auto issue_S = [&](int i) -> bool {
+        const int st = i % NST;
+        if (!mbar_wait(&bar_full[st], (i / NST) & 1, ctx, 11)) return false;
+        tc_fence_after();
+        const uint32_t dst = tmem + (i % NS) * 128;
+        uint32_t a, bb;
+        if (is_dkv) {
+          a = smem_u32(smem + Cfg::kKvOffK);
+          bb = smem_u32(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes);
+        } else {
+          a = smem_u32(smem + Cfg::kDqOffQ);
+          bb = smem_u32(smem + Cfg::kDqOffK + st * Cfg::kTileBytes);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
+          mma_ss(dst, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(bb + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        issued_any = true;
+        return true;
+      };
+      // dP (or dP^T) of iteration i into the dP buffer.
+      auto issue_dP = [&](int i) -> bool {
+        uint32_t a, bb;
+        if (is_dkv) {
+          const int st = i % NST;
+          if (!mbar_wait(&bar_full[st], (i / NST) & 1, ctx, 13)) return false;
+          a = smem_u32(smem + Cfg::kKvOffV);
+          bb = smem_u32(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes + Cfg::kTileBytes);
+        } else {
+          const int vs = i & 1;
+          if (!mbar_wait(&bar_vfull[vs], (i >> 1) & 1, ctx, 13)) return false;
+          a = smem_u32(smem + Cfg::kDqOffDO);
+          bb = smem_u32(smem + Cfg::kDqOffV + vs * Cfg::kTileBytes);
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
+          mma_ss(tmem + colDP, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(bb + off, 16, 1024), idesc_s,
+                 kk > 0 ? 1u : 0u);
+        }
+        issued_any = true;
+        if (!is_dkv) mma_commit(&bar_vempty[i & 1]);
+        return true;
+      };
+      // Gradient MMAs of iteration i from the bf16 P/dS in S buffer i % NS.
+      auto issue_grad = [&](int i) {
+        const uint32_t sbuf = tmem + (i % NS) * 128;
+        const int st = i % NST;
+        if (is_dkv) {
           const uint32_t sQ = smem_u32(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes);
           const uint32_t sDO = sQ + Cfg::kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-            mma_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idesc_s,
-                   kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-            mma_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), idesc_s,
-                   kk > 0 ? 1u : 0u);
-          }
-          issued = true;
-          mma_commit(&bar_s);
-          ok = mbar_wait(&bar_p, it & 1, ctx, 12);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-            mma_ts(tmem + kColAcc, tmem + packed_col(kColS, kk),
-                   sdesc_sw128(sDO + kk * 2048, kHalfTileBytes, 1024), idesc_g, acc);
-            mma_ts(tmem + kColAcc + D, tmem + packed_col(kColDP, kk),
-                   sdesc_sw128(sQ + kk * 2048, kHalfTileBytes, 1024), idesc_g, acc);
+            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+            mma_ts(tmem + Cfg::kKvColDV, sbuf + kk * 16, sdesc_sw128(sDO + kk * 2048, kHalfTileBytes, 1024),
+                   idesc_g, acc);
+            mma_ts(tmem + Cfg::kKvColDK, sbuf + kk * 16 + 8, sdesc_sw128(sQ + kk * 2048, kHalfTileBytes, 1024),
+                   idesc_g, acc);
           }
-          mma_commit(&bar_empty[st]);
-        }
-      } else {
-        const uint32_t sQ = smem_u32(smem + Cfg::kDqOffQ);
-        const uint32_t sDO = smem_u32(smem + Cfg::kDqOffDO);
-        auto issue_dq = [&](int jj) -> bool {
-          if (!mbar_wait(&bar_p, jj & 1, ctx, 12)) return false;
-          tc_fence_after();
-          const int st = jj & 1;
-          const uint32_t kbase = smem_u32(smem + Cfg::kDqOffK + st * Cfg::kTileBytes);
+        } else {
+          const uint32_t kb = smem_u32(smem + Cfg::kDqOffK + st * Cfg::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + kColAcc, tmem + packed_col(kColS, kk), sdesc_sw128(kbase + kk * 2048, kHalfTileBytes, 1024),
-                   idesc_g, (jj > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bar_empty[st]);
-          return true;
-        };
-        for (int j = 0; j < n_it && ok; ++j) {
-          if (j > 0) {
-            ok = issue_dq(j - 1);
-            if (!ok) break;
-          }
-          const int st = j & 1;
-          ok = mbar_wait(&bar_full[st], (j >> 1) & 1, ctx, 11);
+            mma_ts(tmem + Cfg::kDqColAcc, sbuf + kk * 16, sdesc_sw128(kb + kk * 2048, kHalfTileBytes, 1024), idesc_g,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bar_empty[st]);
+      };
+
+      bool ok = mbar_wait(&bar_fixed, 0, ctx, 10);
+      if (ok) ok = issue_S(0);
+      if (ok) ok = issue_dP(0);
+      if (ok) mma_commit(&bar_s);
+      for (int it = 0; it < n_it && ok; ++it) {
+        const bool has_next = it + 1 < n_it;
+        if (NS == 2 && has_next) {
+          ok = issue_S(it + 1);
           if (!ok) break;
-          tc_fence_after();
-          const uint32_t kbase = smem_u32(smem + Cfg::kDqOffK + st * Cfg::kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-            mma_ss(tmem + kColS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), idesc_s,
-                   kk > 0 ? 1u : 0u);
-          }
-          issued = true;
-          ok = mbar_wait(&bar_full[2 + st], (j >> 1) & 1, ctx, 13);
+        }
+        ok = mbar_wait(&bar_dpfree, it & 1, ctx, 14);
+        if (!ok) break;
+        if (has_next) {
+          ok = issue_dP(it + 1);
           if (!ok) break;
-          tc_fence_after();
-          const uint32_t vbase = smem_u32(smem + Cfg::kDqOffV + st * Cfg::kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-            mma_ss(tmem + kColDP, sdesc_sw128(sDO + off, 16, 1024), sdesc_sw128(vbase + off, 16, 1024), idesc_s,
-                   kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bar_empty[2 + st]);
+          if (NS == 2) mma_commit(&bar_s);
+        }
+        ok = mbar_wait(&bar_p, it & 1, ctx, 12);
+        if (!ok) break;
+        tc_fence_after();
+        issue_grad(it);
+        if (NS == 1 && has_next) {
+          ok = issue_S(it + 1);
+          if (!ok) break;
           mma_commit(&bar_s);
         }
-        if (ok) ok = issue_dq(n_it - 1);
       }
       if (ok) {
         mma_commit(&bar_fin);
-      } else if (issued) {
+      } else if (issued_any) {
         mma_commit(&bar_drain);
         mbar_wait_drain(&bar_drain, 0, p.budget_ns);
       }
@@ -411,64 +530,32 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_base + kColS + wg * 64;
-    const uint32_t tDP = tmem + lane_base + kColDP + wg * 64;
-    const uint64_t sl2x2 = f2_make(p.scale_log2, p.scale_log2);
+    const float sl2 = p.scale_log2;
     bool ok = true;
     if (is_dkv) {
       const int k_idx = tile * kTile + row;
+      const uint32_t tDP = tmem + lane_base + Cfg::kKvColDP + wg * 64;
       for (int it = 0; it < n_it; ++it) {
-        const int st = it & 1;
+        const int st = it % NST;
         const int qt = i0 + it % ni;
         ok = warp_wait(&bar_s, it & 1, ctx, 20);
         if (!ok) break;
-        ok = warp_wait(&bar_full[st], (it >> 1) & 1, ctx, 22);  // LSE2 / D vectors of this stage
+        ok = warp_wait(&bar_full[st], (it / NST) & 1, ctx, 22);  // -LSE2 / D vectors of this stage
         if (!ok) break;
         tc_fence_after();
-        uint32_t rs[64], rp[64];
-        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
-        tmem_ld32(tDP, *reinterpret_cast<uint32_t(*)[32]>(&rp[0]));
-        tmem_ld32(tDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&rp[32]));
-        tmem_wait_ld();
-        const float* vl = reinterpret_cast<const float*>(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes +
-                                                         2 * Cfg::kTileBytes) + wg * 64;
-        const float* vd = vl + kTile;
-        // Query columns visible to this key row: [lo, hi) relative to this warpgroup's 64 columns.
+        const uint32_t tS = tmem + lane_base + (it % NS) * 128 + wg * 64;
+        const float* vnl2 = reinterpret_cast<const float*>(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes +
+                                                           2 * Cfg::kTileBytes) + wg * 64;
+        const float* vD = vnl2 + kTile;
+        // Query columns visible to this key row: [lo, hi) in this warpgroup's 64-column frame.
         const int hi_tile = min(kTile, p.T - qt * kTile);
-        const bool masked = (p.causal && qt == tile) || hi_tile < kTile;
-        const int lo = ((p.causal && qt == tile) ? row : 0) - wg * 64;
+        const bool diag = p.causal && qt == tile;
+        const int lo = (diag ? row : 0) - wg * 64;
         const int hi = hi_tile - wg * 64;
-        uint32_t pk[32], dk[32];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float4 l4 = *reinterpret_cast<const float4*>(vl + 2 * i);
-          const float4 d4 = *reinterpret_cast<const float4*>(vd + 2 * i);
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = 2 * (i + u);
-            const float la = u ? l4.z : l4.x, lb = u ? l4.w : l4.y;
-            const float da = u ? d4.z : d4.x, db = u ? d4.w : d4.y;
-            const uint64_t sarg = f2_fma(f2_make(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])), sl2x2,
-                                         f2_make(-la, -lb));
-            float a0, a1;
-            f2_split(sarg, a0, a1);
-            float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-            if (masked) {
-              p0 = (c >= lo && c < hi) ? p0 : 0.f;
-              p1 = (c + 1 >= lo && c + 1 < hi) ? p1 : 0.f;
-            }
-            const uint64_t pp = f2_make(p0, p1);
-            const uint64_t ds = f2_mul(pp, f2_sub(f2_make(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])),
-                                                  f2_make(da, db)));
-            float d0, d1;
-            f2_split(ds, d0, d1);
-            pk[i + u] = pack_bf16x2(p0, p1);
-            dk[i + u] = pack_bf16x2(d0, d1);
-          }
-        }
-        tmem_st_packed32(tS, pk);
-        tmem_st_packed32(tDP, dk);
+        if (diag || hi_tile < kTile)
+          compute_tile<true, true>(tS, tDP, vnl2, vD, 0.f, 0.f, sl2, lo, hi, &bar_dpfree);
+        else
+          compute_tile<true, false>(tS, tDP, vnl2, vD, 0.f, 0.f, sl2, lo, hi, &bar_dpfree);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bar_p);
@@ -479,56 +566,36 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
         const bool valid = k_idx < p.T;
         const size_t off = ((static_cast<size_t>(b) * p.T + (valid ? k_idx : 0)) * p.Hkv + kvh) * D;
         if (wg == 0)
-          store_row_bf16<D>(tmem + lane_base + kColAcc, reinterpret_cast<__nv_bfloat16*>(p.dv) + off, 1.f, valid);
+          store_row_bf16<D>(tmem + lane_base + Cfg::kKvColDV, reinterpret_cast<__nv_bfloat16*>(p.dv) + off, 1.f,
+                            valid);
         else
-          store_row_bf16<D>(tmem + lane_base + kColAcc + D, reinterpret_cast<__nv_bfloat16*>(p.dk) + off, p.scale,
+          store_row_bf16<D>(tmem + lane_base + Cfg::kKvColDK, reinterpret_cast<__nv_bfloat16*>(p.dk) + off, p.scale,
                             valid);
       }
     } else {
       const int q_idx = tile * kTile + row;
       const bool valid = q_idx < p.T;
       const size_t vec_idx = (static_cast<size_t>(b) * p.Hq + h) * p.Tpad + q_idx;  // < B*Hq*Tpad
-      const float lse2_r = p.lse2[vec_idx];
+      const float nl2_r = p.lse2[vec_idx];
       const float D_r = p.Dvec[vec_idx];
-      const uint64_t neg_l2 = f2_make(-lse2_r, -lse2_r);
-      const uint64_t Dx2 = f2_make(D_r, D_r);
+      const uint32_t tDP = tmem + lane_base + Cfg::kDqColDP + wg * 64;
+      const bool tile_ragged = (tile + 1) * kTile > p.T;
       for (int j = 0; j < n_it; ++j) {
         ok = warp_wait(&bar_s, j & 1, ctx, 20);
         if (!ok) break;
         tc_fence_after();
-        uint32_t rs[64], rp[64];
-        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
-        tmem_ld32(tDP, *reinterpret_cast<uint32_t(*)[32]>(&rp[0]));
-        tmem_ld32(tDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&rp[32]));
-        tmem_wait_ld();
-        // Key columns visible to this query row: [0, lim) relative to this warpgroup's 64 columns.
+        const uint32_t tS = tmem + lane_base + (j & 1) * 128 + wg * 64;
+        // Key columns visible to this query row: [0, lim) in this warpgroup's 64-column frame.
+        const bool diag = p.causal && j == tile;
+        const bool kv_ragged = !p.causal && (j + 1) * kTile > p.T;
         int lim_tile = kTile;
-        if (p.causal && j == tile) lim_tile = row + 1;
-        if (!p.causal && (j + 1) * kTile > p.T) lim_tile = p.T - j * kTile;
-        const bool masked = (p.causal && j == tile) || (!p.causal && (j + 1) * kTile > p.T) ||
-                            (tile + 1) * kTile > p.T;
+        if (diag) lim_tile = row + 1;
+        if (kv_ragged) lim_tile = p.T - j * kTile;
         const int lim = (valid ? lim_tile : 0) - wg * 64;
-        uint32_t dk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = 2 * i;
-          const uint64_t sarg =
-              f2_fma(f2_make(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])), sl2x2, neg_l2);
-          float a0, a1;
-          f2_split(sarg, a0, a1);
-          float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-          if (masked) {
-            p0 = c < lim ? p0 : 0.f;
-            p1 = c + 1 < lim ? p1 : 0.f;
-          }
-          const uint64_t ds =
-              f2_mul(f2_make(p0, p1), f2_sub(f2_make(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])), Dx2));
-          float d0, d1;
-          f2_split(ds, d0, d1);
-          dk[i] = pack_bf16x2(d0, d1);
-        }
-        tmem_st_packed32(tS, dk);
+        if (diag || kv_ragged || tile_ragged)
+          compute_tile<false, true>(tS, tDP, nullptr, nullptr, nl2_r, D_r, sl2, 0, lim, &bar_dpfree);
+        else
+          compute_tile<false, false>(tS, tDP, nullptr, nullptr, nl2_r, D_r, sl2, 0, lim, &bar_dpfree);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bar_p);
@@ -537,7 +604,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
       if (ok) {
         tc_fence_after();
         const size_t off = ((static_cast<size_t>(b) * p.T + (valid ? q_idx : 0)) * p.Hq + h) * D;
-        store_row_bf16<D / 2>(tmem + lane_base + kColAcc + wg * (D / 2),
+        store_row_bf16<D / 2>(tmem + lane_base + Cfg::kDqColAcc + wg * (D / 2),
                               reinterpret_cast<__nv_bfloat16*>(p.dq) + off + wg * (D / 2), p.scale, valid);
       }
     }
