@@ -273,13 +273,314 @@ __device__ __forceinline__ void compute_tile(uint32_t tS, uint32_t tDP, const fl
   tile_round<DKV, MASKED>(3, sb, db, vnl2, vD, nl2_r, D_r, sl2, lo, hi, tS);
 }
 
+// `p[it & 1]` ("bf16 P/dS of iteration it are in TMEM") alternates between two
+// barriers: S(it+1) is committed before the MMA thread waits for P(it), so the
+// compute warps may finish iteration it+1 before that wait is observed, and a
+// single barrier could then have moved two phases on.
+struct MainBars {
+  uint64_t fixed, full[3], empty[3], vfull[2], vempty[2], s, dpfree, p[2], fin, drain;
+};
+
+struct TaskInfo {
+  int b, kvh, h, tile, n_it, i0, ni;
+};
+
+// Descriptor offset (in 16-byte units) of K-step kk inside a K-major tile of
+// 64-wide halves: 32 bytes per step inside a 128-byte row, a new half every 4 steps.
+__device__ __forceinline__ constexpr uint32_t kmaj_step(int kk) {
+  return static_cast<uint32_t>(((kk >> 2) * kHalfTileBytes + (kk & 3) * 32) >> 4);
+}
+
+// One task of either kind, all roles. Every pipeline depth is a compile-time
+// constant and every MMA descriptor is a base plus a constant, so the single
+// issuing thread spends a few instructions per MMA.
+template <int D, bool DKV>
+__device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, MainBars& bars, uint32_t tmem,
+                                         const WaitCtx& ctx, const TaskInfo& t, int warp, int lane) {
+  using Cfg = MainCfg<D>;
+  constexpr int NS = DKV ? Cfg::kKvNS : 2;                    // S buffers in TMEM
+  constexpr int NST = DKV ? Cfg::kKvStages : Cfg::kDqKStages;  // main ring depth
+  constexpr uint32_t colDP = DKV ? Cfg::kKvColDP : Cfg::kDqColDP;
+  constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: N = 128
+  constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);    // gradients: N = D, B MN-major
+  constexpr uint32_t kTileD = Cfg::kTileBytes >> 4;             // tile stride, descriptor units
+  constexpr uint32_t kStageD = Cfg::kStageBytes >> 4;
+  const int n_it = t.n_it;
+
+  if (warp == 0) {
+    // ============================================================ TMA producer
+    if (lane != 0) return;
+    tma_prefetch_desc(&p.tmap_q);
+    tma_prefetch_desc(&p.tmap_k);
+    tma_prefetch_desc(&p.tmap_v);
+    tma_prefetch_desc(&p.tmap_do);
+    int issued[3] = {0, 0, 0}, vissued[2] = {0, 0};
+    bool ok = true;
+    mbar_arrive_expect_tx(&bars.fixed, 2 * Cfg::kTileBytes);
+    if (DKV) {
+      for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+        tma_load_4d(smem + Cfg::kKvOffK + hf * kHalfTileBytes, &p.tmap_k, &bars.fixed, hf * 64, t.kvh,
+                    t.tile * kTile, t.b);
+        tma_load_4d(smem + Cfg::kKvOffV + hf * kHalfTileBytes, &p.tmap_v, &bars.fixed, hf * 64, t.kvh,
+                    t.tile * kTile, t.b);
+      }
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int st = it % NST, n = it / NST;
+        if (n > 0) ok = mbar_wait(&bars.empty[st], (n - 1) & 1, ctx, 1);
+        if (!ok) break;
+        const int hq = t.kvh * p.G + it / t.ni;
+        const int qt = t.i0 + it % t.ni;
+        uint8_t* stage = smem + Cfg::kKvOffStage + st * Cfg::kStageBytes;
+        mbar_arrive_expect_tx(&bars.full[st], 2 * Cfg::kTileBytes + 1024);
+        for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+          tma_load_4d(stage + hf * kHalfTileBytes, &p.tmap_q, &bars.full[st], hf * 64, hq, qt * kTile, t.b);
+          tma_load_4d(stage + Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_do, &bars.full[st], hf * 64, hq,
+                      qt * kTile, t.b);
+        }
+        const size_t vec = (static_cast<size_t>(t.b) * p.Hq + hq) * p.Tpad + static_cast<size_t>(qt) * kTile;
+        bulk_load(stage + 2 * Cfg::kTileBytes, p.lse2 + vec, 512, &bars.full[st]);
+        bulk_load(stage + 2 * Cfg::kTileBytes + 512, p.Dvec + vec, 512, &bars.full[st]);
+        issued[st]++;
+      }
+    } else {
+      for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+        tma_load_4d(smem + Cfg::kDqOffQ + hf * kHalfTileBytes, &p.tmap_q, &bars.fixed, hf * 64, t.h,
+                    t.tile * kTile, t.b);
+        tma_load_4d(smem + Cfg::kDqOffDO + hf * kHalfTileBytes, &p.tmap_do, &bars.fixed, hf * 64, t.h,
+                    t.tile * kTile, t.b);
+      }
+      for (int j = 0; j < n_it && ok; ++j) {
+        const int st = j % NST, n = j / NST;
+        if (n > 0) ok = mbar_wait(&bars.empty[st], (n - 1) & 1, ctx, 1);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars.full[st], Cfg::kTileBytes);
+        for (int hf = 0; hf < Cfg::kHalves; ++hf)
+          tma_load_4d(smem + Cfg::kDqOffK + st * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_k, &bars.full[st],
+                      hf * 64, t.kvh, j * kTile, t.b);
+        issued[st]++;
+        const int vs = j & 1, vn = j >> 1;
+        if (vn > 0) ok = mbar_wait(&bars.vempty[vs], (vn - 1) & 1, ctx, 2);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars.vfull[vs], Cfg::kTileBytes);
+        for (int hf = 0; hf < Cfg::kHalves; ++hf)
+          tma_load_4d(smem + Cfg::kDqOffV + vs * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v, &bars.vfull[vs],
+                      hf * 64, t.kvh, j * kTile, t.b);
+        vissued[vs]++;
+      }
+    }
+    // Wait until every stage is released, so no MMA commit arrives after exit.
+    for (int s2 = 0; s2 < 3 && ok; ++s2)
+      if (issued[s2] > 0) ok = mbar_wait(&bars.empty[s2], (issued[s2] - 1) & 1, ctx, 3);
+    for (int s2 = 0; s2 < 2 && ok; ++s2)
+      if (vissued[s2] > 0) ok = mbar_wait(&bars.vempty[s2], (vissued[s2] - 1) & 1, ctx, 4);
+    if (!ok) {
+      mbar_wait_drain(&bars.fixed, 0, p.budget_ns);
+      for (int s2 = 0; s2 < 3; ++s2)
+        if (issued[s2] > 0) mbar_wait_drain(&bars.full[s2], (issued[s2] - 1) & 1, p.budget_ns);
+      for (int s2 = 0; s2 < 2; ++s2)
+        if (vissued[s2] > 0) mbar_wait_drain(&bars.vfull[s2], (vissued[s2] - 1) & 1, p.budget_ns);
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane != 0) return;
+    // Base descriptors (stage / slot 0); a stage or K-step moves the start address only.
+    uint64_t dA_S, dA_P, dB_S, dB_P, dG1, dG2;
+    uint32_t strideB_S, strideB_P;
+    if (DKV) {
+      const uint32_t st0 = smem_u32(smem + Cfg::kKvOffStage);
+      dA_S = sdesc_sw128(smem_u32(smem + Cfg::kKvOffK), 16, 1024);             // K
+      dA_P = sdesc_sw128(smem_u32(smem + Cfg::kKvOffV), 16, 1024);             // V
+      dB_S = sdesc_sw128(st0, 16, 1024);                                       // Q   (K-major)
+      dB_P = sdesc_sw128(st0 + Cfg::kTileBytes, 16, 1024);                     // dO  (K-major)
+      dG1 = sdesc_sw128(st0 + Cfg::kTileBytes, kHalfTileBytes, 1024);          // dO  (MN-major) for dV
+      dG2 = sdesc_sw128(st0, kHalfTileBytes, 1024);                            // Q   (MN-major) for dK
+      strideB_S = kStageD;
+      strideB_P = kStageD;
+    } else {
+      dA_S = sdesc_sw128(smem_u32(smem + Cfg::kDqOffQ), 16, 1024);             // Q
+      dA_P = sdesc_sw128(smem_u32(smem + Cfg::kDqOffDO), 16, 1024);            // dO
+      dB_S = sdesc_sw128(smem_u32(smem + Cfg::kDqOffK), 16, 1024);             // K slot 0 (K-major)
+      dB_P = sdesc_sw128(smem_u32(smem + Cfg::kDqOffV), 16, 1024);             // V slot 0 (K-major)
+      dG1 = sdesc_sw128(smem_u32(smem + Cfg::kDqOffK), kHalfTileBytes, 1024);  // K slot 0 (MN-major) for dQ
+      dG2 = 0;
+      strideB_S = kTileD;
+      strideB_P = kTileD;
+    }
+    bool issued_any = false;
+    auto issue_S = [&](int i) -> bool {
+      const int st = i % NST;
+      if (!mbar_wait(&bars.full[st], (i / NST) & 1, ctx, 11)) return false;
+      tc_fence_after();
+      const uint32_t dst = tmem + (i % NS) * 128;
+      const uint64_t b0 = dB_S + st * strideB_S;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss(dst, dA_S + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+      issued_any = true;
+      return true;
+    };
+    auto issue_dP = [&](int i) -> bool {
+      int slot;
+      if (DKV) {
+        slot = i % NST;
+        if (!mbar_wait(&bars.full[slot], (i / NST) & 1, ctx, 13)) return false;
+      } else {
+        slot = i & 1;
+        if (!mbar_wait(&bars.vfull[slot], (i >> 1) & 1, ctx, 13)) return false;
+      }
+      tc_fence_after();
+      const uint64_t b0 = dB_P + slot * strideB_P;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss(tmem + colDP, dA_P + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+      issued_any = true;
+      if (!DKV) mma_commit(&bars.vempty[slot]);
+      return true;
+    };
+    auto issue_grad = [&](int i) {
+      const int st = i % NST;
+      const uint32_t sbuf = tmem + (i % NS) * 128;
+      if (DKV) {
+        const uint64_t g1 = dG1 + st * kStageD, g2 = dG2 + st * kStageD;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          mma_ts(tmem + Cfg::kKvColDV, sbuf + kk * 16, g1 + kk * 128, idesc_g, acc);
+          mma_ts(tmem + Cfg::kKvColDK, sbuf + kk * 16 + 8, g2 + kk * 128, idesc_g, acc);
+        }
+      } else {
+        const uint64_t g1 = dG1 + st * kTileD;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + Cfg::kDqColAcc, sbuf + kk * 16, g1 + kk * 128, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(&bars.empty[st]);
+    };
+
+    bool ok = mbar_wait(&bars.fixed, 0, ctx, 10);
+    if (ok) ok = issue_S(0);
+    if (ok) ok = issue_dP(0);
+    if (ok) mma_commit(&bars.s);
+    for (int it = 0; it < n_it && ok; ++it) {
+      const bool has_next = it + 1 < n_it;
+      if (NS == 2 && has_next) {
+        ok = issue_S(it + 1);
+        if (!ok) break;
+      }
+      ok = mbar_wait(&bars.dpfree, it & 1, ctx, 14);
+      if (!ok) break;
+      if (has_next) {
+        ok = issue_dP(it + 1);
+        if (!ok) break;
+        if (NS == 2) mma_commit(&bars.s);
+      }
+      ok = mbar_wait(&bars.p[it & 1], (it >> 1) & 1, ctx, 12);
+      if (!ok) break;
+      tc_fence_after();
+      issue_grad(it);
+      if (NS == 1 && has_next) {
+        ok = issue_S(it + 1);
+        if (!ok) break;
+        mma_commit(&bars.s);
+      }
+    }
+    if (ok) {
+      mma_commit(&bars.fin);
+    } else if (issued_any) {
+      mma_commit(&bars.drain);
+      mbar_wait_drain(&bars.drain, 0, p.budget_ns);
+    }
+  } else {
+    // ============================================================ compute warpgroups
+    const int wg = (warp - 2) >> 2;  // 0 or 1: score columns [wg*64, wg*64+64)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tDP = tmem + lane_base + colDP + wg * 64;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    if (DKV) {
+      const int k_idx = t.tile * kTile + row;
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it % NST;
+        const int qt = t.i0 + it % t.ni;
+        ok = warp_wait(&bars.s, it & 1, ctx, 20);
+        if (!ok) break;
+        ok = warp_wait(&bars.full[st], (it / NST) & 1, ctx, 22);  // -LSE2 / D vectors of this stage
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tS = tmem + lane_base + (it % NS) * 128 + wg * 64;
+        const float* vnl2 = reinterpret_cast<const float*>(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes +
+                                                           2 * Cfg::kTileBytes) + wg * 64;
+        const float* vD = vnl2 + kTile;
+        // Query columns visible to this key row: [lo, hi) in this warpgroup's 64-column frame.
+        const int hi_tile = min(kTile, p.T - qt * kTile);
+        const bool diag = p.causal && qt == t.tile;
+        const int lo = (diag ? row : 0) - wg * 64;
+        const int hi = hi_tile - wg * 64;
+        if (diag || hi_tile < kTile)
+          compute_tile<true, true>(tS, tDP, vnl2, vD, 0.f, 0.f, sl2, lo, hi, &bars.dpfree);
+        else
+          compute_tile<true, false>(tS, tDP, vnl2, vD, 0.f, 0.f, sl2, lo, hi, &bars.dpfree);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars.p[it & 1]);
+      }
+      if (ok) ok = warp_wait(&bars.fin, 0, ctx, 21);
+      if (ok) {
+        tc_fence_after();
+        const bool valid = k_idx < p.T;
+        const size_t off = ((static_cast<size_t>(t.b) * p.T + (valid ? k_idx : 0)) * p.Hkv + t.kvh) * D;
+        if (wg == 0)
+          store_row_bf16<D>(tmem + lane_base + Cfg::kKvColDV, reinterpret_cast<__nv_bfloat16*>(p.dv) + off, 1.f,
+                            valid);
+        else
+          store_row_bf16<D>(tmem + lane_base + Cfg::kKvColDK, reinterpret_cast<__nv_bfloat16*>(p.dk) + off, p.scale,
+                            valid);
+      }
+    } else {
+      const int q_idx = t.tile * kTile + row;
+      const bool valid = q_idx < p.T;
+      const size_t vec_idx = (static_cast<size_t>(t.b) * p.Hq + t.h) * p.Tpad + q_idx;  // < B*Hq*Tpad
+      const float nl2_r = p.lse2[vec_idx];
+      const float D_r = p.Dvec[vec_idx];
+      const bool tile_ragged = (t.tile + 1) * kTile > p.T;
+      for (int j = 0; j < n_it; ++j) {
+        ok = warp_wait(&bars.s, j & 1, ctx, 20);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tS = tmem + lane_base + (j & 1) * 128 + wg * 64;
+        // Key columns visible to this query row: [0, lim) in this warpgroup's 64-column frame.
+        const bool diag = p.causal && j == t.tile;
+        const bool kv_ragged = !p.causal && (j + 1) * kTile > p.T;
+        int lim_tile = kTile;
+        if (diag) lim_tile = row + 1;
+        if (kv_ragged) lim_tile = p.T - j * kTile;
+        const int lim = (valid ? lim_tile : 0) - wg * 64;
+        if (diag || kv_ragged || tile_ragged)
+          compute_tile<false, true>(tS, tDP, nullptr, nullptr, nl2_r, D_r, sl2, 0, lim, &bars.dpfree);
+        else
+          compute_tile<false, false>(tS, tDP, nullptr, nullptr, nl2_r, D_r, sl2, 0, lim, &bars.dpfree);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars.p[j & 1]);
+      }
+      if (ok) ok = warp_wait(&bars.fin, 0, ctx, 21);
+      if (ok) {
+        tc_fence_after();
+        const size_t off = ((static_cast<size_t>(t.b) * p.T + (valid ? q_idx : 0)) * p.Hq + t.h) * D;
+        store_row_bf16<D / 2>(tmem + lane_base + Cfg::kDqColAcc + wg * (D / 2),
+                              reinterpret_cast<__nv_bfloat16*>(p.dq) + off + wg * (D / 2), p.scale, valid);
+      }
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
-  using Cfg = MainCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  __shared__ uint64_t bar_fixed, bar_full[3], bar_empty[3], bar_vfull[2], bar_vempty[2];
-  __shared__ uint64_t bar_s, bar_dpfree, bar_p, bar_fin, bar_drain;
+  __shared__ MainBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -289,20 +590,21 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
   const bool is_dkv = static_cast<int>(blockIdx.x) < n_dkv;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar_fixed, 1);
+    mbar_init(&bars.fixed, 1);
     for (int s = 0; s < 3; ++s) {
-      mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 1);
+      mbar_init(&bars.full[s], 1);
+      mbar_init(&bars.empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_vfull[s], 1);
-      mbar_init(&bar_vempty[s], 1);
+      mbar_init(&bars.vfull[s], 1);
+      mbar_init(&bars.vempty[s], 1);
     }
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_dpfree, kComputeThreads);
-    mbar_init(&bar_p, kComputeThreads);
-    mbar_init(&bar_fin, 1);
-    mbar_init(&bar_drain, 1);
+    mbar_init(&bars.s, 1);
+    mbar_init(&bars.dpfree, kComputeThreads);
+    mbar_init(&bars.p[0], kComputeThreads);
+    mbar_init(&bars.p[1], kComputeThreads);
+    mbar_init(&bars.fin, 1);
+    mbar_init(&bars.drain, 1);
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -315,300 +617,34 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const WaitCtx ctx{&abort_sh, p.status, p.budget_ns, kKidBwdMain};
-  constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: N = 128
-  constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);    // gradient MMAs: N = D, B MN-major
 
-  // ---------------------------------------------------------------- task decode
-  int b, kvh, h = 0, tile, n_it;
-  int i0 = 0, ni = 1;  // dK/dV: first query tile and query tiles per head
+  TaskInfo t;
+  t.h = 0;
+  t.i0 = 0;
+  t.ni = 1;
   if (is_dkv) {
     const int nbk = p.B * p.Hkv;
-    tile = static_cast<int>(blockIdx.x) / nbk;
+    t.tile = static_cast<int>(blockIdx.x) / nbk;
     const int bk = static_cast<int>(blockIdx.x) % nbk;
-    b = bk / p.Hkv;
-    kvh = bk % p.Hkv;
-    i0 = p.causal ? tile : 0;
-    ni = p.nT - i0;
-    n_it = p.G * ni;
+    t.b = bk / p.Hkv;
+    t.kvh = bk % p.Hkv;
+    t.i0 = p.causal ? t.tile : 0;
+    t.ni = p.nT - t.i0;
+    t.n_it = p.G * t.ni;
   } else {
-    const int t = static_cast<int>(blockIdx.x) - n_dkv;
+    const int q = static_cast<int>(blockIdx.x) - n_dkv;
     const int nbh = p.B * p.Hq;
-    tile = p.nT - 1 - t / nbh;
-    const int bh = t % nbh;
-    b = bh / p.Hq;
-    h = bh % p.Hq;
-    kvh = h / p.G;
-    n_it = p.causal ? tile + 1 : p.nT;
+    t.tile = p.nT - 1 - q / nbh;
+    const int bh = q % nbh;
+    t.b = bh / p.Hq;
+    t.h = bh % p.Hq;
+    t.kvh = t.h / p.G;
+    t.n_it = p.causal ? t.tile + 1 : p.nT;
   }
-  const int NS = is_dkv ? Cfg::kKvNS : 2;
-  const int NST = is_dkv ? Cfg::kKvStages : Cfg::kDqKStages;
-
-  if (warp == 0) {
-    // ============================================================ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&p.tmap_q);
-      tma_prefetch_desc(&p.tmap_k);
-      tma_prefetch_desc(&p.tmap_v);
-      tma_prefetch_desc(&p.tmap_do);
-      int issued[3] = {0, 0, 0}, vissued[2] = {0, 0};
-      bool ok = true;
-      mbar_arrive_expect_tx(&bar_fixed, 2 * Cfg::kTileBytes);
-      if (is_dkv) {
-        for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-          tma_load_4d(smem + Cfg::kKvOffK + hf * kHalfTileBytes, &p.tmap_k, &bar_fixed, hf * 64, kvh, tile * kTile, b);
-          tma_load_4d(smem + Cfg::kKvOffV + hf * kHalfTileBytes, &p.tmap_v, &bar_fixed, hf * 64, kvh, tile * kTile, b);
-        }
-        for (int it = 0; it < n_it && ok; ++it) {
-          const int st = it % NST, n = it / NST;
-          if (n > 0) ok = mbar_wait(&bar_empty[st], (n - 1) & 1, ctx, 1);
-          if (!ok) break;
-          const int hq = kvh * p.G + it / ni;
-          const int qt = i0 + it % ni;
-          uint8_t* stage = smem + Cfg::kKvOffStage + st * Cfg::kStageBytes;
-          mbar_arrive_expect_tx(&bar_full[st], 2 * Cfg::kTileBytes + 1024);
-          for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-            tma_load_4d(stage + hf * kHalfTileBytes, &p.tmap_q, &bar_full[st], hf * 64, hq, qt * kTile, b);
-            tma_load_4d(stage + Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_do, &bar_full[st], hf * 64, hq,
-                        qt * kTile, b);
-          }
-          const size_t vec = (static_cast<size_t>(b) * p.Hq + hq) * p.Tpad + static_cast<size_t>(qt) * kTile;
-          bulk_load(stage + 2 * Cfg::kTileBytes, p.lse2 + vec, 512, &bar_full[st]);
-          bulk_load(stage + 2 * Cfg::kTileBytes + 512, p.Dvec + vec, 512, &bar_full[st]);
-          issued[st]++;
-        }
-      } else {
-        for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-          tma_load_4d(smem + Cfg::kDqOffQ + hf * kHalfTileBytes, &p.tmap_q, &bar_fixed, hf * 64, h, tile * kTile, b);
-          tma_load_4d(smem + Cfg::kDqOffDO + hf * kHalfTileBytes, &p.tmap_do, &bar_fixed, hf * 64, h, tile * kTile, b);
-        }
-        for (int j = 0; j < n_it && ok; ++j) {
-          const int st = j % NST, n = j / NST;
-          if (n > 0) ok = mbar_wait(&bar_empty[st], (n - 1) & 1, ctx, 1);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&bar_full[st], Cfg::kTileBytes);
-          for (int hf = 0; hf < Cfg::kHalves; ++hf)
-            tma_load_4d(smem + Cfg::kDqOffK + st * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_k, &bar_full[st],
-                        hf * 64, kvh, j * kTile, b);
-          issued[st]++;
-          const int vs = j & 1, vn = j >> 1;
-          if (vn > 0) ok = mbar_wait(&bar_vempty[vs], (vn - 1) & 1, ctx, 2);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&bar_vfull[vs], Cfg::kTileBytes);
-          for (int hf = 0; hf < Cfg::kHalves; ++hf)
-            tma_load_4d(smem + Cfg::kDqOffV + vs * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v, &bar_vfull[vs],
-                        hf * 64, kvh, j * kTile, b);
-          vissued[vs]++;
-        }
-      }
-      // Wait until every stage is released, so no MMA commit arrives after exit.
-      for (int s = 0; s < 3 && ok; ++s)
-        if (issued[s] > 0) ok = mbar_wait(&bar_empty[s], (issued[s] - 1) & 1, ctx, 3);
-      for (int s = 0; s < 2 && ok; ++s)
-        if (vissued[s] > 0) ok = mbar_wait(&bar_vempty[s], (vissued[s] - 1) & 1, ctx, 4);
-      if (!ok) {
-        mbar_wait_drain(&bar_fixed, 0, p.budget_ns);
-        for (int s = 0; s < 3; ++s)
-          if (issued[s] > 0) mbar_wait_drain(&bar_full[s], (issued[s] - 1) & 1, p.budget_ns);
-        for (int s = 0; s < 2; ++s)
-          if (vissued[s] > 0) mbar_wait_drain(&bar_vfull[s], (vissued[s] - 1) & 1, p.budget_ns);
-      }
-    }
-  } else if (warp == 1) {
-    // ============================================================ MMA issuer
-    if (lane == 0) {
-      bool issued_any = false;
-      const uint32_t colDP = is_dkv ? Cfg::kKvColDP : Cfg::kDqColDP;
-      // S (or S^T) of iteration i into S buffer i % NS.
-      auto issue_S = [&](int i) -> bool {
-        const int st = i % NST;
-        if (!mbar_wait(&bar_full[st], (i / NST) & 1, ctx, 11)) return false;
-        tc_fence_after();
-        const uint32_t dst = tmem + (i % NS) * 128;
-        uint32_t a, bb;
-        if (is_dkv) {
-          a = smem_u32(smem + Cfg::kKvOffK);
-          bb = smem_u32(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes);
-        } else {
-          a = smem_u32(smem + Cfg::kDqOffQ);
-          bb = smem_u32(smem + Cfg::kDqOffK + st * Cfg::kTileBytes);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-          mma_ss(dst, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(bb + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-        }
-        issued_any = true;
-        return true;
-      };
-      // dP (or dP^T) of iteration i into the dP buffer.
-      auto issue_dP = [&](int i) -> bool {
-        uint32_t a, bb;
-        if (is_dkv) {
-          const int st = i % NST;
-          if (!mbar_wait(&bar_full[st], (i / NST) & 1, ctx, 13)) return false;
-          a = smem_u32(smem + Cfg::kKvOffV);
-          bb = smem_u32(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes + Cfg::kTileBytes);
-        } else {
-          const int vs = i & 1;
-          if (!mbar_wait(&bar_vfull[vs], (i >> 1) & 1, ctx, 13)) return false;
-          a = smem_u32(smem + Cfg::kDqOffDO);
-          bb = smem_u32(smem + Cfg::kDqOffV + vs * Cfg::kTileBytes);
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-          mma_ss(tmem + colDP, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(bb + off, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
-        }
-        issued_any = true;
-        if (!is_dkv) mma_commit(&bar_vempty[i & 1]);
-        return true;
-      };
-      // Gradient MMAs of iteration i from the bf16 P/dS in S buffer i % NS.
-      auto issue_grad = [&](int i) {
-        const uint32_t sbuf = tmem + (i % NS) * 128;
-        const int st = i % NST;
-        if (is_dkv) {
-          const uint32_t sQ = smem_u32(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes);
-          const uint32_t sDO = sQ + Cfg::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-            mma_ts(tmem + Cfg::kKvColDV, sbuf + kk * 16, sdesc_sw128(sDO + kk * 2048, kHalfTileBytes, 1024),
-                   idesc_g, acc);
-            mma_ts(tmem + Cfg::kKvColDK, sbuf + kk * 16 + 8, sdesc_sw128(sQ + kk * 2048, kHalfTileBytes, 1024),
-                   idesc_g, acc);
-          }
-        } else {
-          const uint32_t kb = smem_u32(smem + Cfg::kDqOffK + st * Cfg::kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + Cfg::kDqColAcc, sbuf + kk * 16, sdesc_sw128(kb + kk * 2048, kHalfTileBytes, 1024), idesc_g,
-                   (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&bar_empty[st]);
-      };
-
-      bool ok = mbar_wait(&bar_fixed, 0, ctx, 10);
-      if (ok) ok = issue_S(0);
-      if (ok) ok = issue_dP(0);
-      if (ok) mma_commit(&bar_s);
-      for (int it = 0; it < n_it && ok; ++it) {
-        const bool has_next = it + 1 < n_it;
-        if (NS == 2 && has_next) {
-          ok = issue_S(it + 1);
-          if (!ok) break;
-        }
-        ok = mbar_wait(&bar_dpfree, it & 1, ctx, 14);
-        if (!ok) break;
-        if (has_next) {
-          ok = issue_dP(it + 1);
-          if (!ok) break;
-          if (NS == 2) mma_commit(&bar_s);
-        }
-        ok = mbar_wait(&bar_p, it & 1, ctx, 12);
-        if (!ok) break;
-        tc_fence_after();
-        issue_grad(it);
-        if (NS == 1 && has_next) {
-          ok = issue_S(it + 1);
-          if (!ok) break;
-          mma_commit(&bar_s);
-        }
-      }
-      if (ok) {
-        mma_commit(&bar_fin);
-      } else if (issued_any) {
-        mma_commit(&bar_drain);
-        mbar_wait_drain(&bar_drain, 0, p.budget_ns);
-      }
-    }
-  } else {
-    // ============================================================ compute warpgroups
-    const int wg = (warp - 2) >> 2;  // 0 or 1: score columns [wg*64, wg*64+64)
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const float sl2 = p.scale_log2;
-    bool ok = true;
-    if (is_dkv) {
-      const int k_idx = tile * kTile + row;
-      const uint32_t tDP = tmem + lane_base + Cfg::kKvColDP + wg * 64;
-      for (int it = 0; it < n_it; ++it) {
-        const int st = it % NST;
-        const int qt = i0 + it % ni;
-        ok = warp_wait(&bar_s, it & 1, ctx, 20);
-        if (!ok) break;
-        ok = warp_wait(&bar_full[st], (it / NST) & 1, ctx, 22);  // -LSE2 / D vectors of this stage
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t tS = tmem + lane_base + (it % NS) * 128 + wg * 64;
-        const float* vnl2 = reinterpret_cast<const float*>(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes +
-                                                           2 * Cfg::kTileBytes) + wg * 64;
-        const float* vD = vnl2 + kTile;
-        // Query columns visible to this key row: [lo, hi) in this warpgroup's 64-column frame.
-        const int hi_tile = min(kTile, p.T - qt * kTile);
-        const bool diag = p.causal && qt == tile;
-        const int lo = (diag ? row : 0) - wg * 64;
-        const int hi = hi_tile - wg * 64;
-        if (diag || hi_tile < kTile)
-          compute_tile<true, true>(tS, tDP, vnl2, vD, 0.f, 0.f, sl2, lo, hi, &bar_dpfree);
-        else
-          compute_tile<true, false>(tS, tDP, vnl2, vD, 0.f, 0.f, sl2, lo, hi, &bar_dpfree);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bar_p);
-      }
-      if (ok) ok = warp_wait(&bar_fin, 0, ctx, 21);
-      if (ok) {
-        tc_fence_after();
-        const bool valid = k_idx < p.T;
-        const size_t off = ((static_cast<size_t>(b) * p.T + (valid ? k_idx : 0)) * p.Hkv + kvh) * D;
-        if (wg == 0)
-          store_row_bf16<D>(tmem + lane_base + Cfg::kKvColDV, reinterpret_cast<__nv_bfloat16*>(p.dv) + off, 1.f,
-                            valid);
-        else
-          store_row_bf16<D>(tmem + lane_base + Cfg::kKvColDK, reinterpret_cast<__nv_bfloat16*>(p.dk) + off, p.scale,
-                            valid);
-      }
-    } else {
-      const int q_idx = tile * kTile + row;
-      const bool valid = q_idx < p.T;
-      const size_t vec_idx = (static_cast<size_t>(b) * p.Hq + h) * p.Tpad + q_idx;  // < B*Hq*Tpad
-      const float nl2_r = p.lse2[vec_idx];
-      const float D_r = p.Dvec[vec_idx];
-      const uint32_t tDP = tmem + lane_base + Cfg::kDqColDP + wg * 64;
-      const bool tile_ragged = (tile + 1) * kTile > p.T;
-      for (int j = 0; j < n_it; ++j) {
-        ok = warp_wait(&bar_s, j & 1, ctx, 20);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t tS = tmem + lane_base + (j & 1) * 128 + wg * 64;
-        // Key columns visible to this query row: [0, lim) in this warpgroup's 64-column frame.
-        const bool diag = p.causal && j == tile;
-        const bool kv_ragged = !p.causal && (j + 1) * kTile > p.T;
-        int lim_tile = kTile;
-        if (diag) lim_tile = row + 1;
-        if (kv_ragged) lim_tile = p.T - j * kTile;
-        const int lim = (valid ? lim_tile : 0) - wg * 64;
-        if (diag || kv_ragged || tile_ragged)
-          compute_tile<false, true>(tS, tDP, nullptr, nullptr, nl2_r, D_r, sl2, 0, lim, &bar_dpfree);
-        else
-          compute_tile<false, false>(tS, tDP, nullptr, nullptr, nl2_r, D_r, sl2, 0, lim, &bar_dpfree);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bar_p);
-      }
-      if (ok) ok = warp_wait(&bar_fin, 0, ctx, 21);
-      if (ok) {
-        tc_fence_after();
-        const size_t off = ((static_cast<size_t>(b) * p.T + (valid ? q_idx : 0)) * p.Hq + h) * D;
-        store_row_bf16<D / 2>(tmem + lane_base + Cfg::kDqColAcc + wg * (D / 2),
-                              reinterpret_cast<__nv_bfloat16*>(p.dq) + off + wg * (D / 2), p.scale, valid);
-      }
-    }
-  }
+  if (is_dkv)
+    run_task<D, true>(p, smem, bars, tmem, ctx, t, warp, lane);
+  else
+    run_task<D, false>(p, smem, bars, tmem, ctx, t, warp, lane);
 
   tc_fence_before();
   __syncthreads();

@@ -136,3 +136,23 @@ def test_bad_arguments_on_gpu():
         gqa.attn_fwd(q[:, :, :5].contiguous(), k, v)  # Hq=5 over Hkv=2
     assert e.value.code == gqa.GQA_ERR_INVALID_ARG
     assert gqa.attn_sync_status() == gqa.GQA_OK
+
+
+@pytest.mark.parametrize("name", ["c2", "c5"])
+def test_repeated_steps_no_timeout(name):
+    """Pipeline barriers under repetition: 40 fwd+bwd steps, every one must end with
+    a clean status word and the same bytes (a phase race shows up as a timeout or
+    as different bits)."""
+    w = WORKLOADS[name]
+    q, k, v, dout = (x.to(DEV) for x in workload_inputs(w))
+    ref = None
+    for i in range(40):
+        o, lse = gqa.attn_fwd(q, k, v, causal=True)
+        dq, dk, dv = gqa.attn_bwd(q, k, v, o, lse, dout, causal=True)
+        assert gqa.attn_sync_status() == gqa.GQA_OK, f"step {i}: {gqa.attn_last_error()}"
+        cur = [t.clone() for t in (o, lse, dq, dk, dv)]
+        if ref is None:
+            ref = cur
+        else:
+            for a, b in zip(ref, cur):
+                assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f"step {i}"
