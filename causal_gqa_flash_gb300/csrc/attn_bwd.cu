@@ -137,21 +137,26 @@ template <int D>
 struct MainCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = kHalves * kHalfTileBytes;
-  // dQ task: [Q][dO], K ring of 3, V ring of 2
+  static constexpr int kAuxBytes = 4096;  // 128 rows x 16 bf16, unswizzled K-major (one K-step)
+  // dQ task: [Q][dO][QX][DX][ONES], K ring, V ring
   static constexpr int kDqKStages = 3;
-  static constexpr int kDqVStages = 2;
+  static constexpr int kDqVStages = (D == 64) ? 2 : 1;
   static constexpr int kDqOffQ = 0;
   static constexpr int kDqOffDO = kTileBytes;
-  static constexpr int kDqOffK = 2 * kTileBytes;
+  static constexpr int kDqOffQX = 2 * kTileBytes;
+  static constexpr int kDqOffDX = kDqOffQX + kAuxBytes;
+  static constexpr int kDqOffOnes = kDqOffDX + kAuxBytes;
+  static constexpr int kDqOffK = kDqOffOnes + kAuxBytes;
   static constexpr int kDqOffV = kDqOffK + kDqKStages * kTileBytes;
   static constexpr int kDqBytes = kDqOffV + kDqVStages * kTileBytes;
-  // dK/dV task: [K][V], stages of [Q][dO][-LSE2 x128][D x128]
+  // dK/dV task: [K][V][ONES], stages of [Q][dO][QX][DX]
   static constexpr int kKvNS = (D == 64) ? 2 : 1;       // S buffers
   static constexpr int kKvStages = (D == 64) ? 3 : 2;   // Q/dO stages
-  static constexpr int kStageBytes = 2 * kTileBytes + 1024;
+  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kAuxBytes;
   static constexpr int kKvOffK = 0;
   static constexpr int kKvOffV = kTileBytes;
-  static constexpr int kKvOffStage = 2 * kTileBytes;
+  static constexpr int kKvOffOnes = 2 * kTileBytes;
+  static constexpr int kKvOffStage = 2 * kTileBytes + kAuxBytes;
   static constexpr int kKvBytes = kKvOffStage + kKvStages * kStageBytes;
   static constexpr int kUsed = (kDqBytes > kKvBytes ? kDqBytes : kKvBytes) + 1024;
   static constexpr int kSmemBytes = kUsed > kOneCtaPerSmSmem ? kUsed : kOneCtaPerSmSmem;
@@ -162,6 +167,29 @@ struct MainCfg {
   static constexpr uint32_t kKvColDV = kKvColDP + 128;
   static constexpr uint32_t kKvColDK = kKvColDV + D;
 };
+
+// Unswizzled K-major layout of a 128 x 16 bf16 operand: byte offset of (row, 8-column half).
+__device__ __forceinline__ uint32_t aux_off(int row, int half) {
+  return static_cast<uint32_t>((row >> 3) * 256 + half * 128 + (row & 7) * 16);
+}
+
+// The extra K-step that folds a per-row value into an accumulator: a row of this
+// operand is [hi(x), lo(x), 0, ...] with hi + lo = x to ~2^-17 relative, and it
+// meets a row [1, 1, 0, ...] of the ONES operand, adding x.
+__device__ __forceinline__ void write_aux_row(uint8_t* tile, int row, float x) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+  const uint32_t w0 = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
+                      (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
+  *reinterpret_cast<uint4*>(tile + aux_off(row, 0)) = make_uint4(w0, 0u, 0u, 0u);
+  *reinterpret_cast<uint4*>(tile + aux_off(row, 1)) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+__device__ __forceinline__ void write_ones_row(uint8_t* tile, int row) {
+  const uint32_t one2 = 0x3F803F80u;  // bf16 1.0 in both halves
+  *reinterpret_cast<uint4*>(tile + aux_off(row, 0)) = make_uint4(one2, 0u, 0u, 0u);
+  *reinterpret_cast<uint4*>(tile + aux_off(row, 1)) = make_uint4(0u, 0u, 0u, 0u);
+}
 
 // Store `ncols` (multiple of 32) fp32 columns of this thread's row as bf16 to dst.
 template <int NCOLS>
@@ -183,66 +211,31 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* ds
   }
 }
 
-// One 16-column round of a dK/dV tile (row = key, columns = queries).
-// nl2/dv: this round's 16 values of -LSE2 and D (per query). Visible iff lo <= col < hi.
-template <bool MASKED>
-__device__ __forceinline__ void dkv_round(const uint32_t (&s)[16], const uint32_t (&dp)[16], const float* nl2,
-                                          const float* dv, float sl2, int col0, int lo, int hi, uint32_t tS_round) {
+// One 16-column round. The accumulators already hold S - LSE2/c and dP - D, so
+// P = 2^(c * s') and dS = P * dp'. Columns outside [lo, hi) are masked (MASKED only).
+// dK/dV rounds write bf16 P to columns [0, 8) and dS to [8, 16) of the round;
+// dQ rounds write dS to [0, 8).
+template <bool DKV, bool MASKED>
+__device__ __forceinline__ void tile_round(const uint32_t (&s)[16], const uint32_t (&dp)[16], float sl2, int col0,
+                                           int lo, int hi, uint32_t tS_round) {
   uint32_t pk[8], dk[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * i]), sl2, nl2[2 * i]));
-    float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * i + 1]), sl2, nl2[2 * i + 1]));
+    float p0 = ex2_approx(__uint_as_float(s[2 * i]) * sl2);
+    float p1 = ex2_approx(__uint_as_float(s[2 * i + 1]) * sl2);
     if (MASKED) {
       const int c = col0 + 2 * i;
       p0 = (c >= lo && c < hi) ? p0 : 0.f;
       p1 = (c + 1 >= lo && c + 1 < hi) ? p1 : 0.f;
     }
-    const float d0 = p0 * (__uint_as_float(dp[2 * i]) - dv[2 * i]);
-    const float d1 = p1 * (__uint_as_float(dp[2 * i + 1]) - dv[2 * i + 1]);
-    pk[i] = pack_bf16x2(p0, p1);
-    dk[i] = pack_bf16x2(d0, d1);
+    if (DKV) pk[i] = pack_bf16x2(p0, p1);
+    dk[i] = pack_bf16x2(p0 * __uint_as_float(dp[2 * i]), p1 * __uint_as_float(dp[2 * i + 1]));
   }
-  tmem_st8(tS_round, pk);
-  tmem_st8(tS_round + 8, dk);
-}
-
-// One 16-column round of a dQ tile (row = query, columns = keys). Visible iff col < lim.
-template <bool MASKED>
-__device__ __forceinline__ void dq_round(const uint32_t (&s)[16], const uint32_t (&dp)[16], float nl2_r, float D_r,
-                                         float sl2, int col0, int lim, uint32_t tS_round) {
-  uint32_t dk[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * i]), sl2, nl2_r));
-    float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * i + 1]), sl2, nl2_r));
-    if (MASKED) {
-      const int c = col0 + 2 * i;
-      p0 = c < lim ? p0 : 0.f;
-      p1 = c + 1 < lim ? p1 : 0.f;
-    }
-    dk[i] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * i]) - D_r), p1 * (__uint_as_float(dp[2 * i + 1]) - D_r));
-  }
-  tmem_st8(tS_round, dk);
-}
-
-// One round of either kind; DKV rounds read this round's -LSE2 / D vectors from shared memory.
-template <bool DKV, bool MASKED>
-__device__ __forceinline__ void tile_round(int r, const uint32_t (&s)[16], const uint32_t (&dp)[16],
-                                           const float* vnl2, const float* vD, float nl2_r, float D_r, float sl2,
-                                           int lo, int hi, uint32_t tS) {
   if (DKV) {
-    float nl[16], dv[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 a = *reinterpret_cast<const float4*>(vnl2 + r * 16 + 4 * i);
-      const float4 b = *reinterpret_cast<const float4*>(vD + r * 16 + 4 * i);
-      nl[4 * i] = a.x; nl[4 * i + 1] = a.y; nl[4 * i + 2] = a.z; nl[4 * i + 3] = a.w;
-      dv[4 * i] = b.x; dv[4 * i + 1] = b.y; dv[4 * i + 2] = b.z; dv[4 * i + 3] = b.w;
-    }
-    dkv_round<MASKED>(s, dp, nl, dv, sl2, r * 16, lo, hi, tS + r * 16);
+    tmem_st8(tS_round, pk);
+    tmem_st8(tS_round + 8, dk);
   } else {
-    dq_round<MASKED>(s, dp, nl2_r, D_r, sl2, r * 16, hi, tS + r * 16);
+    tmem_st8(tS_round, dk);
   }
 }
 
@@ -250,27 +243,27 @@ __device__ __forceinline__ void tile_round(int r, const uint32_t (&s)[16], const
 // the TMEM load of round r+2 in flight while round r+1 is computed. Signals
 // dp_free as soon as every dP column of this warpgroup is in registers.
 template <bool DKV, bool MASKED>
-__device__ __forceinline__ void compute_tile(uint32_t tS, uint32_t tDP, const float* vnl2, const float* vD,
-                                             float nl2_r, float D_r, float sl2, int lo, int hi, uint64_t* bar_dpfree) {
+__device__ __forceinline__ void compute_tile(uint32_t tS, uint32_t tDP, float sl2, int lo, int hi,
+                                             uint64_t* bar_dpfree) {
   uint32_t sa[16], da[16], sb[16], db[16];
   tmem_ld16(tS, sa);
   tmem_ld16(tDP, da);
   tmem_ld16(tS + 16, sb);
   tmem_ld16(tDP + 16, db);
   tmem_wait_ld();
-  tile_round<DKV, MASKED>(0, sa, da, vnl2, vD, nl2_r, D_r, sl2, lo, hi, tS);
+  tile_round<DKV, MASKED>(sa, da, sl2, 0, lo, hi, tS);
   tmem_ld16(tS + 32, sa);
   tmem_ld16(tDP + 32, da);
-  tile_round<DKV, MASKED>(1, sb, db, vnl2, vD, nl2_r, D_r, sl2, lo, hi, tS);
+  tile_round<DKV, MASKED>(sb, db, sl2, 16, lo, hi, tS + 16);
   tmem_wait_ld();
   tmem_ld16(tS + 48, sb);
   tmem_ld16(tDP + 48, db);
-  tile_round<DKV, MASKED>(2, sa, da, vnl2, vD, nl2_r, D_r, sl2, lo, hi, tS);
+  tile_round<DKV, MASKED>(sa, da, sl2, 32, lo, hi, tS + 32);
   tmem_wait_ld();
   // every dP column of this warpgroup is in registers: the MMA may overwrite dP
   tc_fence_before();
   mbar_arrive(bar_dpfree);
-  tile_round<DKV, MASKED>(3, sb, db, vnl2, vD, nl2_r, D_r, sl2, lo, hi, tS);
+  tile_round<DKV, MASKED>(sb, db, sl2, 48, lo, hi, tS + 48);
 }
 
 // `p[it & 1]` ("bf16 P/dS of iteration it are in TMEM") alternates between two
@@ -300,74 +293,128 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
   using Cfg = MainCfg<D>;
   constexpr int NS = DKV ? Cfg::kKvNS : 2;                    // S buffers in TMEM
   constexpr int NST = DKV ? Cfg::kKvStages : Cfg::kDqKStages;  // main ring depth
+  constexpr int NV = Cfg::kDqVStages;                         // dQ V ring depth
   constexpr uint32_t colDP = DKV ? Cfg::kKvColDP : Cfg::kDqColDP;
   constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: N = 128
   constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);    // gradients: N = D, B MN-major
   constexpr uint32_t kTileD = Cfg::kTileBytes >> 4;             // tile stride, descriptor units
   constexpr uint32_t kStageD = Cfg::kStageBytes >> 4;
   const int n_it = t.n_it;
+  const float inv_sl2 = 1.f / p.scale_log2;
 
   if (warp == 0) {
-    // ============================================================ TMA producer
-    if (lane != 0) return;
-    tma_prefetch_desc(&p.tmap_q);
-    tma_prefetch_desc(&p.tmap_k);
-    tma_prefetch_desc(&p.tmap_v);
-    tma_prefetch_desc(&p.tmap_do);
+    // ============================================================ producer warp
+    // Lane 0 issues TMA and waits; all 32 lanes write the unswizzled ONES / QX / DX
+    // operands (4 rows each) from the workspace's -LSE2 and D.
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tmap_q);
+      tma_prefetch_desc(&p.tmap_k);
+      tma_prefetch_desc(&p.tmap_v);
+      tma_prefetch_desc(&p.tmap_do);
+    }
     int issued[3] = {0, 0, 0}, vissued[2] = {0, 0};
     bool ok = true;
-    mbar_arrive_expect_tx(&bars.fixed, 2 * Cfg::kTileBytes);
+    const size_t vec_bh0 = (static_cast<size_t>(t.b) * p.Hq) * p.Tpad;
+    if (lane == 0) mbar_arrive_expect_tx(&bars.fixed, 2 * Cfg::kTileBytes);
     if (DKV) {
-      for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-        tma_load_4d(smem + Cfg::kKvOffK + hf * kHalfTileBytes, &p.tmap_k, &bars.fixed, hf * 64, t.kvh,
-                    t.tile * kTile, t.b);
-        tma_load_4d(smem + Cfg::kKvOffV + hf * kHalfTileBytes, &p.tmap_v, &bars.fixed, hf * 64, t.kvh,
-                    t.tile * kTile, t.b);
-      }
+      if (lane == 0)
+        for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+          tma_load_4d(smem + Cfg::kKvOffK + hf * kHalfTileBytes, &p.tmap_k, &bars.fixed, hf * 64, t.kvh,
+                      t.tile * kTile, t.b);
+          tma_load_4d(smem + Cfg::kKvOffV + hf * kHalfTileBytes, &p.tmap_v, &bars.fixed, hf * 64, t.kvh,
+                      t.tile * kTile, t.b);
+        }
+      // -LSE2 and D of the next stage's 128 query rows, 4 per lane, fetched one
+      // stage ahead so their latency hides behind the wait for a free stage.
+      float vnl[4], vd[4];
+      auto fetch = [&](int it) {
+        const int hq = t.kvh * p.G + it / t.ni;
+        const int qt = t.i0 + it % t.ni;
+        const size_t vec = vec_bh0 + static_cast<size_t>(hq) * p.Tpad + static_cast<size_t>(qt) * kTile + lane;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          vnl[k] = __ldg(p.lse2 + vec + 32 * k);
+          vd[k] = __ldg(p.Dvec + vec + 32 * k);
+        }
+      };
+      if (n_it > 0) fetch(0);
+      for (int r = lane; r < kTile; r += 32) write_ones_row(smem + Cfg::kKvOffOnes, r);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.fixed);
       for (int it = 0; it < n_it && ok; ++it) {
         const int st = it % NST, n = it / NST;
-        if (n > 0) ok = mbar_wait(&bars.empty[st], (n - 1) & 1, ctx, 1);
+        if (n > 0 && lane == 0) ok = mbar_wait(&bars.empty[st], (n - 1) & 1, ctx, 1);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         const int hq = t.kvh * p.G + it / t.ni;
         const int qt = t.i0 + it % t.ni;
         uint8_t* stage = smem + Cfg::kKvOffStage + st * Cfg::kStageBytes;
-        mbar_arrive_expect_tx(&bars.full[st], 2 * Cfg::kTileBytes + 1024);
-        for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-          tma_load_4d(stage + hf * kHalfTileBytes, &p.tmap_q, &bars.full[st], hf * 64, hq, qt * kTile, t.b);
-          tma_load_4d(stage + Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_do, &bars.full[st], hf * 64, hq,
-                      qt * kTile, t.b);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars.full[st], 2 * Cfg::kTileBytes);
+          for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+            tma_load_4d(stage + hf * kHalfTileBytes, &p.tmap_q, &bars.full[st], hf * 64, hq, qt * kTile, t.b);
+            tma_load_4d(stage + Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_do, &bars.full[st], hf * 64, hq,
+                        qt * kTile, t.b);
+          }
         }
-        const size_t vec = (static_cast<size_t>(t.b) * p.Hq + hq) * p.Tpad + static_cast<size_t>(qt) * kTile;
-        bulk_load(stage + 2 * Cfg::kTileBytes, p.lse2 + vec, 512, &bars.full[st]);
-        bulk_load(stage + 2 * Cfg::kTileBytes + 512, p.Dvec + vec, 512, &bars.full[st]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          write_aux_row(stage + 2 * Cfg::kTileBytes, lane + 32 * k, vnl[k] * inv_sl2);
+          write_aux_row(stage + 2 * Cfg::kTileBytes + Cfg::kAuxBytes, lane + 32 * k, -vd[k]);
+        }
+        if (it + 1 < n_it) fetch(it + 1);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.full[st]);
         issued[st]++;
       }
     } else {
-      for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-        tma_load_4d(smem + Cfg::kDqOffQ + hf * kHalfTileBytes, &p.tmap_q, &bars.fixed, hf * 64, t.h,
-                    t.tile * kTile, t.b);
-        tma_load_4d(smem + Cfg::kDqOffDO + hf * kHalfTileBytes, &p.tmap_do, &bars.fixed, hf * 64, t.h,
-                    t.tile * kTile, t.b);
+      if (lane == 0)
+        for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+          tma_load_4d(smem + Cfg::kDqOffQ + hf * kHalfTileBytes, &p.tmap_q, &bars.fixed, hf * 64, t.h,
+                      t.tile * kTile, t.b);
+          tma_load_4d(smem + Cfg::kDqOffDO + hf * kHalfTileBytes, &p.tmap_do, &bars.fixed, hf * 64, t.h,
+                      t.tile * kTile, t.b);
+        }
+      const size_t vec = vec_bh0 + static_cast<size_t>(t.h) * p.Tpad + static_cast<size_t>(t.tile) * kTile + lane;
+      float vnl[4], vd[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        vnl[k] = __ldg(p.lse2 + vec + 32 * k);
+        vd[k] = __ldg(p.Dvec + vec + 32 * k);
       }
-      for (int j = 0; j < n_it && ok; ++j) {
-        const int st = j % NST, n = j / NST;
-        if (n > 0) ok = mbar_wait(&bars.empty[st], (n - 1) & 1, ctx, 1);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bars.full[st], Cfg::kTileBytes);
-        for (int hf = 0; hf < Cfg::kHalves; ++hf)
-          tma_load_4d(smem + Cfg::kDqOffK + st * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_k, &bars.full[st],
-                      hf * 64, t.kvh, j * kTile, t.b);
-        issued[st]++;
-        const int vs = j & 1, vn = j >> 1;
-        if (vn > 0) ok = mbar_wait(&bars.vempty[vs], (vn - 1) & 1, ctx, 2);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bars.vfull[vs], Cfg::kTileBytes);
-        for (int hf = 0; hf < Cfg::kHalves; ++hf)
-          tma_load_4d(smem + Cfg::kDqOffV + vs * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v, &bars.vfull[vs],
-                      hf * 64, t.kvh, j * kTile, t.b);
-        vissued[vs]++;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        write_ones_row(smem + Cfg::kDqOffOnes, lane + 32 * k);
+        write_aux_row(smem + Cfg::kDqOffQX, lane + 32 * k, vnl[k] * inv_sl2);
+        write_aux_row(smem + Cfg::kDqOffDX, lane + 32 * k, -vd[k]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars.fixed);
+        for (int j = 0; j < n_it && ok; ++j) {
+          const int st = j % NST, n = j / NST;
+          if (n > 0) ok = mbar_wait(&bars.empty[st], (n - 1) & 1, ctx, 1);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars.full[st], Cfg::kTileBytes);
+          for (int hf = 0; hf < Cfg::kHalves; ++hf)
+            tma_load_4d(smem + Cfg::kDqOffK + st * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_k, &bars.full[st],
+                        hf * 64, t.kvh, j * kTile, t.b);
+          issued[st]++;
+          const int vs = j % NV, vn = j / NV;
+          if (vn > 0) ok = mbar_wait(&bars.vempty[vs], (vn - 1) & 1, ctx, 2);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars.vfull[vs], Cfg::kTileBytes);
+          for (int hf = 0; hf < Cfg::kHalves; ++hf)
+            tma_load_4d(smem + Cfg::kDqOffV + vs * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v,
+                        &bars.vfull[vs], hf * 64, t.kvh, j * kTile, t.b);
+          vissued[vs]++;
+        }
       }
     }
+    if (lane != 0) return;
     // Wait until every stage is released, so no MMA commit arrives after exit.
     for (int s2 = 0; s2 < 3 && ok; ++s2)
       if (issued[s2] > 0) ok = mbar_wait(&bars.empty[s2], (issued[s2] - 1) & 1, ctx, 3);
@@ -384,27 +431,39 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
     // ============================================================ MMA issuer
     if (lane != 0) return;
     // Base descriptors (stage / slot 0); a stage or K-step moves the start address only.
-    uint64_t dA_S, dA_P, dB_S, dB_P, dG1, dG2;
-    uint32_t strideB_S, strideB_P;
+    uint64_t dA_S, dA_P, dB_S, dB_P, dG1, dG2, dXA_S, dXA_P, dXB_S, dXB_P;
+    uint32_t strideB_S, strideB_P, strideX;
     if (DKV) {
       const uint32_t st0 = smem_u32(smem + Cfg::kKvOffStage);
+      const uint64_t ones = sdesc_noswz(smem_u32(smem + Cfg::kKvOffOnes), 128, 256);
       dA_S = sdesc_sw128(smem_u32(smem + Cfg::kKvOffK), 16, 1024);             // K
       dA_P = sdesc_sw128(smem_u32(smem + Cfg::kKvOffV), 16, 1024);             // V
       dB_S = sdesc_sw128(st0, 16, 1024);                                       // Q   (K-major)
       dB_P = sdesc_sw128(st0 + Cfg::kTileBytes, 16, 1024);                     // dO  (K-major)
       dG1 = sdesc_sw128(st0 + Cfg::kTileBytes, kHalfTileBytes, 1024);          // dO  (MN-major) for dV
       dG2 = sdesc_sw128(st0, kHalfTileBytes, 1024);                            // Q   (MN-major) for dK
+      dXA_S = ones;                                                            // ONES x QX^T  -> -LSE2/c
+      dXA_P = ones;                                                            // ONES x DX^T  -> -D
+      dXB_S = sdesc_noswz(st0 + 2 * Cfg::kTileBytes, 128, 256);
+      dXB_P = sdesc_noswz(st0 + 2 * Cfg::kTileBytes + Cfg::kAuxBytes, 128, 256);
       strideB_S = kStageD;
       strideB_P = kStageD;
+      strideX = kStageD;
     } else {
+      const uint64_t ones = sdesc_noswz(smem_u32(smem + Cfg::kDqOffOnes), 128, 256);
       dA_S = sdesc_sw128(smem_u32(smem + Cfg::kDqOffQ), 16, 1024);             // Q
       dA_P = sdesc_sw128(smem_u32(smem + Cfg::kDqOffDO), 16, 1024);            // dO
       dB_S = sdesc_sw128(smem_u32(smem + Cfg::kDqOffK), 16, 1024);             // K slot 0 (K-major)
       dB_P = sdesc_sw128(smem_u32(smem + Cfg::kDqOffV), 16, 1024);             // V slot 0 (K-major)
       dG1 = sdesc_sw128(smem_u32(smem + Cfg::kDqOffK), kHalfTileBytes, 1024);  // K slot 0 (MN-major) for dQ
       dG2 = 0;
+      dXA_S = sdesc_noswz(smem_u32(smem + Cfg::kDqOffQX), 128, 256);           // QX x ONES^T -> -LSE2/c
+      dXA_P = sdesc_noswz(smem_u32(smem + Cfg::kDqOffDX), 128, 256);           // DX x ONES^T -> -D
+      dXB_S = ones;
+      dXB_P = ones;
       strideB_S = kTileD;
       strideB_P = kTileD;
+      strideX = 0;
     }
     bool issued_any = false;
     auto issue_S = [&](int i) -> bool {
@@ -416,23 +475,27 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(dst, dA_S + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+      mma_ss(dst, dXA_S, dXB_S + st * strideX, idesc_s, 1u);
       issued_any = true;
       return true;
     };
     auto issue_dP = [&](int i) -> bool {
-      int slot;
+      int slot, xst;
       if (DKV) {
         slot = i % NST;
+        xst = slot;
         if (!mbar_wait(&bars.full[slot], (i / NST) & 1, ctx, 13)) return false;
       } else {
-        slot = i & 1;
-        if (!mbar_wait(&bars.vfull[slot], (i >> 1) & 1, ctx, 13)) return false;
+        slot = i % NV;
+        xst = 0;
+        if (!mbar_wait(&bars.vfull[slot], (i / NV) & 1, ctx, 13)) return false;
       }
       tc_fence_after();
       const uint64_t b0 = dB_P + slot * strideB_P;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(tmem + colDP, dA_P + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+      mma_ss(tmem + colDP, dXA_P, dXB_P + xst * strideX, idesc_s, 1u);
       issued_any = true;
       if (!DKV) mma_commit(&bars.vempty[slot]);
       return true;
@@ -502,26 +565,20 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
     if (DKV) {
       const int k_idx = t.tile * kTile + row;
       for (int it = 0; it < n_it; ++it) {
-        const int st = it % NST;
         const int qt = t.i0 + it % t.ni;
         ok = warp_wait(&bars.s, it & 1, ctx, 20);
         if (!ok) break;
-        ok = warp_wait(&bars.full[st], (it / NST) & 1, ctx, 22);  // -LSE2 / D vectors of this stage
-        if (!ok) break;
         tc_fence_after();
         const uint32_t tS = tmem + lane_base + (it % NS) * 128 + wg * 64;
-        const float* vnl2 = reinterpret_cast<const float*>(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes +
-                                                           2 * Cfg::kTileBytes) + wg * 64;
-        const float* vD = vnl2 + kTile;
         // Query columns visible to this key row: [lo, hi) in this warpgroup's 64-column frame.
         const int hi_tile = min(kTile, p.T - qt * kTile);
         const bool diag = p.causal && qt == t.tile;
         const int lo = (diag ? row : 0) - wg * 64;
         const int hi = hi_tile - wg * 64;
         if (diag || hi_tile < kTile)
-          compute_tile<true, true>(tS, tDP, vnl2, vD, 0.f, 0.f, sl2, lo, hi, &bars.dpfree);
+          compute_tile<true, true>(tS, tDP, sl2, lo, hi, &bars.dpfree);
         else
-          compute_tile<true, false>(tS, tDP, vnl2, vD, 0.f, 0.f, sl2, lo, hi, &bars.dpfree);
+          compute_tile<true, false>(tS, tDP, sl2, lo, hi, &bars.dpfree);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars.p[it & 1]);
@@ -541,9 +598,6 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
     } else {
       const int q_idx = t.tile * kTile + row;
       const bool valid = q_idx < p.T;
-      const size_t vec_idx = (static_cast<size_t>(t.b) * p.Hq + t.h) * p.Tpad + q_idx;  // < B*Hq*Tpad
-      const float nl2_r = p.lse2[vec_idx];
-      const float D_r = p.Dvec[vec_idx];
       const bool tile_ragged = (t.tile + 1) * kTile > p.T;
       for (int j = 0; j < n_it; ++j) {
         ok = warp_wait(&bars.s, j & 1, ctx, 20);
@@ -558,9 +612,9 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
         if (kv_ragged) lim_tile = p.T - j * kTile;
         const int lim = (valid ? lim_tile : 0) - wg * 64;
         if (diag || kv_ragged || tile_ragged)
-          compute_tile<false, true>(tS, tDP, nullptr, nullptr, nl2_r, D_r, sl2, 0, lim, &bars.dpfree);
+          compute_tile<false, true>(tS, tDP, sl2, 0, lim, &bars.dpfree);
         else
-          compute_tile<false, false>(tS, tDP, nullptr, nullptr, nl2_r, D_r, sl2, 0, lim, &bars.dpfree);
+          compute_tile<false, false>(tS, tDP, sl2, 0, lim, &bars.dpfree);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars.p[j & 1]);
@@ -590,9 +644,9 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
   const bool is_dkv = static_cast<int>(blockIdx.x) < n_dkv;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars.fixed, 1);
+    mbar_init(&bars.fixed, 2);  // TMA bytes + the producer warp's aux operands
     for (int s = 0; s < 3; ++s) {
-      mbar_init(&bars.full[s], 1);
+      mbar_init(&bars.full[s], is_dkv ? 2 : 1);  // dK/dV stages also carry aux operands
       mbar_init(&bars.empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {

@@ -305,6 +305,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// Unswizzled K-major operand of 16 columns (one K-step): 8-row x 16-byte core
+// matrices; the two 8-column halves are LBO apart, 8-row groups SBO apart.
+__device__ __forceinline__ uint64_t sdesc_noswz(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05; layout type 0 = no swizzle
+  return d;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
 // a_mn / b_mn select MN-major (1) instead of K-major (0) smem operands.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
