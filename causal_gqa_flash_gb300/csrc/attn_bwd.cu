@@ -51,20 +51,30 @@ __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x &
 
 // ============================================================================
 // Preprocess: D = rowsum(dO * O), -LSE2 = -LSE * log2(e); padded rows get 0.
-// Rows are visited in memory order (b, t, h); D/8 threads read one row with
-// 16-byte loads, so a warp reads contiguous bytes.
+// Rows are visited in (b, h, t) order: D/8 threads read one 128- or 256-byte
+// row of O and dO with 16-byte loads, and the LSE read and the D / -LSE2
+// writes of consecutive rows are consecutive in memory.
 // ============================================================================
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
   constexpr int TPR = D / 8;
-  const long long nrows = static_cast<long long>(p.B) * p.T * p.Hq;
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  const long long nrows = static_cast<long long>(p.B) * p.Hq * p.T;
   const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long r = gtid / TPR;
+  const long long r = gtid / TPR;  // ((b * Hq + h) * T + t)
   const int part = static_cast<int>(gtid % TPR);
   float acc = 0.f;
+  int t = 0;
+  long long bh = 0;
   if (r < nrows) {
-    const uint4 a = reinterpret_cast<const uint4*>(p.o)[r * TPR + part];
-    const uint4 c = reinterpret_cast<const uint4*>(p.dO)[r * TPR + part];
+    t = static_cast<int>(r % p.T);
+    bh = r / p.T;
+    const int h = static_cast<int>(bh % p.Hq);
+    const long long b = bh / p.Hq;
+    const long long row = (b * p.T + t) * p.Hq + h;  // memory row of O / dO
+    const uint4 a = reinterpret_cast<const uint4*>(p.o)[row * TPR + part];
+    const uint4 c = reinterpret_cast<const uint4*>(p.dO)[row * TPR + part];
     acc = bf16lo(a.x) * bf16lo(c.x);
     acc = fmaf(bf16hi(a.x), bf16hi(c.x), acc);
     acc = fmaf(bf16lo(a.y), bf16lo(c.y), acc);
@@ -77,13 +87,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (part == 0 && r < nrows) {
-    const int h = static_cast<int>(r % p.Hq);
-    const long long bt = r / p.Hq;
-    const int t = static_cast<int>(bt % p.T);
-    const int b = static_cast<int>(bt / p.T);
-    const size_t idx = (static_cast<size_t>(b) * p.Hq + h) * p.Tpad + t;
+    const size_t idx = static_cast<size_t>(bh) * p.Tpad + t;
     p.Dvec[idx] = acc;
-    p.lse2[idx] = -p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.T + t] * 1.4426950408889634f;
+    p.lse2[idx] = -p.lse[static_cast<size_t>(r)] * 1.4426950408889634f;
   }
   // Zero the padding rows [T, Tpad) of every (b, h).
   const int pad = p.Tpad - p.T;
@@ -91,8 +97,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
     const long long npad = static_cast<long long>(p.B) * p.Hq * pad;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long x = gtid; x < npad; x += stride) {
-      const long long bh = x / pad;
-      const size_t idx = static_cast<size_t>(bh) * p.Tpad + p.T + static_cast<int>(x % pad);
+      const long long pbh = x / pad;
+      const size_t idx = static_cast<size_t>(pbh) * p.Tpad + p.T + static_cast<int>(x % pad);
       p.Dvec[idx] = 0.f;
       p.lse2[idx] = 0.f;
     }
@@ -149,10 +155,21 @@ struct MainCfg {
   static constexpr int kDqOffK = kDqOffOnes + kAuxBytes;
   static constexpr int kDqOffV = kDqOffK + kDqKStages * kTileBytes;
   static constexpr int kDqBytes = kDqOffV + kDqVStages * kTileBytes;
-  // dK/dV task: [K][V][ONES], stages of [Q][dO][QX][DX]
+  // dK/dV task: [K][V][ONES], stages of [Q][dO][QX][DX] (d = 128) or
+  // [dO][ZERO][Q][QX][DX] (d = 64). At d = 64 the gradient MMAs compute [dV | dK]
+  // as one N = 128 chain over the block-diagonal operand [dO | 0] (P steps) and
+  // [0 | Q] (dS steps): the zero tile sits between dO and Q so one LBO spans both.
+  // N = 64 MMAs run well below the tensor peak when the compute warps stream
+  // TMEM at the same time; N = 128 ones do not.
+  static constexpr bool kBlockDiag = (D == 64);
   static constexpr int kKvNS = (D == 64) ? 2 : 1;       // S buffers
   static constexpr int kKvStages = (D == 64) ? 3 : 2;   // Q/dO stages
-  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kAuxBytes;
+  static constexpr int kStOffDO = kBlockDiag ? 0 : kTileBytes;
+  static constexpr int kStOffZ = kTileBytes;             // d = 64 only
+  static constexpr int kStOffQ = kBlockDiag ? 2 * kTileBytes : 0;
+  static constexpr int kStOffQX = kBlockDiag ? 3 * kTileBytes : 2 * kTileBytes;
+  static constexpr int kStOffDX = kStOffQX + kAuxBytes;
+  static constexpr int kStageBytes = kStOffDX + kAuxBytes;
   static constexpr int kKvOffK = 0;
   static constexpr int kKvOffV = kTileBytes;
   static constexpr int kKvOffOnes = 2 * kTileBytes;
@@ -339,6 +356,13 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
       };
       if (n_it > 0) fetch(0);
       for (int r = lane; r < kTile; r += 32) write_ones_row(smem + Cfg::kKvOffOnes, r);
+      if (Cfg::kBlockDiag) {
+        // the zero tile of every stage (never written by TMA)
+        for (int st = 0; st < NST; ++st) {
+          uint4* z = reinterpret_cast<uint4*>(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes + Cfg::kStOffZ);
+          for (int i = lane; i < Cfg::kTileBytes / 16; i += 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.fixed);
@@ -353,15 +377,16 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars.full[st], 2 * Cfg::kTileBytes);
           for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-            tma_load_4d(stage + hf * kHalfTileBytes, &p.tmap_q, &bars.full[st], hf * 64, hq, qt * kTile, t.b);
-            tma_load_4d(stage + Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_do, &bars.full[st], hf * 64, hq,
+            tma_load_4d(stage + Cfg::kStOffQ + hf * kHalfTileBytes, &p.tmap_q, &bars.full[st], hf * 64, hq,
+                        qt * kTile, t.b);
+            tma_load_4d(stage + Cfg::kStOffDO + hf * kHalfTileBytes, &p.tmap_do, &bars.full[st], hf * 64, hq,
                         qt * kTile, t.b);
           }
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          write_aux_row(stage + 2 * Cfg::kTileBytes, lane + 32 * k, vnl[k] * inv_sl2);
-          write_aux_row(stage + 2 * Cfg::kTileBytes + Cfg::kAuxBytes, lane + 32 * k, -vd[k]);
+          write_aux_row(stage + Cfg::kStOffQX, lane + 32 * k, vnl[k] * inv_sl2);
+          write_aux_row(stage + Cfg::kStOffDX, lane + 32 * k, -vd[k]);
         }
         if (it + 1 < n_it) fetch(it + 1);
         fence_proxy_async_smem();
@@ -438,14 +463,19 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
       const uint64_t ones = sdesc_noswz(smem_u32(smem + Cfg::kKvOffOnes), 128, 256);
       dA_S = sdesc_sw128(smem_u32(smem + Cfg::kKvOffK), 16, 1024);             // K
       dA_P = sdesc_sw128(smem_u32(smem + Cfg::kKvOffV), 16, 1024);             // V
-      dB_S = sdesc_sw128(st0, 16, 1024);                                       // Q   (K-major)
-      dB_P = sdesc_sw128(st0 + Cfg::kTileBytes, 16, 1024);                     // dO  (K-major)
-      dG1 = sdesc_sw128(st0 + Cfg::kTileBytes, kHalfTileBytes, 1024);          // dO  (MN-major) for dV
-      dG2 = sdesc_sw128(st0, kHalfTileBytes, 1024);                            // Q   (MN-major) for dK
+      dB_S = sdesc_sw128(st0 + Cfg::kStOffQ, 16, 1024);                        // Q   (K-major)
+      dB_P = sdesc_sw128(st0 + Cfg::kStOffDO, 16, 1024);                       // dO  (K-major)
+      if (Cfg::kBlockDiag) {
+        dG1 = sdesc_sw128(st0 + Cfg::kStOffDO, Cfg::kTileBytes, 1024);         // [dO | 0] (MN-major, N = 128)
+        dG2 = sdesc_sw128(st0 + Cfg::kStOffZ, Cfg::kTileBytes, 1024);          // [0 | Q]
+      } else {
+        dG1 = sdesc_sw128(st0 + Cfg::kStOffDO, kHalfTileBytes, 1024);          // dO  (MN-major) for dV
+        dG2 = sdesc_sw128(st0 + Cfg::kStOffQ, kHalfTileBytes, 1024);           // Q   (MN-major) for dK
+      }
       dXA_S = ones;                                                            // ONES x QX^T  -> -LSE2/c
       dXA_P = ones;                                                            // ONES x DX^T  -> -D
-      dXB_S = sdesc_noswz(st0 + 2 * Cfg::kTileBytes, 128, 256);
-      dXB_P = sdesc_noswz(st0 + 2 * Cfg::kTileBytes + Cfg::kAuxBytes, 128, 256);
+      dXB_S = sdesc_noswz(st0 + Cfg::kStOffQX, 128, 256);
+      dXB_P = sdesc_noswz(st0 + Cfg::kStOffDX, 128, 256);
       strideB_S = kStageD;
       strideB_P = kStageD;
       strideX = kStageD;
@@ -503,7 +533,17 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
     auto issue_grad = [&](int i) {
       const int st = i % NST;
       const uint32_t sbuf = tmem + (i % NS) * 128;
-      if (DKV) {
+      if (DKV && Cfg::kBlockDiag) {
+        // [dV | dK] (128 columns) += [P^T | dS^T] x blockdiag(dO, Q): 16 N = 128 steps
+        constexpr uint32_t idesc_bd = idesc_bf16_f32(128, 128, 0, 1);
+        const uint64_t g1 = dG1 + st * kStageD, g2 = dG2 + st * kStageD;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + Cfg::kKvColDV, sbuf + kk * 16, g1 + kk * 128, idesc_bd, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + Cfg::kKvColDV, sbuf + kk * 16 + 8, g2 + kk * 128, idesc_bd, 1u);
+      } else if (DKV) {
         const uint64_t g1 = dG1 + st * kStageD, g2 = dG2 + st * kStageD;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -643,6 +683,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
   const int n_dkv = p.n_dkv_tasks;
   const bool is_dkv = static_cast<int>(blockIdx.x) < n_dkv;
 
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_init(&bars.fixed, 2);  // TMA bytes + the producer warp's aux operands
     for (int s = 0; s < 3; ++s) {
@@ -671,6 +712,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const WaitCtx ctx{&abort_sh, p.status, p.budget_ns, kKidBwdMain};
+  pdl_wait_previous();  // the workspace is written by the preprocess kernel
 
   TaskInfo t;
   t.h = 0;
@@ -731,10 +773,9 @@ cudaError_t launch_bwd_pre(const BwdPreParams& p, int d, cudaStream_t stream) {
   const int tpr = d / 8;
   const long long threads = nrows * tpr;
   const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
-  if (d == 64)
-    bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(p);
-  else
-    bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(p);
+  cudaError_t e = d == 64 ? launch_pdl(bwd_pre_kernel<64>, grid, 256, 0, stream, p)
+                          : launch_pdl(bwd_pre_kernel<128>, grid, 256, 0, stream, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -744,10 +785,12 @@ cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream) {
   cudaError_t e;
   if (d == 64) {
     if ((e = ensure_smem_attr(bwd_main_kernel<64>, MainCfg<64>::kSmemBytes, 0)) != cudaSuccess) return e;
-    bwd_main_kernel<64><<<grid, kMainThreads, MainCfg<64>::kSmemBytes, stream>>>(p);
+    e = launch_pdl(bwd_main_kernel<64>, grid, kMainThreads, MainCfg<64>::kSmemBytes, stream, p);
+    if (e != cudaSuccess) return e;
   } else {
     if ((e = ensure_smem_attr(bwd_main_kernel<128>, MainCfg<128>::kSmemBytes, 1)) != cudaSuccess) return e;
-    bwd_main_kernel<128><<<grid, kMainThreads, MainCfg<128>::kSmemBytes, stream>>>(p);
+    e = launch_pdl(bwd_main_kernel<128>, grid, kMainThreads, MainCfg<128>::kSmemBytes, stream, p);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
   const int kvh = h / p.G;
   const int n_kv = p.causal ? qt + 1 : p.nT;
 
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
     for (int s = 0; s < KS; ++s) { mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1); }
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const WaitCtx ctx{&abort_sh, p.status, p.budget_ns, kKidFwd};
+  pdl_wait_previous();  // inputs may be written by the previous kernel; outputs may still be read by it
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -210,14 +212,13 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
       tc_fence_after();
       float s[kTile];
       {
-        uint32_t r[32];
+        // one batched load of the whole row, one wait
+        uint32_t r[kTile];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tS + c * 32, r);
-          tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+        tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
-        }
+        for (int i = 0; i < kTile; ++i) s[i] = __uint_as_float(r[i]);
       }
       if (p.causal && j == qt) {
 #pragma unroll
@@ -229,9 +230,18 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
         for (int c = 0; c < kTile; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // row max: a tree of 3-input maxima (independent chains, half the instructions)
+      float m8[8];
 #pragma unroll
-      for (int c = 1; c < kTile; ++c) mx = fmaxf(mx, s[c]);
+      for (int g = 0; g < 8; ++g) {
+        float a = max3(s[g * 16 + 0], s[g * 16 + 1], s[g * 16 + 2]);
+        float b = max3(s[g * 16 + 3], s[g * 16 + 4], s[g * 16 + 5]);
+        float c = max3(s[g * 16 + 6], s[g * 16 + 7], s[g * 16 + 8]);
+        float d = max3(s[g * 16 + 9], s[g * 16 + 10], s[g * 16 + 11]);
+        float e = max3(s[g * 16 + 12], s[g * 16 + 13], s[g * 16 + 14]);
+        m8[g] = max3(max3(a, b, c), max3(d, e, s[g * 16 + 15]), a);
+      }
+      const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       const float m_tile = mx * sl2;
       const bool need = m_tile > m_used + kRescaleThreshold;
       float alpha = 1.f;
@@ -241,6 +251,7 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
         l *= alpha;
       }
       const float neg_m = -m_used;
+      float lsum[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -248,11 +259,12 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
         for (int i = 0; i < 16; ++i) {
           const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, neg_m));
           const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, neg_m));
-          l += p0 + p1;
+          lsum[i & 3] += p0 + p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + c * 16, pk);
       }
+      l += (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
       // Rescale O (already complete: S_j's commit follows PV_{j-1}) when any row of this warp needs it.
       if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -319,7 +331,8 @@ cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
     attr_set[dev] = true;
   }
   const unsigned grid = static_cast<unsigned>(p.B) * p.Hq * p.nT;
-  attn_fwd_kernel<D><<<grid, kFwdThreads, smem, stream>>>(p);
+  e = launch_pdl(attn_fwd_kernel<D>, grid, kFwdThreads, smem, stream, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

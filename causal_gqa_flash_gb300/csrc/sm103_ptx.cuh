@@ -126,6 +126,17 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 }
 
 // ----------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel lets the next kernel of the stream be
+// scheduled as soon as all of its CTAs have started, and waits for the previous
+// kernel's completion (and memory) before its first global-memory access, so
+// launch latency and prologues overlap the previous kernel's tail.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_previous() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ----------------------------------------------------------------------------
 // Named barriers (sub-CTA groups of warps)
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
