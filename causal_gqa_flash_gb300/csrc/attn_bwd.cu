@@ -38,14 +38,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
@@ -108,11 +100,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
 // ============================================================================
 // dQ and dK/dV: one launch, two kinds of task.
 //
-// CTA = 10 warps: warp 0 issues TMA, warp 1 issues tcgen05 MMAs and owns TMEM,
-// warps 2-9 are two compute warpgroups. Each compute thread owns one TMEM lane
-// (one row) and its warpgroup owns half of the 128 score columns, processed in
-// four rounds of 16 columns whose TMEM loads are software-pipelined (the next
-// round is in flight while this one is computed).
+// CTA = 19 warps: warp 0 issues TMA, warp 1 issues the S and dP MMAs and owns
+// TMEM, warps 2-17 are four compute warpgroups, warp 18 issues the gradient MMAs. Each compute thread owns one TMEM lane
+// (one row) and its warpgroup owns 32 of the 128 score columns.
 //
 // Blocks [0, n_dkv) are dK/dV tasks (one per key tile, kv head, batch; key tile
 // ascending = causal cost descending); the following n_dq blocks are dQ tasks
@@ -120,24 +110,28 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
 // runs per SM and the heaviest tasks start first.
 //
 // Pipeline per iteration `it` (one 128x128 score tile):
-//   MMA:     S(it+1) into the other S buffer | dP(it+1) once compute(it) has
-//            read dP(it) | gradient MMAs of `it` once compute(it) is done.
-//   compute: read S(it), dP(it) -> P = 2^(S*scale*log2e - LSE2), dS = P(dP - D)
-//            -> bf16 P and dS written back over the 16 S columns of each round.
-// so the tensor core works on iteration it+1 while iteration it is computed.
-// With one S buffer (dK/dV at d = 128, where dV and dK take 256 columns) only
-// dP(it+1) overlaps compute(it).
+//   compute: load its 32 columns of S(it) and dP(it) into registers and release
+//            both accumulators at once (sdp_free); P = 2^(S*scale*log2e - LSE2),
+//            dS = P (dP - D) in registers; bf16 P and dS into their own TMEM
+//            region once the gradient MMAs of it-1 have read it (pds_free), then
+//            pds_full.
+//   MMA:     S(it+1), dP(it+1) as soon as sdp_free(it) | gradient MMAs of it on
+//            pds_full(it).
+// so the tensor core computes the scores of it+1 while the compute warps work on
+// it, and the compute warps never wait for a half-read accumulator.
 //
-// TMEM columns (S buffers are 128 fp32 columns each):
-//   dQ:        S0 [0,128) S1 [128,256) dP [256,384) dQ [384,384+D)
-//   dK/dV 64:  S0 [0,128) S1 [128,256) dP [256,384) dV [384,448) dK [448,512)
-//   dK/dV 128: S  [0,128)              dP [128,256) dV [256,384) dK [384,512)
-// Round r of warpgroup g covers score columns c0 = 64g + 16r .. c0+15; its bf16
-// P goes to S columns [c0, c0+8) and dS to [c0+8, c0+16) (dQ writes only dS at
-// [c0, c0+8)), so the A operand of K-step kk (16 score columns) is at 16*kk.
+// TMEM columns (S and dP are 128 fp32 columns; P and dS 64 columns of bf16 pairs):
+//   dQ:        S [0,128) dP [128,256) dS [256,320) dQ [320,320+D)
+//   dK/dV 64:  S [0,128) dP [128,256) P [256,320) dS [320,384) dV [384,448) dK [448,512)
+//   dK/dV 128: S [0,128) dP [128,256) dV [256,384) dK [384,512); no room for a separate
+//              P/dS region, so P goes to S columns [0,64) and dS to [64,128) once every
+//              warpgroup has read S (sdp_free), and S(it+1) follows the gradient MMAs.
+// Warpgroup g writes the bf16 pairs of its score columns [32g, 32g+32) to columns
+// [16g, 16g+16) of the P (dS) region, so the A operand of K-step kk is at 8*kk.
 // ============================================================================
-constexpr int kMainThreads = 320;
-constexpr int kComputeThreads = 256;
+constexpr int kMainThreads = 608;
+constexpr int kComputeThreads = 512;
+constexpr int kGradWarp = 18;  // second MMA issuer (gradient MMAs)
 
 template <int D>
 struct MainCfg {
@@ -162,7 +156,6 @@ struct MainCfg {
   // N = 64 MMAs run well below the tensor peak when the compute warps stream
   // TMEM at the same time; N = 128 ones do not.
   static constexpr bool kBlockDiag = (D == 64);
-  static constexpr int kKvNS = (D == 64) ? 2 : 1;       // S buffers
   static constexpr int kKvStages = (D == 64) ? 3 : 2;   // Q/dO stages
   static constexpr int kStOffDO = kBlockDiag ? 0 : kTileBytes;
   static constexpr int kStOffZ = kTileBytes;             // d = 64 only
@@ -178,11 +171,16 @@ struct MainCfg {
   static constexpr int kUsed = (kDqBytes > kKvBytes ? kDqBytes : kKvBytes) + 1024;
   static constexpr int kSmemBytes = kUsed > kOneCtaPerSmSmem ? kUsed : kOneCtaPerSmSmem;
   // TMEM columns
-  static constexpr uint32_t kDqColDP = 256;
-  static constexpr uint32_t kDqColAcc = 384;
-  static constexpr uint32_t kKvColDP = kKvNS * 128;
-  static constexpr uint32_t kKvColDV = kKvColDP + 128;
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColDP = 128;
+  static constexpr uint32_t kDqColDS = 256;
+  static constexpr uint32_t kDqColAcc = 320;
+  static constexpr bool kKvSepPdS = (D == 64);  // dK/dV: P/dS region of its own
+  static constexpr uint32_t kKvColP = kKvSepPdS ? 256 : 0;
+  static constexpr uint32_t kKvColDS = kKvSepPdS ? 320 : 64;
+  static constexpr uint32_t kKvColDV = kKvSepPdS ? 384 : 256;
   static constexpr uint32_t kKvColDK = kKvColDV + D;
+  static_assert(kDqColAcc + D <= 512 && kKvColDK + D <= 512, "TMEM columns");
 };
 
 // Unswizzled K-major layout of a 128 x 16 bf16 operand: byte offset of (row, 8-column half).
@@ -208,87 +206,74 @@ __device__ __forceinline__ void write_ones_row(uint8_t* tile, int row) {
   *reinterpret_cast<uint4*>(tile + aux_off(row, 1)) = make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Store `ncols` (multiple of 32) fp32 columns of this thread's row as bf16 to dst.
+// Store NCOLS (16 or a multiple of 32) fp32 columns of this thread's row as bf16 to dst.
 template <int NCOLS>
 __device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* dst, float scale, bool valid) {
-#pragma unroll
-  for (int c = 0; c < NCOLS / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld32(taddr + c * 32, r);
+  if constexpr (NCOLS == 16) {
+    uint32_t r[16];
+    tmem_ld16(taddr, r);
     tmem_wait_ld();
-    uint32_t pk[16];
+    uint32_t pk[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < 8; ++i)
       pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
     if (valid) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    }
+  } else {
+    static_assert(NCOLS % 32 == 0, "NCOLS");
 #pragma unroll
-      for (int v4 = 0; v4 < 4; ++v4) d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+    for (int c = 0; c < NCOLS / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c * 32, r);
+      tmem_wait_ld();
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
+      if (valid) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+      }
     }
   }
 }
 
-// One 16-column round. The accumulators already hold S - LSE2/c and dP - D, so
-// P = 2^(c * s') and dS = P * dp'. Columns outside [lo, hi) are masked (MASKED only).
-// dK/dV rounds write bf16 P to columns [0, 8) and dS to [8, 16) of the round;
-// dQ rounds write dS to [0, 8).
+// This thread's 32 score columns of one tile. The accumulators already hold
+// S - LSE2/c and dP - D, so P = 2^(c * s') and dS = P * dp'. Columns outside
+// [lo, hi) of the warpgroup's frame are masked (MASKED only). Writes the bf16
+// pairs of P (dK/dV only) and dS.
 template <bool DKV, bool MASKED>
-__device__ __forceinline__ void tile_round(const uint32_t (&s)[16], const uint32_t (&dp)[16], float sl2, int col0,
-                                           int lo, int hi, uint32_t tS_round) {
-  uint32_t pk[8], dk[8];
+__device__ __forceinline__ void score_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32], float sl2, int lo,
+                                            int hi, uint32_t (&pk)[16], uint32_t (&dk)[16]) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 16; ++i) {
     float p0 = ex2_approx(__uint_as_float(s[2 * i]) * sl2);
     float p1 = ex2_approx(__uint_as_float(s[2 * i + 1]) * sl2);
     if (MASKED) {
-      const int c = col0 + 2 * i;
-      p0 = (c >= lo && c < hi) ? p0 : 0.f;
-      p1 = (c + 1 >= lo && c + 1 < hi) ? p1 : 0.f;
+      p0 = (2 * i >= lo && 2 * i < hi) ? p0 : 0.f;
+      p1 = (2 * i + 1 >= lo && 2 * i + 1 < hi) ? p1 : 0.f;
     }
     if (DKV) pk[i] = pack_bf16x2(p0, p1);
     dk[i] = pack_bf16x2(p0 * __uint_as_float(dp[2 * i]), p1 * __uint_as_float(dp[2 * i + 1]));
   }
-  if (DKV) {
-    tmem_st8(tS_round, pk);
-    tmem_st8(tS_round + 8, dk);
-  } else {
-    tmem_st8(tS_round, dk);
-  }
 }
 
-// The compute part of one tile for one warpgroup: four rounds of 16 columns with
-// the TMEM load of round r+2 in flight while round r+1 is computed. Signals
-// dp_free as soon as every dP column of this warpgroup is in registers.
-template <bool DKV, bool MASKED>
-__device__ __forceinline__ void compute_tile(uint32_t tS, uint32_t tDP, float sl2, int lo, int hi,
-                                             uint64_t* bar_dpfree) {
-  uint32_t sa[16], da[16], sb[16], db[16];
-  tmem_ld16(tS, sa);
-  tmem_ld16(tDP, da);
-  tmem_ld16(tS + 16, sb);
-  tmem_ld16(tDP + 16, db);
-  tmem_wait_ld();
-  tile_round<DKV, MASKED>(sa, da, sl2, 0, lo, hi, tS);
-  tmem_ld16(tS + 32, sa);
-  tmem_ld16(tDP + 32, da);
-  tile_round<DKV, MASKED>(sb, db, sl2, 16, lo, hi, tS + 16);
-  tmem_wait_ld();
-  tmem_ld16(tS + 48, sb);
-  tmem_ld16(tDP + 48, db);
-  tile_round<DKV, MASKED>(sa, da, sl2, 32, lo, hi, tS + 32);
-  tmem_wait_ld();
-  // every dP column of this warpgroup is in registers: the MMA may overwrite dP
-  tc_fence_before();
-  mbar_arrive(bar_dpfree);
-  tile_round<DKV, MASKED>(sb, db, sl2, 48, lo, hi, tS + 48);
-}
-
-// `p[it & 1]` ("bf16 P/dS of iteration it are in TMEM") alternates between two
-// barriers: S(it+1) is committed before the MMA thread waits for P(it), so the
-// compute warps may finish iteration it+1 before that wait is observed, and a
-// single barrier could then have moved two phases on.
+// Barriers of one task. Every one of them is at most one phase ahead of any
+// waiter: sdp_full(it+1) is committed only after sdp_free(it) completed, which
+// needs every compute thread to have passed sdp_full(it); pds_full(it+1) needs
+// pds_free(it), which the MMA thread commits only after it saw pds_full(it);
+// and the reverse pairs likewise.
 struct MainBars {
-  uint64_t fixed, full[3], empty[3], vfull[2], vempty[2], s, dpfree, p[2], fin, drain;
+  uint64_t fixed, full[3], empty[3], vfull[2], vempty[2];
+  uint64_t sdp_full;  // MMA -> compute: S(it) and dP(it) are in TMEM
+  uint64_t sdp_free;  // compute -> MMA: every thread has S(it), dP(it) in registers
+  uint64_t pds_full;  // compute -> MMA: bf16 P/dS of it are in TMEM
+  uint64_t pds_free;  // MMA -> compute: the gradient MMAs of it have completed
+  uint64_t fin, drain, drain2;
 };
 
 struct TaskInfo {
@@ -308,10 +293,11 @@ template <int D, bool DKV>
 __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, MainBars& bars, uint32_t tmem,
                                          const WaitCtx& ctx, const TaskInfo& t, int warp, int lane) {
   using Cfg = MainCfg<D>;
-  constexpr int NS = DKV ? Cfg::kKvNS : 2;                    // S buffers in TMEM
+  constexpr bool kSep = DKV ? Cfg::kKvSepPdS : true;           // P/dS region separate from S
+  constexpr uint32_t colP = DKV ? Cfg::kKvColP : 0;
+  constexpr uint32_t colDS = DKV ? Cfg::kKvColDS : Cfg::kDqColDS;
   constexpr int NST = DKV ? Cfg::kKvStages : Cfg::kDqKStages;  // main ring depth
   constexpr int NV = Cfg::kDqVStages;                         // dQ V ring depth
-  constexpr uint32_t colDP = DKV ? Cfg::kKvColDP : Cfg::kDqColDP;
   constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: N = 128
   constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);    // gradients: N = D, B MN-major
   constexpr uint32_t kTileD = Cfg::kTileBytes >> 4;             // tile stride, descriptor units
@@ -452,9 +438,16 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
       for (int s2 = 0; s2 < 2; ++s2)
         if (vissued[s2] > 0) mbar_wait_drain(&bars.vfull[s2], (vissued[s2] - 1) & 1, p.budget_ns);
     }
-  } else if (warp == 1) {
-    // ============================================================ MMA issuer
-    if (lane != 0) return;
+  } else if (warp == 1 || warp == kGradWarp) {
+    // ============================================================ MMA issuers
+    // All 32 lanes of an issuing warp run its loop; the elected lane (always lane
+    // 0 of the converged warp) issues every MMA and commit, so commits track its
+    // MMAs. With a separate P/dS region, warp 1 issues S and dP and warp kGradWarp
+    // the gradient MMAs, so neither chain of barrier checks and issues holds up the
+    // other; otherwise (dK/dV at d = 128) S(it+1) must follow the gradient MMAs of
+    // it and warp 1 issues everything.
+    constexpr bool kTwoIssuers = kSep;
+    if (!kTwoIssuers && warp == kGradWarp) return;
     // Base descriptors (stage / slot 0); a stage or K-step moves the start address only.
     uint64_t dA_S, dA_P, dB_S, dB_P, dG1, dG2, dXA_S, dXA_P, dXB_S, dXB_P;
     uint32_t strideB_S, strideB_P, strideX;
@@ -496,175 +489,235 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
       strideX = 0;
     }
     bool issued_any = false;
-    auto issue_S = [&](int i) -> bool {
+    // S(i); waits for its stage unless the caller already did (dK/dV: one stage carries Q and dO).
+    auto issue_S = [&](int i, bool wait_stage) -> bool {
       const int st = i % NST;
-      if (!mbar_wait(&bars.full[st], (i / NST) & 1, ctx, 11)) return false;
-      tc_fence_after();
-      const uint32_t dst = tmem + (i % NS) * 128;
+      if (wait_stage) {
+        if (!warp_wait(&bars.full[st], (i / NST) & 1, ctx, 11)) return false;
+        tc_fence_after();
+      }
+      const uint32_t dst = tmem + Cfg::kColS;
       const uint64_t b0 = dB_S + st * strideB_S;
+      if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss(dst, dA_S + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
-      mma_ss(dst, dXA_S, dXB_S + st * strideX, idesc_s, 1u);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(dst, dA_S + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+        mma_ss(dst, dXA_S, dXB_S + st * strideX, idesc_s, 1u);
+      }
+      __syncwarp();
       issued_any = true;
       return true;
     };
-    auto issue_dP = [&](int i) -> bool {
+    auto issue_dP = [&](int i, bool wait_stage) -> bool {
       int slot, xst;
       if (DKV) {
         slot = i % NST;
         xst = slot;
-        if (!mbar_wait(&bars.full[slot], (i / NST) & 1, ctx, 13)) return false;
+        if (wait_stage) {
+          if (!warp_wait(&bars.full[slot], (i / NST) & 1, ctx, 13)) return false;
+          tc_fence_after();
+        }
       } else {
         slot = i % NV;
         xst = 0;
-        if (!mbar_wait(&bars.vfull[slot], (i / NV) & 1, ctx, 13)) return false;
+        if (!warp_wait(&bars.vfull[slot], (i / NV) & 1, ctx, 13)) return false;
+        tc_fence_after();
       }
-      tc_fence_after();
       const uint64_t b0 = dB_P + slot * strideB_P;
+      if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss(tmem + colDP, dA_P + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
-      mma_ss(tmem + colDP, dXA_P, dXB_P + xst * strideX, idesc_s, 1u);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + Cfg::kColDP, dA_P + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+        mma_ss(tmem + Cfg::kColDP, dXA_P, dXB_P + xst * strideX, idesc_s, 1u);
+        if (!DKV) mma_commit(&bars.vempty[slot]);
+      }
+      __syncwarp();
       issued_any = true;
-      if (!DKV) mma_commit(&bars.vempty[slot]);
       return true;
     };
     auto issue_grad = [&](int i) {
       const int st = i % NST;
-      const uint32_t sbuf = tmem + (i % NS) * 128;
-      if (DKV && Cfg::kBlockDiag) {
-        // [dV | dK] (128 columns) += [P^T | dS^T] x blockdiag(dO, Q): 16 N = 128 steps
-        constexpr uint32_t idesc_bd = idesc_bf16_f32(128, 128, 0, 1);
-        const uint64_t g1 = dG1 + st * kStageD, g2 = dG2 + st * kStageD;
+      const uint32_t tP = tmem + colP, tDS = tmem + colDS;
+      if (elect_one()) {
+        if (DKV && Cfg::kBlockDiag) {
+          // [dV | dK] (128 columns) += [P^T | dS^T] x blockdiag(dO, Q): 16 N = 128 steps
+          constexpr uint32_t idesc_bd = idesc_bf16_f32(128, 128, 0, 1);
+          const uint64_t g1 = dG1 + st * kStageD, g2 = dG2 + st * kStageD;
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + Cfg::kKvColDV, sbuf + kk * 16, g1 + kk * 128, idesc_bd, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tmem + Cfg::kKvColDV, tP + kk * 8, g1 + kk * 128, idesc_bd, (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + Cfg::kKvColDV, sbuf + kk * 16 + 8, g2 + kk * 128, idesc_bd, 1u);
-      } else if (DKV) {
-        const uint64_t g1 = dG1 + st * kStageD, g2 = dG2 + st * kStageD;
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tmem + Cfg::kKvColDV, tDS + kk * 8, g2 + kk * 128, idesc_bd, 1u);
+        } else if (DKV) {
+          const uint64_t g1 = dG1 + st * kStageD, g2 = dG2 + st * kStageD;
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + Cfg::kKvColDV, sbuf + kk * 16, g1 + kk * 128, idesc_g, acc);
-          mma_ts(tmem + Cfg::kKvColDK, sbuf + kk * 16 + 8, g2 + kk * 128, idesc_g, acc);
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+            mma_ts(tmem + Cfg::kKvColDV, tP + kk * 8, g1 + kk * 128, idesc_g, acc);
+            mma_ts(tmem + Cfg::kKvColDK, tDS + kk * 8, g2 + kk * 128, idesc_g, acc);
+          }
+        } else {
+          const uint64_t g1 = dG1 + st * kTileD;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tmem + Cfg::kDqColAcc, tDS + kk * 8, g1 + kk * 128, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
         }
-      } else {
-        const uint64_t g1 = dG1 + st * kTileD;
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + Cfg::kDqColAcc, sbuf + kk * 16, g1 + kk * 128, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.pds_free);
+        mma_commit(&bars.empty[st]);
       }
-      mma_commit(&bars.empty[st]);
+      __syncwarp();
+      issued_any = true;
+    };
+    auto commit = [&](uint64_t* bar) {
+      if (elect_one()) mma_commit(bar);
+      __syncwarp();
     };
 
-    bool ok = mbar_wait(&bars.fixed, 0, ctx, 10);
-    if (ok) ok = issue_S(0);
-    if (ok) ok = issue_dP(0);
-    if (ok) mma_commit(&bars.s);
-    for (int it = 0; it < n_it && ok; ++it) {
-      const bool has_next = it + 1 < n_it;
-      if (NS == 2 && has_next) {
-        ok = issue_S(it + 1);
-        if (!ok) break;
+    bool ok = true;
+    if (warp == 1) {
+      ok = warp_wait(&bars.fixed, 0, ctx, 10);
+      if (ok) {
+        tc_fence_after();
+        ok = issue_S(0, true);
       }
-      ok = mbar_wait(&bars.dpfree, it & 1, ctx, 14);
-      if (!ok) break;
-      if (has_next) {
-        ok = issue_dP(it + 1);
-        if (!ok) break;
-        if (NS == 2) mma_commit(&bars.s);
-      }
-      ok = mbar_wait(&bars.p[it & 1], (it >> 1) & 1, ctx, 12);
-      if (!ok) break;
-      tc_fence_after();
-      issue_grad(it);
-      if (NS == 1 && has_next) {
-        ok = issue_S(it + 1);
-        if (!ok) break;
-        mma_commit(&bars.s);
-      }
+      if (ok) ok = issue_dP(0, !DKV);
+      if (ok) commit(&bars.sdp_full);
     }
-    if (ok) {
-      mma_commit(&bars.fin);
-    } else if (issued_any) {
-      mma_commit(&bars.drain);
-      mbar_wait_drain(&bars.drain, 0, p.budget_ns);
+    if (kTwoIssuers && warp == 1) {
+      // S and dP of it+1 as soon as every compute thread holds S(it), dP(it)
+      for (int it = 0; it + 1 < n_it && ok; ++it) {
+        ok = warp_wait(&bars.sdp_free, it & 1, ctx, 14);
+        if (!ok) break;
+        ok = issue_S(it + 1, true);
+        if (ok) ok = issue_dP(it + 1, !DKV);
+        if (!ok) break;
+        commit(&bars.sdp_full);
+      }
+    } else if (kTwoIssuers) {
+      // gradient MMAs of it once its bf16 P/dS are in TMEM
+      for (int it = 0; it < n_it && ok; ++it) {
+        ok = warp_wait(&bars.pds_full, it & 1, ctx, 12);
+        if (!ok) break;
+        tc_fence_after();
+        issue_grad(it);
+      }
+      // every S/dP MMA completed before the last P/dS was written
+      if (ok) commit(&bars.fin);
+    } else {
+      for (int it = 0; it < n_it && ok; ++it) {
+        const bool has_next = it + 1 < n_it;
+        ok = warp_wait(&bars.sdp_free, it & 1, ctx, 14);
+        if (!ok) break;
+        if (has_next) {
+          ok = issue_dP(it + 1, true);
+          if (!ok) break;
+        }
+        ok = warp_wait(&bars.pds_full, it & 1, ctx, 12);
+        if (!ok) break;
+        tc_fence_after();
+        issue_grad(it);
+        if (has_next) {
+          // P/dS of it live in the S columns: S(it+1) after the gradient MMAs
+          ok = issue_S(it + 1, false);
+          if (!ok) break;
+          commit(&bars.sdp_full);
+        }
+      }
+      if (ok) commit(&bars.fin);
+    }
+    if (!ok && issued_any) {
+      uint64_t* dr = warp == 1 ? &bars.drain : &bars.drain2;
+      commit(dr);
+      mbar_wait_drain(dr, 0, p.budget_ns);
     }
   } else {
     // ============================================================ compute warpgroups
-    const int wg = (warp - 2) >> 2;  // 0 or 1: score columns [wg*64, wg*64+64)
+    const int wg = (warp - 2) >> 2;  // 0..3: score columns [wg*32, wg*32+32)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tDP = tmem + lane_base + colDP + wg * 64;
+    const uint32_t tS = tmem + lane_base + Cfg::kColS + wg * 32;
+    const uint32_t tDP = tmem + lane_base + Cfg::kColDP + wg * 32;
+    const uint32_t tP = tmem + lane_base + colP + wg * 16;
+    const uint32_t tDS = tmem + lane_base + colDS + wg * 16;
     const float sl2 = p.scale_log2;
     bool ok = true;
+    // One tile: S, dP -> registers -> sdp_free; P, dS -> TMEM -> pds_full.
+    auto tile = [&](int it, bool masked, int lo, int hi) -> bool {
+      if (!warp_wait(&bars.sdp_full, it & 1, ctx, 20)) return false;
+      tc_fence_after();
+      uint32_t s[32], dp[32];
+      tmem_ld32(tS, s);
+      tmem_ld32(tDP, dp);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars.sdp_free);
+      uint32_t pk[16], dk[16];
+      if (masked)
+        score_chunk<DKV, true>(s, dp, sl2, lo, hi, pk, dk);
+      else
+        score_chunk<DKV, false>(s, dp, sl2, lo, hi, pk, dk);
+      // The P/dS region must be free: read by the gradient MMAs of it-1 (separate
+      // region), or S(it) read by every warpgroup (region inside S).
+      if (kSep) {
+        if (it > 0 && !warp_wait(&bars.pds_free, (it - 1) & 1, ctx, 22)) return false;
+      } else {
+        if (!warp_wait(&bars.sdp_free, it & 1, ctx, 23)) return false;
+      }
+      tc_fence_after();
+      if (DKV) tmem_st16(tP, pk);
+      tmem_st16(tDS, dk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars.pds_full);
+      return true;
+    };
     if (DKV) {
       const int k_idx = t.tile * kTile + row;
-      for (int it = 0; it < n_it; ++it) {
+      for (int it = 0; it < n_it && ok; ++it) {
         const int qt = t.i0 + it % t.ni;
-        ok = warp_wait(&bars.s, it & 1, ctx, 20);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t tS = tmem + lane_base + (it % NS) * 128 + wg * 64;
-        // Query columns visible to this key row: [lo, hi) in this warpgroup's 64-column frame.
+        // Query columns visible to this key row: [lo, hi) in this warpgroup's 32-column frame.
         const int hi_tile = min(kTile, p.T - qt * kTile);
         const bool diag = p.causal && qt == t.tile;
-        const int lo = (diag ? row : 0) - wg * 64;
-        const int hi = hi_tile - wg * 64;
-        if (diag || hi_tile < kTile)
-          compute_tile<true, true>(tS, tDP, sl2, lo, hi, &bars.dpfree);
-        else
-          compute_tile<true, false>(tS, tDP, sl2, lo, hi, &bars.dpfree);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars.p[it & 1]);
+        const int lo = (diag ? row : 0) - wg * 32;
+        const int hi = hi_tile - wg * 32;
+        ok = tile(it, diag || hi_tile < kTile, lo, hi);
       }
       if (ok) ok = warp_wait(&bars.fin, 0, ctx, 21);
       if (ok) {
         tc_fence_after();
         const bool valid = k_idx < p.T;
         const size_t off = ((static_cast<size_t>(t.b) * p.T + (valid ? k_idx : 0)) * p.Hkv + t.kvh) * D;
-        if (wg == 0)
-          store_row_bf16<D>(tmem + lane_base + Cfg::kKvColDV, reinterpret_cast<__nv_bfloat16*>(p.dv) + off, 1.f,
-                            valid);
+        // warpgroups 0, 1: dV halves; 2, 3: dK halves
+        const int part = wg & 1;
+        if (wg < 2)
+          store_row_bf16<D / 2>(tmem + lane_base + Cfg::kKvColDV + part * (D / 2),
+                                reinterpret_cast<__nv_bfloat16*>(p.dv) + off + part * (D / 2), 1.f, valid);
         else
-          store_row_bf16<D>(tmem + lane_base + Cfg::kKvColDK, reinterpret_cast<__nv_bfloat16*>(p.dk) + off, p.scale,
-                            valid);
+          store_row_bf16<D / 2>(tmem + lane_base + Cfg::kKvColDK + part * (D / 2),
+                                reinterpret_cast<__nv_bfloat16*>(p.dk) + off + part * (D / 2), p.scale, valid);
       }
     } else {
       const int q_idx = t.tile * kTile + row;
       const bool valid = q_idx < p.T;
       const bool tile_ragged = (t.tile + 1) * kTile > p.T;
-      for (int j = 0; j < n_it; ++j) {
-        ok = warp_wait(&bars.s, j & 1, ctx, 20);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t tS = tmem + lane_base + (j & 1) * 128 + wg * 64;
-        // Key columns visible to this query row: [0, lim) in this warpgroup's 64-column frame.
+      for (int j = 0; j < n_it && ok; ++j) {
+        // Key columns visible to this query row: [0, lim) in this warpgroup's 32-column frame.
         const bool diag = p.causal && j == t.tile;
         const bool kv_ragged = !p.causal && (j + 1) * kTile > p.T;
         int lim_tile = kTile;
         if (diag) lim_tile = row + 1;
         if (kv_ragged) lim_tile = p.T - j * kTile;
-        const int lim = (valid ? lim_tile : 0) - wg * 64;
-        if (diag || kv_ragged || tile_ragged)
-          compute_tile<false, true>(tS, tDP, sl2, 0, lim, &bars.dpfree);
-        else
-          compute_tile<false, false>(tS, tDP, sl2, 0, lim, &bars.dpfree);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars.p[j & 1]);
+        const int lim = (valid ? lim_tile : 0) - wg * 32;
+        ok = tile(j, diag || kv_ragged || tile_ragged, 0, lim);
       }
       if (ok) ok = warp_wait(&bars.fin, 0, ctx, 21);
       if (ok) {
         tc_fence_after();
         const size_t off = ((static_cast<size_t>(t.b) * p.T + (valid ? q_idx : 0)) * p.Hq + t.h) * D;
-        store_row_bf16<D / 2>(tmem + lane_base + Cfg::kDqColAcc + wg * (D / 2),
-                              reinterpret_cast<__nv_bfloat16*>(p.dq) + off + wg * (D / 2), p.scale, valid);
+        store_row_bf16<D / 4>(tmem + lane_base + Cfg::kDqColAcc + wg * (D / 4),
+                              reinterpret_cast<__nv_bfloat16*>(p.dq) + off + wg * (D / 4), p.scale, valid);
       }
     }
   }
@@ -694,12 +747,13 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
       mbar_init(&bars.vfull[s], 1);
       mbar_init(&bars.vempty[s], 1);
     }
-    mbar_init(&bars.s, 1);
-    mbar_init(&bars.dpfree, kComputeThreads);
-    mbar_init(&bars.p[0], kComputeThreads);
-    mbar_init(&bars.p[1], kComputeThreads);
+    mbar_init(&bars.sdp_full, 1);
+    mbar_init(&bars.sdp_free, kComputeThreads);
+    mbar_init(&bars.pds_full, kComputeThreads);
+    mbar_init(&bars.pds_free, 1);
     mbar_init(&bars.fin, 1);
     mbar_init(&bars.drain, 1);
+    mbar_init(&bars.drain2, 1);
     abort_sh = 0;
     fence_mbar_init();
   }

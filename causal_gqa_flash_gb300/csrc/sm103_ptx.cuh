@@ -136,6 +136,21 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait_previous() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// One lane of a converged warp (the lowest active one) gets true. A warp that
+// issues tcgen05 MMAs runs its loop with all 32 lanes and lets the elected lane
+// issue: the descriptors then live in uniform registers and each MMA costs a few
+// instructions, where a lone lane needs many more and loses issue slots to the
+// compute warps of its sub-partition.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t is_leader;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(is_leader));
+  return is_leader != 0;
+}
+
 // ----------------------------------------------------------------------------
 // Named barriers (sub-CTA groups of warps)
 // ----------------------------------------------------------------------------
