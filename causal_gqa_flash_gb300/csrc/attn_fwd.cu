@@ -10,12 +10,16 @@
 //  * one CTA = one 128-query tile of one (batch, query head); two CTAs share
 //    an SM so one's softmax overlaps the other's tensor-core work;
 //  * warp 0 issues TMA loads (Q once, a K ring and a V ring, 128B swizzle),
-//    warp 1 issues tcgen05 MMAs from one thread and owns the TMEM allocation,
-//    warps 2-5 are the softmax warpgroup: one thread per query row, which is
-//    one TMEM lane, so row max and row sum need no shuffles;
-//  * S = Q K^T (SS MMA, fp32 in TMEM columns [0,128)), P is written back as
-//    bf16 over S's first 64 columns and O += P V is a TS MMA (A from TMEM,
-//    V as an MN-major smem operand) into TMEM columns [128, 128+d);
+//    warp 1 issues tcgen05 MMAs (all lanes run the loop, one elected lane
+//    issues) and owns the TMEM allocation, warps 2-5 are the softmax
+//    warpgroup: one thread per query row, which is one TMEM lane, so row max
+//    and row sum need no shuffles;
+//  * S = Q K^T (SS MMA, fp32 in TMEM columns [0,128)) and O += P V (TS MMA, P
+//    as bf16 pairs from TMEM, V as an MN-major smem operand). At d = 64, P has
+//    columns of its own: the softmax loads the whole S row into registers and
+//    releases S at once, so S(j+1) is computed while P(j) is; at d = 128 (no
+//    TMEM room for two CTAs otherwise) P is written over S's first 64 columns
+//    and S(j+1) follows PV(j);
 //  * the running max is rescaled lazily: O and l are only rescaled when a
 //    row's max grows by more than 2^8, otherwise p = 2^(s - m_stale) <= 256;
 //  * causal tiles past the diagonal are never visited; only the diagonal tile
@@ -27,12 +31,17 @@ namespace {
 
 constexpr int kFwdThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0;     // S fp32 [128 x 128]; P bf16 aliases [0, 64)
-constexpr uint32_t kColO = 128;   // O fp32 [128 x d]
+constexpr uint32_t kColS = 0;     // S fp32 [128 x 128]
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct FwdCfg {
+  // TMEM: d = 64: S [0,128) P [128,192) O [192,256); d = 128: S [0,128) with P
+  // over [0,64), O [128,256).
+  static constexpr bool kSepP = (D == 64);
+  static constexpr uint32_t kColP = kSepP ? 128 : 0;
+  static constexpr uint32_t kColO = kSepP ? 192 : 128;
+  static_assert(kColO + D <= kTmemCols, "TMEM columns");
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = kHalves * kHalfTileBytes;  // 128 rows x D bf16
   static constexpr int kKStages = (D == 64) ? 2 : 1;
@@ -56,7 +65,12 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
   constexpr int VS = Cfg::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  __shared__ uint64_t bar_q, bar_kf[KS], bar_ke[KS], bar_vf[VS], bar_ve[VS], bar_s, bar_p, bar_o, bar_drain;
+  constexpr bool kSepP = Cfg::kSepP;
+  constexpr uint32_t kColP = Cfg::kColP, kColO = Cfg::kColO;
+  // bar_s: S(j) in TMEM (MMA commit); bar_sfree: every softmax thread holds S(j)
+  // in registers (d = 64 only); bar_p: P(j) in TMEM; bar_pfree: PV(j) done (d = 64).
+  __shared__ uint64_t bar_q, bar_kf[KS], bar_ke[KS], bar_vf[VS], bar_ve[VS], bar_s, bar_sfree, bar_p, bar_pfree, bar_o,
+      bar_drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -78,7 +92,9 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
     for (int s = 0; s < KS; ++s) { mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1); }
     for (int s = 0; s < VS; ++s) { mbar_init(&bar_vf[s], 1); mbar_init(&bar_ve[s], 1); }
     mbar_init(&bar_s, 1);
+    mbar_init(&bar_sfree, 128);
     mbar_init(&bar_p, 128);
+    mbar_init(&bar_pfree, 1);
     mbar_init(&bar_o, 1);
     mbar_init(&bar_drain, 1);
     abort_sh = 0;
@@ -143,56 +159,80 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
-      const uint32_t sQ = smem_u32(smem + Cfg::kOffQ);
-      const uint32_t sK = smem_u32(smem + Cfg::kOffK);
-      const uint32_t sV = smem_u32(smem + Cfg::kOffV);
-      bool issued = false;
-      auto issue_pv = [&](int jj) -> bool {
-        const int vs = jj % VS;
-        if (!mbar_wait(&bar_p, jj & 1, ctx, 12)) return false;
-        if (!mbar_wait(&bar_vf[vs], (jj / VS) & 1, ctx, 13)) return false;
-        tc_fence_after();
-        const uint32_t vbase = sV + vs * Cfg::kTileBytes;
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+    const uint64_t dQ = sdesc_sw128(smem_u32(smem + Cfg::kOffQ), 16, 1024);
+    const uint64_t dK = sdesc_sw128(smem_u32(smem + Cfg::kOffK), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(smem + Cfg::kOffV), kHalfTileBytes, 1024);
+    constexpr uint32_t kTileD = Cfg::kTileBytes >> 4;  // descriptor units
+    bool issued = false;
+    auto commit = [&](uint64_t* bar) {
+      if (elect_one()) mma_commit(bar);
+      __syncwarp();
+    };
+    auto issue_s = [&](int j) -> bool {
+      const int ks = j % KS;
+      if (!warp_wait(&bar_kf[ks], (j / KS) & 1, ctx, 11)) return false;
+      tc_fence_after();
+      const uint64_t kb = dK + ks * kTileD;
+      if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, kHalfTileBytes, 1024);
-          mma_ts(tmem + kColO, tmem + kColS + kk * 8, bdesc, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = static_cast<uint32_t>(((kk >> 2) * kHalfTileBytes + (kk & 3) * 32) >> 4);
+          mma_ss(tmem + kColS, dQ + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
         }
+        mma_commit(&bar_s);
+        mma_commit(&bar_ke[ks]);
+      }
+      __syncwarp();
+      issued = true;
+      return true;
+    };
+    auto issue_pv = [&](int jj) -> bool {
+      const int vs = jj % VS;
+      if (!warp_wait(&bar_p, jj & 1, ctx, 12)) return false;
+      if (!warp_wait(&bar_vf[vs], (jj / VS) & 1, ctx, 13)) return false;
+      tc_fence_after();
+      const uint64_t vb = dV + vs * kTileD;
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + kColO, tmem + kColP + kk * 8, vb + kk * 128, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+        if (kSepP) mma_commit(&bar_pfree);
         mma_commit(&bar_ve[vs]);
-        return true;
-      };
-      bool ok = mbar_wait(&bar_q, 0, ctx, 10);
+      }
+      __syncwarp();
+      issued = true;
+      return true;
+    };
+    bool ok = warp_wait(&bar_q, 0, ctx, 10);
+    if (kSepP) {
+      // S(j+1) as soon as the softmax holds S(j); PV(j) once P(j) is written.
+      if (ok) ok = issue_s(0);
       for (int j = 0; j < n_kv && ok; ++j) {
-        const int ks = j % KS;
+        if (j + 1 < n_kv) {
+          ok = warp_wait(&bar_sfree, j & 1, ctx, 14);
+          if (ok) ok = issue_s(j + 1);
+          if (!ok) break;
+        }
+        ok = issue_pv(j);
+      }
+    } else {
+      for (int j = 0; j < n_kv && ok; ++j) {
         // O += P_{j-1} V_{j-1} must be issued before S_j overwrites P_{j-1}.
         if (j > 0) {
           ok = issue_pv(j - 1);
           if (!ok) break;
         }
-        ok = mbar_wait(&bar_kf[ks], (j / KS) & 1, ctx, 11);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kbase = sK + ks * Cfg::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-          mma_ss(tmem + kColS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
-        }
-        issued = true;
-        mma_commit(&bar_s);
-        mma_commit(&bar_ke[ks]);
+        ok = issue_s(j);
       }
       if (ok) ok = issue_pv(n_kv - 1);
-      if (ok) {
-        mma_commit(&bar_o);
-      } else if (issued) {
-        mma_commit(&bar_drain);
-        mbar_wait_drain(&bar_drain, 0, p.budget_ns);
-      }
+    }
+    if (ok) {
+      commit(&bar_o);
+    } else if (issued) {
+      commit(&bar_drain);
+      mbar_wait_drain(&bar_drain, 0, p.budget_ns);
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroup
@@ -201,6 +241,7 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
     const int q_idx = qt * kTile + row;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_base + kColS;
+    const uint32_t tP = tmem + lane_base + kColP;
     const uint32_t tO = tmem + lane_base + kColO;
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY;  // running max in log2 units (possibly stale by <= 8)
@@ -219,6 +260,11 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < kTile; ++i) s[i] = __uint_as_float(r[i]);
+      }
+      if (kSepP) {
+        // S is in registers: the MMA may compute S(j+1) into the same columns.
+        tc_fence_before();
+        mbar_arrive(&bar_sfree);
       }
       if (p.causal && j == qt) {
 #pragma unroll
@@ -250,22 +296,35 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
         m_used = m_tile;
         l *= alpha;
       }
-      const float neg_m = -m_used;
-      float lsum[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+      // p = 2^(s*c - m) two columns at a time (packed fp32 FMA and add), bf16 pairs kept
+      // in registers until the P columns are free.
+      const uint64_t c2 = f2_make(sl2, sl2), nm2 = f2_make(-m_used, -m_used);
+      uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};  // independent partial sums of pairs
+      uint32_t pk[kTile / 2];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, neg_m));
-          const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, neg_m));
-          lsum[i & 3] += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tS + c * 16, pk);
+      for (int i = 0; i < kTile / 2; ++i) {
+        float x0, x1;
+        f2_split(f2_fma(f2_make(s[2 * i], s[2 * i + 1]), c2, nm2), x0, x1);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        lsum[i & 3] = f2_add(lsum[i & 3], f2_make(p0, p1));
+        pk[i] = pack_bf16x2(p0, p1);
       }
-      l += (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
-      // Rescale O (already complete: S_j's commit follows PV_{j-1}) when any row of this warp needs it.
+      {
+        float a0, a1, b0, b1;
+        f2_split(f2_add(f2_add(lsum[0], lsum[1]), f2_add(lsum[2], lsum[3])), a0, a1);
+        l += a0 + a1;
+        (void)b0;
+        (void)b1;
+      }
+      // d = 64: P(j-1) and O must no longer be read by PV(j-1).
+      if (kSepP && j > 0) {
+        ok = warp_wait(&bar_pfree, (j - 1) & 1, ctx, 22);
+        if (!ok) break;
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c * 16]));
+      // Rescale O (complete: PV_{j-1} has finished) when any row of this warp needs it.
       if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
