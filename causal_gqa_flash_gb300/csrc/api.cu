@@ -159,6 +159,8 @@ gqa_status_t make_map(const char* fn, const char* name, CUtensorMap* m, const vo
 }
 
 size_t round_up_tile(int T) { return ((size_t)T + kTile - 1) / kTile * kTile; }
+// Task counters of the persistent dQ / dK/dV launch, after the two fp32 arrays.
+constexpr size_t kSchedBytes = 256;
 
 }  // namespace
 
@@ -174,7 +176,7 @@ void attn_set_wait_budget_ns(unsigned long long budget_ns) {
 
 size_t attn_bwd_workspace_bytes(int B, int T, int Hq) {
   if (B <= 0 || T <= 0 || Hq <= 0) return 0;
-  return 2 * (size_t)B * (size_t)Hq * round_up_tile(T) * sizeof(float);
+  return 2 * (size_t)B * (size_t)Hq * round_up_tile(T) * sizeof(float) + kSchedBytes;
 }
 
 gqa_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int Hq,
@@ -216,7 +218,7 @@ namespace {
 
 // Checks shared by the backward stages; fills the workspace pointers.
 gqa_status_t check_workspace(const char* fn, const void* workspace, size_t workspace_bytes, int B, int T, int Hq,
-                             float** Dvec, float** lse2, int* Tpad) {
+                             float** Dvec, float** lse2, int* Tpad, unsigned** sched) {
   gqa_status_t s;
   if ((s = check_ptr(fn, "workspace", workspace))) return s;
   const size_t need = attn_bwd_workspace_bytes(B, T, Hq);
@@ -225,12 +227,14 @@ gqa_status_t check_workspace(const char* fn, const void* workspace, size_t works
   *Tpad = (int)round_up_tile(T);
   *Dvec = static_cast<float*>(const_cast<void*>(workspace));
   *lse2 = *Dvec + (size_t)B * Hq * (*Tpad);
+  *sched = reinterpret_cast<unsigned*>(*lse2 + (size_t)B * Hq * (*Tpad));
   return GQA_OK;
 }
 
 // Parameters of the dQ and dK/dV kernels (shape, pointers and tensor maps already checked by the caller).
 gqa_status_t make_bwd_params(const char* fn, BwdParams* p, const void* q, const void* k, const void* v,
-                             const void* dO, float* Dvec, float* lse2, int Tpad, int B, int T, int Hq, int Hkv,
+                             const void* dO, float* Dvec, float* lse2, unsigned* sched, int Tpad, int B, int T,
+                             int Hq, int Hkv,
                              int d, int causal, DeviceState* ds) {
   memset(p, 0, sizeof(*p));
   gqa_status_t s;
@@ -240,6 +244,7 @@ gqa_status_t make_bwd_params(const char* fn, BwdParams* p, const void* q, const 
     return s;
   p->Dvec = Dvec;
   p->lse2 = lse2;
+  p->sched = sched;
   p->B = B;
   p->T = T;
   p->Hq = Hq;
@@ -261,8 +266,9 @@ gqa_status_t bwd_preprocess_impl(const char* fn, const void* o, const float* lse
   if ((s = check_shape(fn, B, T, Hq, 1, d))) return s;
   if ((s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)) || (s = check_ptr(fn, "dO", dO))) return s;
   float *Dvec, *lse2;
+  unsigned* sched;
   int Tpad;
-  if ((s = check_workspace(fn, workspace, workspace_bytes, B, T, Hq, &Dvec, &lse2, &Tpad))) return s;
+  if ((s = check_workspace(fn, workspace, workspace_bytes, B, T, Hq, &Dvec, &lse2, &Tpad, &sched))) return s;
   DeviceState* ds = nullptr;
   if ((s = device_state(fn, &ds))) return s;
   BwdPreParams pp;
@@ -271,6 +277,7 @@ gqa_status_t bwd_preprocess_impl(const char* fn, const void* o, const float* lse
   pp.lse = lse;
   pp.Dvec = Dvec;
   pp.lse2 = lse2;
+  pp.sched = sched;
   pp.B = B;
   pp.T = T;
   pp.Hq = Hq;
@@ -292,12 +299,13 @@ gqa_status_t bwd_main_impl(const char* fn, int which, const void* q, const void*
   if ((which & 1) && (s = check_ptr(fn, "dq", dq))) return s;
   if ((which & 2) && ((s = check_ptr(fn, "dk", dk)) || (s = check_ptr(fn, "dv", dv)))) return s;
   float *Dvec, *lse2;
+  unsigned* sched;
   int Tpad;
-  if ((s = check_workspace(fn, workspace, workspace_bytes, B, T, Hq, &Dvec, &lse2, &Tpad))) return s;
+  if ((s = check_workspace(fn, workspace, workspace_bytes, B, T, Hq, &Dvec, &lse2, &Tpad, &sched))) return s;
   DeviceState* ds = nullptr;
   if ((s = device_state(fn, &ds))) return s;
   BwdParams p;
-  if ((s = make_bwd_params(fn, &p, q, k, v, dO, Dvec, lse2, Tpad, B, T, Hq, Hkv, d, causal, ds))) return s;
+  if ((s = make_bwd_params(fn, &p, q, k, v, dO, Dvec, lse2, sched, Tpad, B, T, Hq, Hkv, d, causal, ds))) return s;
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
@@ -348,8 +356,9 @@ gqa_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o
       (s = check_ptr(fn, "dq", dq)) || (s = check_ptr(fn, "dk", dk)) || (s = check_ptr(fn, "dv", dv)))
     return s;
   float *Dvec, *lse2;
+  unsigned* sched;
   int Tpad;
-  if ((s = check_workspace(fn, workspace, workspace_bytes, B, T, Hq, &Dvec, &lse2, &Tpad))) return s;
+  if ((s = check_workspace(fn, workspace, workspace_bytes, B, T, Hq, &Dvec, &lse2, &Tpad, &sched))) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if ((s = bwd_preprocess_impl(fn, o, lse, dO, workspace, workspace_bytes, B, T, Hq, d, st))) return s;
   return bwd_main_impl(fn, 3, q, k, v, dO, dq, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv, d, causal, st);

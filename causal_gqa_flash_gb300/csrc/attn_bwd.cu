@@ -52,6 +52,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
   constexpr int TPR = D / 8;
   pdl_launch_dependents();
   pdl_wait_previous();
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    p.sched[0] = 0u;  // task counters of the dQ / dK/dV launch
+    p.sched[1] = 0u;
+  }
   const long long nrows = static_cast<long long>(p.B) * p.Hq * p.T;
   const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long r = gtid / TPR;  // ((b * Hq + h) * T + t)
@@ -98,78 +102,101 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
 }
 
 // ============================================================================
-// dQ and dK/dV: one launch, two kinds of task.
+// dQ and dK/dV: one persistent launch, two kinds of task.
 //
-// CTA = 19 warps: warp 0 issues TMA, warp 1 issues the S and dP MMAs and owns
-// TMEM, warps 2-17 are four compute warpgroups, warp 18 issues the gradient MMAs. Each compute thread owns one TMEM lane
-// (one row) and its warpgroup owns 32 of the 128 score columns.
+// One CTA per SM (all 512 TMEM columns) loops over tasks taken from a counter
+// in the workspace, heaviest first: tasks [0, n_dkv) are dK/dV tasks (one per
+// key tile, kv head, batch; key tile ascending = causal cost descending), the
+// following n_dq are dQ tasks (query tile descending). Every output element is
+// written by the one task that owns it, so which CTA runs a task does not
+// change any result.
 //
-// Blocks [0, n_dkv) are dK/dV tasks (one per key tile, kv head, batch; key tile
-// ascending = causal cost descending); the following n_dq blocks are dQ tasks
-// (query tile descending). Both kinds allocate all 512 TMEM columns, so one CTA
-// runs per SM and the heaviest tasks start first.
+// CTA = 19 warps: warp 0 fetches tasks and issues TMA, warp 1 issues the S and
+// dP MMAs and owns TMEM, warps 2-17 are four compute warpgroups, warp 18 issues
+// the gradient MMAs. Each compute thread owns one TMEM lane (one row) and its
+// warpgroup owns 32 of the 128 score columns.
 //
-// Pipeline per iteration `it` (one 128x128 score tile):
-//   compute: load its 32 columns of S(it) and dP(it) into registers and release
+// Pipeline per score tile (global index G, counted over all tasks of the CTA):
+//   compute: load its 32 columns of S(G) and dP(G) into registers and release
 //            both accumulators at once (sdp_free); P = 2^(S*scale*log2e - LSE2),
 //            dS = P (dP - D) in registers; bf16 P and dS into their own TMEM
-//            region once the gradient MMAs of it-1 have read it (pds_free), then
+//            region once the gradient MMAs of G-1 have read it (pds_free), then
 //            pds_full.
-//   MMA:     S(it+1), dP(it+1) as soon as sdp_free(it) | gradient MMAs of it on
-//            pds_full(it).
-// so the tensor core computes the scores of it+1 while the compute warps work on
-// it, and the compute warps never wait for a half-read accumulator.
+//   MMA:     S(G+1), dP(G+1) as soon as sdp_free(G) | gradient MMAs of G on
+//            pds_full(G).
+// so the tensor core computes the scores of G+1 while the compute warps work on
+// G, across task boundaries too: the next task's operands are loaded and its
+// first scores computed while this task's last tile and epilogue run.
+// Per task: fixed_full (its fixed operands are in shared memory), fixed_free
+// (its last S/dP MMAs are done, the fixed operands may be replaced), acc_full
+// (its last gradient MMAs are done), acc_free (the epilogue has read its
+// accumulators, the next task's first gradient MMA may overwrite them).
 //
 // TMEM columns (S and dP are 128 fp32 columns; P and dS 64 columns of bf16 pairs):
 //   dQ:        S [0,128) dP [128,256) dS [256,320) dQ [320,320+D)
 //   dK/dV 64:  S [0,128) dP [128,256) P [256,320) dS [320,384) dV [384,448) dK [448,512)
 //   dK/dV 128: S [0,128) dP [128,256) dV [256,384) dK [384,512); no room for a separate
 //              P/dS region, so P goes to S columns [0,64) and dS to [64,128) once every
-//              warpgroup has read S (sdp_free), and S(it+1) follows the gradient MMAs.
+//              warpgroup has read S (sdp_free), and S(G+1) follows the gradient MMAs
+//              (warp 1 then issues every MMA of the task).
 // Warpgroup g writes the bf16 pairs of its score columns [32g, 32g+32) to columns
 // [16g, 16g+16) of the P (dS) region, so the A operand of K-step kk is at 8*kk.
 // ============================================================================
 constexpr int kMainThreads = 608;
 constexpr int kComputeThreads = 512;
-constexpr int kGradWarp = 18;  // second MMA issuer (gradient MMAs)
+constexpr int kGradWarp = 18;       // second MMA issuer (gradient MMAs)
+constexpr int kTaskConsumers = 18;  // warps 1..18 each take every task from the producer
 
 template <int D>
 struct MainCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = kHalves * kHalfTileBytes;
   static constexpr int kAuxBytes = 4096;  // 128 rows x 16 bf16, unswizzled K-major (one K-step)
-  // dQ task: [Q][dO][QX][DX][ONES], K ring, V ring
+  static constexpr int kOffOnes = 0;      // both layouts: the ONES operand, written once
+  // Fixed operands of a task (dQ: Q, dO, QX, DX; dK/dV: K, V) are double-buffered
+  // at d = 64, so the next task's are loaded while this task runs.
+  static constexpr int kNF = (D == 64) ? 2 : 1;
+  // dQ task: fixed buffers [Q][dO][QX][DX], K ring, V ring
   static constexpr int kDqKStages = 3;
   static constexpr int kDqVStages = (D == 64) ? 2 : 1;
-  static constexpr int kDqOffQ = 0;
-  static constexpr int kDqOffDO = kTileBytes;
-  static constexpr int kDqOffQX = 2 * kTileBytes;
+  static constexpr int kDqFixBytes = 2 * kTileBytes + 2 * kAuxBytes;
+  static constexpr int kDqOffQ = kAuxBytes;  // buffer 0; buffer f adds f * kDqFixBytes
+  static constexpr int kDqOffDO = kDqOffQ + kTileBytes;
+  static constexpr int kDqOffQX = kDqOffDO + kTileBytes;
   static constexpr int kDqOffDX = kDqOffQX + kAuxBytes;
-  static constexpr int kDqOffOnes = kDqOffDX + kAuxBytes;
-  static constexpr int kDqOffK = kDqOffOnes + kAuxBytes;
+  static constexpr int kDqOffK = kAuxBytes + kNF * kDqFixBytes;
   static constexpr int kDqOffV = kDqOffK + kDqKStages * kTileBytes;
   static constexpr int kDqBytes = kDqOffV + kDqVStages * kTileBytes;
-  // dK/dV task: [K][V][ONES], stages of [Q][dO][QX][DX] (d = 128) or
-  // [dO][ZERO][Q][QX][DX] (d = 64). At d = 64 the gradient MMAs compute [dV | dK]
-  // as one N = 128 chain over the block-diagonal operand [dO | 0] (P steps) and
-  // [0 | Q] (dS steps): the zero tile sits between dO and Q so one LBO spans both.
-  // N = 64 MMAs run well below the tensor peak when the compute warps stream
-  // TMEM at the same time; N = 128 ones do not.
+  // dK/dV task: fixed buffers [K][V], then the Q/dO stage ring. At d = 64 the
+  // gradient MMAs compute [dV | dK] as one N = 128 chain over the block-diagonal
+  // operands [dO_s | 0] (P steps) and [0 | Q_s] (dS steps): one zero tile Z is
+  // shared by all stages, with dO_s = Z - (s+1) tiles and Q_s = Z + (s+1) tiles,
+  // so the LBO of stage s, (s+1) tiles, spans both. At d = 128 a stage is
+  // [Q][dO][QX][DX].
   static constexpr bool kBlockDiag = (D == 64);
   static constexpr int kKvStages = (D == 64) ? 3 : 2;   // Q/dO stages
-  static constexpr int kStOffDO = kBlockDiag ? 0 : kTileBytes;
-  static constexpr int kStOffZ = kTileBytes;             // d = 64 only
-  static constexpr int kStOffQ = kBlockDiag ? 2 * kTileBytes : 0;
-  static constexpr int kStOffQX = kBlockDiag ? 3 * kTileBytes : 2 * kTileBytes;
-  static constexpr int kStOffDX = kStOffQX + kAuxBytes;
-  static constexpr int kStageBytes = kStOffDX + kAuxBytes;
-  static constexpr int kKvOffK = 0;
-  static constexpr int kKvOffV = kTileBytes;
-  static constexpr int kKvOffOnes = 2 * kTileBytes;
-  static constexpr int kKvOffStage = 2 * kTileBytes + kAuxBytes;
-  static constexpr int kKvBytes = kKvOffStage + kKvStages * kStageBytes;
+  static constexpr int kKvFixBytes = 2 * kTileBytes;
+  static constexpr int kKvOffK = kAuxBytes;             // buffer 0; buffer f adds f * kKvFixBytes
+  static constexpr int kKvOffV = kKvOffK + kTileBytes;
+  static constexpr int kKvOffStages = kAuxBytes + kNF * kKvFixBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kAuxBytes;  // d = 128 stage stride
+  static constexpr int kKvOffZ = kKvOffStages + kKvStages * kTileBytes;  // d = 64
+  static constexpr int kKvOffAux = kKvOffStages + (2 * kKvStages + 1) * kTileBytes;  // d = 64: [QX_s][DX_s]
+  static constexpr int kKvBytes =
+      kBlockDiag ? kKvOffAux + kKvStages * 2 * kAuxBytes : kKvOffStages + kKvStages * kStageBytes;
+  __host__ __device__ static constexpr int st_q(int s) {
+    return kBlockDiag ? kKvOffZ + (s + 1) * kTileBytes : kKvOffStages + s * kStageBytes;
+  }
+  __host__ __device__ static constexpr int st_do(int s) {
+    return kBlockDiag ? kKvOffZ - (s + 1) * kTileBytes : kKvOffStages + s * kStageBytes + kTileBytes;
+  }
+  __host__ __device__ static constexpr int st_qx(int s) {
+    return kBlockDiag ? kKvOffAux + s * 2 * kAuxBytes : kKvOffStages + s * kStageBytes + 2 * kTileBytes;
+  }
+  __host__ __device__ static constexpr int st_dx(int s) { return st_qx(s) + kAuxBytes; }
   static constexpr int kUsed = (kDqBytes > kKvBytes ? kDqBytes : kKvBytes) + 1024;
   static constexpr int kSmemBytes = kUsed > kOneCtaPerSmSmem ? kUsed : kOneCtaPerSmSmem;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   // TMEM columns
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColDP = 128;
@@ -206,39 +233,28 @@ __device__ __forceinline__ void write_ones_row(uint8_t* tile, int row) {
   *reinterpret_cast<uint4*>(tile + aux_off(row, 1)) = make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Store NCOLS (16 or a multiple of 32) fp32 columns of this thread's row as bf16 to dst.
-template <int NCOLS>
-__device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* dst, float scale, bool valid) {
-  if constexpr (NCOLS == 16) {
-    uint32_t r[16];
+// Load NC (16 or a multiple of 32) fp32 accumulator columns of this thread's row.
+template <int NC>
+__device__ __forceinline__ void load_acc(uint32_t taddr, uint32_t (&r)[NC]) {
+  if constexpr (NC == 16) {
     tmem_ld16(taddr, r);
-    tmem_wait_ld();
-    uint32_t pk[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
-    if (valid) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
-      d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-    }
   } else {
-    static_assert(NCOLS % 32 == 0, "NCOLS");
+    static_assert(NC % 32 == 0, "NC");
 #pragma unroll
-    for (int c = 0; c < NCOLS / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(taddr + c * 32, r);
-      tmem_wait_ld();
-      uint32_t pk[16];
+    for (int c = 0; c < NC / 32; ++c) tmem_ld32(taddr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+  }
+}
+
+// Store NC accumulator values of one row as bf16 (times scale) to dst.
+template <int NC>
+__device__ __forceinline__ void store_acc_bf16(const uint32_t (&r)[NC], __nv_bfloat16* dst, float scale) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
-      if (valid) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+  for (int v = 0; v < NC / 8; ++v) {
+    uint32_t w[4];
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) d4[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-      }
-    }
+    for (int i = 0; i < 4; ++i)
+      w[i] = pack_bf16x2(__uint_as_float(r[8 * v + 2 * i]) * scale, __uint_as_float(r[8 * v + 2 * i + 1]) * scale);
+    reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -262,23 +278,58 @@ __device__ __forceinline__ void score_chunk(const uint32_t (&s)[32], const uint3
   }
 }
 
-// Barriers of one task. Every one of them is at most one phase ahead of any
-// waiter: sdp_full(it+1) is committed only after sdp_free(it) completed, which
-// needs every compute thread to have passed sdp_full(it); pds_full(it+1) needs
-// pds_free(it), which the MMA thread commits only after it saw pds_full(it);
-// and the reverse pairs likewise.
+// Every barrier is at most one phase ahead of any waiter: sdp_full(G+1) is
+// committed only after sdp_free(G) completed, which needs every compute thread
+// to have passed sdp_full(G); pds_full(G+1) needs pds_free(G), which is committed
+// only after pds_full(G) was seen; fixed_full of a buffer is produced again only
+// after its fixed_free was seen, which needs that fixed_full; acc_free(n) needs acc_full(n)
+// and acc_full(n+1) needs acc_free(n); task_full(n+2) needs task_empty(n).
 struct MainBars {
-  uint64_t fixed, full[3], empty[3], vfull[2], vempty[2];
-  uint64_t sdp_full;  // MMA -> compute: S(it) and dP(it) are in TMEM
-  uint64_t sdp_free;  // compute -> MMA: every thread has S(it), dP(it) in registers
-  uint64_t pds_full;  // compute -> MMA: bf16 P/dS of it are in TMEM
-  uint64_t pds_free;  // MMA -> compute: the gradient MMAs of it have completed
-  uint64_t fin, drain, drain2;
+  uint64_t task_full[2], task_empty[2];   // producer <-> every other warp: next task index
+  uint64_t fixed_full[2], fixed_free[2];   // per fixed buffer: operands loaded / no longer read
+  uint64_t kv_full[3], kv_empty[3];        // dK/dV stage ring
+  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];  // dQ K and V rings
+  uint64_t sdp_full;  // MMA -> compute: S(G) and dP(G) are in TMEM
+  uint64_t sdp_free;  // compute -> MMA: every thread has S(G), dP(G) in registers
+  uint64_t pds_full;  // compute -> MMA: bf16 P/dS of G are in TMEM
+  uint64_t pds_free;  // MMA -> compute: the gradient MMAs of G have completed
+  uint64_t acc_full;  // MMA -> compute (and producer): every MMA of the task is done
+  uint64_t acc_free;  // compute -> MMA: the task's accumulators are in registers
+  uint64_t drain, drain2;
 };
 
 struct TaskInfo {
-  int b, kvh, h, tile, n_it, i0, ni;
+  int dkv, b, kvh, h, tile, n_it, i0, ni;
 };
+
+__device__ __forceinline__ TaskInfo decode_task(const BwdParams& p, int id) {
+  TaskInfo t;
+  t.h = 0;
+  t.i0 = 0;
+  t.ni = 1;
+  if (id < p.n_dkv_tasks) {
+    t.dkv = 1;
+    const int nbk = p.B * p.Hkv;
+    t.tile = id / nbk;
+    const int bk = id % nbk;
+    t.b = bk / p.Hkv;
+    t.kvh = bk % p.Hkv;
+    t.i0 = p.causal ? t.tile : 0;
+    t.ni = p.nT - t.i0;
+    t.n_it = p.G * t.ni;
+  } else {
+    t.dkv = 0;
+    const int q = id - p.n_dkv_tasks;
+    const int nbh = p.B * p.Hq;
+    t.tile = p.nT - 1 - q / nbh;
+    const int bh = q % nbh;
+    t.b = bh / p.Hq;
+    t.h = bh % p.Hq;
+    t.kvh = t.h / p.G;
+    t.n_it = p.causal ? t.tile + 1 : p.nT;
+  }
+  return t;
+}
 
 // Descriptor offset (in 16-byte units) of K-step kk inside a K-major tile of
 // 64-wide halves: 32 bytes per step inside a 128-byte row, a new half every 4 steps.
@@ -286,47 +337,89 @@ __device__ __forceinline__ constexpr uint32_t kmaj_step(int kk) {
   return static_cast<uint32_t>(((kk >> 2) * kHalfTileBytes + (kk & 3) * 32) >> 4);
 }
 
-// One task of either kind, all roles. Every pipeline depth is a compile-time
-// constant and every MMA descriptor is a base plus a constant, so the single
-// issuing thread spends a few instructions per MMA.
-template <int D, bool DKV>
-__device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, MainBars& bars, uint32_t tmem,
-                                         const WaitCtx& ctx, const TaskInfo& t, int warp, int lane) {
-  using Cfg = MainCfg<D>;
-  constexpr bool kSep = DKV ? Cfg::kKvSepPdS : true;           // P/dS region separate from S
-  constexpr uint32_t colP = DKV ? Cfg::kKvColP : 0;
-  constexpr uint32_t colDS = DKV ? Cfg::kKvColDS : Cfg::kDqColDS;
-  constexpr int NST = DKV ? Cfg::kKvStages : Cfg::kDqKStages;  // main ring depth
-  constexpr int NV = Cfg::kDqVStages;                         // dQ V ring depth
-  constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: N = 128
-  constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);    // gradients: N = D, B MN-major
-  constexpr uint32_t kTileD = Cfg::kTileBytes >> 4;             // tile stride, descriptor units
-  constexpr uint32_t kStageD = Cfg::kStageBytes >> 4;
-  const int n_it = t.n_it;
-  const float inv_sl2 = 1.f / p.scale_log2;
+// Lane 0 waits, the warp agrees on the outcome.
+__device__ __forceinline__ bool lane0_wait(uint64_t* bar, uint32_t parity, const WaitCtx& c, unsigned where,
+                                           int lane) {
+  bool ok = true;
+  if (lane == 0) ok = mbar_wait(bar, parity, c, where);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
 
-  if (warp == 0) {
-    // ============================================================ producer warp
-    // Lane 0 issues TMA and waits; all 32 lanes write the unswizzled ONES / QX / DX
-    // operands (4 rows each) from the workspace's -LSE2 and D.
+// Task n of this CTA as published by the producer (-1: no more); every consumer
+// warp arrives once on task_empty after reading it.
+__device__ __forceinline__ int recv_task(MainBars& bars, const volatile int* slot, int n, const WaitCtx& ctx,
+                                         int lane, bool& ok) {
+  ok = warp_wait(&bars.task_full[n & 1], (n >> 1) & 1, ctx, 40);
+  const int id = ok ? slot[n & 1] : -1;
+  __syncwarp();
+  if (ok && lane == 0) mbar_arrive(&bars.task_empty[n & 1]);
+  return id;
+}
+
+// ============================================================================ producer
+template <int D>
+__device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem, MainBars& bars, volatile int* slot,
+                                              const WaitCtx& ctx, int lane) {
+  using Cfg = MainCfg<D>;
+  constexpr int NKV = Cfg::kKvStages, NK = Cfg::kDqKStages, NV = Cfg::kDqVStages, NF = Cfg::kNF;
+  const int n_tasks = p.n_dkv_tasks + p.n_dq_tasks;
+  const float inv_sl2 = 1.f / p.scale_log2;
+  if (lane == 0) {
+    tma_prefetch_desc(&p.tmap_q);
+    tma_prefetch_desc(&p.tmap_k);
+    tma_prefetch_desc(&p.tmap_v);
+    tma_prefetch_desc(&p.tmap_do);
+  }
+  for (int r = lane; r < kTile; r += 32) write_ones_row(smem + Cfg::kOffOnes, r);
+  fence_proxy_async_smem();
+  __syncwarp();
+  int kv_used = 0, q_used = 0, n = 0, n_fixed = 0, prev_kind = -1;
+  bool ok = true;
+  for (;; ++n) {
+    int id = -1;
     if (lane == 0) {
-      tma_prefetch_desc(&p.tmap_q);
-      tma_prefetch_desc(&p.tmap_k);
-      tma_prefetch_desc(&p.tmap_v);
-      tma_prefetch_desc(&p.tmap_do);
+      const int x = static_cast<int>(atomicAdd(p.sched, 1u));
+      id = x < n_tasks ? x : -1;
     }
-    int issued[3] = {0, 0, 0}, vissued[2] = {0, 0};
-    bool ok = true;
+    id = __shfl_sync(0xffffffffu, id, 0);
+    if (n >= 2) ok = lane0_wait(&bars.task_empty[n & 1], ((n - 2) >> 1) & 1, ctx, 41, lane);
+    // Pace on acc_free: the compute warps finish the epilogue of n-1 only after
+    // they received task n, so waiting for epilogue n-2 here keeps this warp in
+    // step with that barrier for the wait on n-1 below.
+    if (ok && n >= 2) ok = lane0_wait(&bars.acc_free, (n - 2) & 1, ctx, 44, lane);
+    if (!ok) break;
+    if (lane == 0) {
+      slot[n & 1] = id;
+      mbar_arrive(&bars.task_full[n & 1]);
+    }
+    if (id < 0) break;
+    const TaskInfo t = decode_task(p, id);
+    // Fixed buffer f held task n-NF, free once that task's last S/dP MMAs are
+    // done; a change of layout needs every MMA of the previous task done (its
+    // epilogue has read the accumulators, so they are).
+    const int f = n % NF, fu = n / NF;
+    if (fu > 0) ok = lane0_wait(&bars.fixed_free[f], (fu - 1) & 1, ctx, 42, lane);
+    if (ok && n > 0 && t.dkv != prev_kind) ok = lane0_wait(&bars.acc_free, (n - 1) & 1, ctx, 43, lane);
+    if (!ok) break;
     const size_t vec_bh0 = (static_cast<size_t>(t.b) * p.Hq) * p.Tpad;
-    if (lane == 0) mbar_arrive_expect_tx(&bars.fixed, 2 * Cfg::kTileBytes);
-    if (DKV) {
+    uint64_t* fbar = &bars.fixed_full[f];
+    if (lane == 0) mbar_arrive_expect_tx(fbar, 2 * Cfg::kTileBytes);
+    ++n_fixed;
+    if (t.dkv) {
+      uint8_t* fix = smem + f * Cfg::kKvFixBytes;
       if (lane == 0)
         for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-          tma_load_4d(smem + Cfg::kKvOffK + hf * kHalfTileBytes, &p.tmap_k, &bars.fixed, hf * 64, t.kvh,
-                      t.tile * kTile, t.b);
-          tma_load_4d(smem + Cfg::kKvOffV + hf * kHalfTileBytes, &p.tmap_v, &bars.fixed, hf * 64, t.kvh,
-                      t.tile * kTile, t.b);
+          tma_load_4d(fix + Cfg::kKvOffK + hf * kHalfTileBytes, &p.tmap_k, fbar, hf * 64, t.kvh, t.tile * kTile, t.b);
+          tma_load_4d(fix + Cfg::kKvOffV + hf * kHalfTileBytes, &p.tmap_v, fbar, hf * 64, t.kvh, t.tile * kTile, t.b);
         }
+      if (Cfg::kBlockDiag && prev_kind != 1) {
+        // the shared zero tile of the stages (never written by TMA; dK/dV tasks come first)
+        uint4* z = reinterpret_cast<uint4*>(smem + Cfg::kKvOffZ);
+        for (int i = lane; i < Cfg::kTileBytes / 16; i += 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(fbar);
       // -LSE2 and D of the next stage's 128 query rows, 4 per lane, fetched one
       // stage ahead so their latency hides behind the wait for a free stage.
       float vnl[4], vd[4];
@@ -340,53 +433,38 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
           vd[k] = __ldg(p.Dvec + vec + 32 * k);
         }
       };
-      if (n_it > 0) fetch(0);
-      for (int r = lane; r < kTile; r += 32) write_ones_row(smem + Cfg::kKvOffOnes, r);
-      if (Cfg::kBlockDiag) {
-        // the zero tile of every stage (never written by TMA)
-        for (int st = 0; st < NST; ++st) {
-          uint4* z = reinterpret_cast<uint4*>(smem + Cfg::kKvOffStage + st * Cfg::kStageBytes + Cfg::kStOffZ);
-          for (int i = lane; i < Cfg::kTileBytes / 16; i += 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.fixed);
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int st = it % NST, n = it / NST;
-        if (n > 0 && lane == 0) ok = mbar_wait(&bars.empty[st], (n - 1) & 1, ctx, 1);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+      fetch(0);
+      for (int it = 0; it < t.n_it && ok; ++it, ++kv_used) {
+        const int st = kv_used % NKV, u = kv_used / NKV;
+        if (u > 0) ok = lane0_wait(&bars.kv_empty[st], (u - 1) & 1, ctx, 1, lane);
         if (!ok) break;
         const int hq = t.kvh * p.G + it / t.ni;
         const int qt = t.i0 + it % t.ni;
-        uint8_t* stage = smem + Cfg::kKvOffStage + st * Cfg::kStageBytes;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bars.full[st], 2 * Cfg::kTileBytes);
+          mbar_arrive_expect_tx(&bars.kv_full[st], 2 * Cfg::kTileBytes);
           for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-            tma_load_4d(stage + Cfg::kStOffQ + hf * kHalfTileBytes, &p.tmap_q, &bars.full[st], hf * 64, hq,
+            tma_load_4d(smem + Cfg::st_q(st) + hf * kHalfTileBytes, &p.tmap_q, &bars.kv_full[st], hf * 64, hq,
                         qt * kTile, t.b);
-            tma_load_4d(stage + Cfg::kStOffDO + hf * kHalfTileBytes, &p.tmap_do, &bars.full[st], hf * 64, hq,
+            tma_load_4d(smem + Cfg::st_do(st) + hf * kHalfTileBytes, &p.tmap_do, &bars.kv_full[st], hf * 64, hq,
                         qt * kTile, t.b);
           }
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          write_aux_row(stage + Cfg::kStOffQX, lane + 32 * k, vnl[k] * inv_sl2);
-          write_aux_row(stage + Cfg::kStOffDX, lane + 32 * k, -vd[k]);
+          write_aux_row(smem + Cfg::st_qx(st), lane + 32 * k, vnl[k] * inv_sl2);
+          write_aux_row(smem + Cfg::st_dx(st), lane + 32 * k, -vd[k]);
         }
-        if (it + 1 < n_it) fetch(it + 1);
+        if (it + 1 < t.n_it) fetch(it + 1);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.full[st]);
-        issued[st]++;
+        if (lane == 0) mbar_arrive(&bars.kv_full[st]);
       }
     } else {
+      uint8_t* fix = smem + f * Cfg::kDqFixBytes;
       if (lane == 0)
         for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-          tma_load_4d(smem + Cfg::kDqOffQ + hf * kHalfTileBytes, &p.tmap_q, &bars.fixed, hf * 64, t.h,
-                      t.tile * kTile, t.b);
-          tma_load_4d(smem + Cfg::kDqOffDO + hf * kHalfTileBytes, &p.tmap_do, &bars.fixed, hf * 64, t.h,
-                      t.tile * kTile, t.b);
+          tma_load_4d(fix + Cfg::kDqOffQ + hf * kHalfTileBytes, &p.tmap_q, fbar, hf * 64, t.h, t.tile * kTile, t.b);
+          tma_load_4d(fix + Cfg::kDqOffDO + hf * kHalfTileBytes, &p.tmap_do, fbar, hf * 64, t.h, t.tile * kTile, t.b);
         }
       const size_t vec = vec_bh0 + static_cast<size_t>(t.h) * p.Tpad + static_cast<size_t>(t.tile) * kTile + lane;
       float vnl[4], vd[4];
@@ -397,330 +475,499 @@ __device__ __forceinline__ void run_task(const BwdParams& p, uint8_t* smem, Main
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        write_ones_row(smem + Cfg::kDqOffOnes, lane + 32 * k);
-        write_aux_row(smem + Cfg::kDqOffQX, lane + 32 * k, vnl[k] * inv_sl2);
-        write_aux_row(smem + Cfg::kDqOffDX, lane + 32 * k, -vd[k]);
+        write_aux_row(fix + Cfg::kDqOffQX, lane + 32 * k, vnl[k] * inv_sl2);
+        write_aux_row(fix + Cfg::kDqOffDX, lane + 32 * k, -vd[k]);
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars.fixed);
-        for (int j = 0; j < n_it && ok; ++j) {
-          const int st = j % NST, n = j / NST;
-          if (n > 0) ok = mbar_wait(&bars.empty[st], (n - 1) & 1, ctx, 1);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&bars.full[st], Cfg::kTileBytes);
+      if (lane == 0) mbar_arrive(fbar);
+      for (int j = 0; j < t.n_it && ok; ++j, ++q_used) {
+        const int ks = q_used % NK, ku = q_used / NK;
+        if (ku > 0) ok = lane0_wait(&bars.k_empty[ks], (ku - 1) & 1, ctx, 1, lane);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars.k_full[ks], Cfg::kTileBytes);
           for (int hf = 0; hf < Cfg::kHalves; ++hf)
-            tma_load_4d(smem + Cfg::kDqOffK + st * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_k, &bars.full[st],
-                        hf * 64, t.kvh, j * kTile, t.b);
-          issued[st]++;
-          const int vs = j % NV, vn = j / NV;
-          if (vn > 0) ok = mbar_wait(&bars.vempty[vs], (vn - 1) & 1, ctx, 2);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&bars.vfull[vs], Cfg::kTileBytes);
+            tma_load_4d(smem + Cfg::kDqOffK + ks * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_k,
+                        &bars.k_full[ks], hf * 64, t.kvh, j * kTile, t.b);
+        }
+        const int vs = q_used % NV, vu = q_used / NV;
+        if (vu > 0) ok = lane0_wait(&bars.v_empty[vs], (vu - 1) & 1, ctx, 2, lane);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars.v_full[vs], Cfg::kTileBytes);
           for (int hf = 0; hf < Cfg::kHalves; ++hf)
             tma_load_4d(smem + Cfg::kDqOffV + vs * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v,
-                        &bars.vfull[vs], hf * 64, t.kvh, j * kTile, t.b);
-          vissued[vs]++;
+                        &bars.v_full[vs], hf * 64, t.kvh, j * kTile, t.b);
         }
       }
     }
-    if (lane != 0) return;
-    // Wait until every stage is released, so no MMA commit arrives after exit.
-    for (int s2 = 0; s2 < 3 && ok; ++s2)
-      if (issued[s2] > 0) ok = mbar_wait(&bars.empty[s2], (issued[s2] - 1) & 1, ctx, 3);
-    for (int s2 = 0; s2 < 2 && ok; ++s2)
-      if (vissued[s2] > 0) ok = mbar_wait(&bars.vempty[s2], (vissued[s2] - 1) & 1, ctx, 4);
-    if (!ok) {
-      mbar_wait_drain(&bars.fixed, 0, p.budget_ns);
-      for (int s2 = 0; s2 < 3; ++s2)
-        if (issued[s2] > 0) mbar_wait_drain(&bars.full[s2], (issued[s2] - 1) & 1, p.budget_ns);
-      for (int s2 = 0; s2 < 2; ++s2)
-        if (vissued[s2] > 0) mbar_wait_drain(&bars.vfull[s2], (vissued[s2] - 1) & 1, p.budget_ns);
+    if (!ok) break;
+    prev_kind = t.dkv;
+  }
+  if (lane != 0) return;
+  // Let every commit on a barrier of this CTA land before it exits: the last
+  // fixed_free and the last release of every ring slot.
+  for (int f = 0; f < NF && ok; ++f) {
+    const int uses = n_fixed / NF + (f < n_fixed % NF ? 1 : 0);
+    if (uses > 0) ok = mbar_wait(&bars.fixed_free[f], (uses - 1) & 1, ctx, 3);
+  }
+  for (int s2 = 0; s2 < NKV && ok; ++s2) {
+    const int uses = kv_used / NKV + (s2 < kv_used % NKV ? 1 : 0);
+    if (uses > 0) ok = mbar_wait(&bars.kv_empty[s2], (uses - 1) & 1, ctx, 4);
+  }
+  for (int s2 = 0; s2 < NK && ok; ++s2) {
+    const int uses = q_used / NK + (s2 < q_used % NK ? 1 : 0);
+    if (uses > 0) ok = mbar_wait(&bars.k_empty[s2], (uses - 1) & 1, ctx, 4);
+  }
+  for (int s2 = 0; s2 < NV && ok; ++s2) {
+    const int uses = q_used / NV + (s2 < q_used % NV ? 1 : 0);
+    if (uses > 0) ok = mbar_wait(&bars.v_empty[s2], (uses - 1) & 1, ctx, 4);
+  }
+  if (!ok) {
+    // Abort path: let every load already issued land before the CTA exits.
+    for (int f = 0; f < NF; ++f) {
+      const int uses = n_fixed / NF + (f < n_fixed % NF ? 1 : 0);
+      if (uses > 0) mbar_wait_drain(&bars.fixed_full[f], (uses - 1) & 1, p.budget_ns);
     }
-  } else if (warp == 1 || warp == kGradWarp) {
-    // ============================================================ MMA issuers
-    // All 32 lanes of an issuing warp run its loop; the elected lane (always lane
-    // 0 of the converged warp) issues every MMA and commit, so commits track its
-    // MMAs. With a separate P/dS region, warp 1 issues S and dP and warp kGradWarp
-    // the gradient MMAs, so neither chain of barrier checks and issues holds up the
-    // other; otherwise (dK/dV at d = 128) S(it+1) must follow the gradient MMAs of
-    // it and warp 1 issues everything.
-    constexpr bool kTwoIssuers = kSep;
-    if (!kTwoIssuers && warp == kGradWarp) return;
-    // Base descriptors (stage / slot 0); a stage or K-step moves the start address only.
-    uint64_t dA_S, dA_P, dB_S, dB_P, dG1, dG2, dXA_S, dXA_P, dXB_S, dXB_P;
-    uint32_t strideB_S, strideB_P, strideX;
-    if (DKV) {
-      const uint32_t st0 = smem_u32(smem + Cfg::kKvOffStage);
-      const uint64_t ones = sdesc_noswz(smem_u32(smem + Cfg::kKvOffOnes), 128, 256);
-      dA_S = sdesc_sw128(smem_u32(smem + Cfg::kKvOffK), 16, 1024);             // K
-      dA_P = sdesc_sw128(smem_u32(smem + Cfg::kKvOffV), 16, 1024);             // V
-      dB_S = sdesc_sw128(st0 + Cfg::kStOffQ, 16, 1024);                        // Q   (K-major)
-      dB_P = sdesc_sw128(st0 + Cfg::kStOffDO, 16, 1024);                       // dO  (K-major)
-      if (Cfg::kBlockDiag) {
-        dG1 = sdesc_sw128(st0 + Cfg::kStOffDO, Cfg::kTileBytes, 1024);         // [dO | 0] (MN-major, N = 128)
-        dG2 = sdesc_sw128(st0 + Cfg::kStOffZ, Cfg::kTileBytes, 1024);          // [0 | Q]
-      } else {
-        dG1 = sdesc_sw128(st0 + Cfg::kStOffDO, kHalfTileBytes, 1024);          // dO  (MN-major) for dV
-        dG2 = sdesc_sw128(st0 + Cfg::kStOffQ, kHalfTileBytes, 1024);           // Q   (MN-major) for dK
-      }
-      dXA_S = ones;                                                            // ONES x QX^T  -> -LSE2/c
-      dXA_P = ones;                                                            // ONES x DX^T  -> -D
-      dXB_S = sdesc_noswz(st0 + Cfg::kStOffQX, 128, 256);
-      dXB_P = sdesc_noswz(st0 + Cfg::kStOffDX, 128, 256);
-      strideB_S = kStageD;
-      strideB_P = kStageD;
-      strideX = kStageD;
-    } else {
-      const uint64_t ones = sdesc_noswz(smem_u32(smem + Cfg::kDqOffOnes), 128, 256);
-      dA_S = sdesc_sw128(smem_u32(smem + Cfg::kDqOffQ), 16, 1024);             // Q
-      dA_P = sdesc_sw128(smem_u32(smem + Cfg::kDqOffDO), 16, 1024);            // dO
-      dB_S = sdesc_sw128(smem_u32(smem + Cfg::kDqOffK), 16, 1024);             // K slot 0 (K-major)
-      dB_P = sdesc_sw128(smem_u32(smem + Cfg::kDqOffV), 16, 1024);             // V slot 0 (K-major)
-      dG1 = sdesc_sw128(smem_u32(smem + Cfg::kDqOffK), kHalfTileBytes, 1024);  // K slot 0 (MN-major) for dQ
-      dG2 = 0;
-      dXA_S = sdesc_noswz(smem_u32(smem + Cfg::kDqOffQX), 128, 256);           // QX x ONES^T -> -LSE2/c
-      dXA_P = sdesc_noswz(smem_u32(smem + Cfg::kDqOffDX), 128, 256);           // DX x ONES^T -> -D
-      dXB_S = ones;
-      dXB_P = ones;
-      strideB_S = kTileD;
-      strideB_P = kTileD;
-      strideX = 0;
+    for (int s2 = 0; s2 < NKV; ++s2) {
+      const int uses = kv_used / NKV + (s2 < kv_used % NKV ? 1 : 0);
+      if (uses > 0) mbar_wait_drain(&bars.kv_full[s2], (uses - 1) & 1, p.budget_ns);
     }
-    bool issued_any = false;
-    // S(i); waits for its stage unless the caller already did (dK/dV: one stage carries Q and dO).
-    auto issue_S = [&](int i, bool wait_stage) -> bool {
-      const int st = i % NST;
-      if (wait_stage) {
-        if (!warp_wait(&bars.full[st], (i / NST) & 1, ctx, 11)) return false;
-        tc_fence_after();
-      }
-      const uint32_t dst = tmem + Cfg::kColS;
-      const uint64_t b0 = dB_S + st * strideB_S;
-      if (elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(dst, dA_S + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
-        mma_ss(dst, dXA_S, dXB_S + st * strideX, idesc_s, 1u);
-      }
-      __syncwarp();
-      issued_any = true;
-      return true;
-    };
-    auto issue_dP = [&](int i, bool wait_stage) -> bool {
-      int slot, xst;
-      if (DKV) {
-        slot = i % NST;
-        xst = slot;
-        if (wait_stage) {
-          if (!warp_wait(&bars.full[slot], (i / NST) & 1, ctx, 13)) return false;
-          tc_fence_after();
-        }
-      } else {
-        slot = i % NV;
-        xst = 0;
-        if (!warp_wait(&bars.vfull[slot], (i / NV) & 1, ctx, 13)) return false;
-        tc_fence_after();
-      }
-      const uint64_t b0 = dB_P + slot * strideB_P;
-      if (elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + Cfg::kColDP, dA_P + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
-        mma_ss(tmem + Cfg::kColDP, dXA_P, dXB_P + xst * strideX, idesc_s, 1u);
-        if (!DKV) mma_commit(&bars.vempty[slot]);
-      }
-      __syncwarp();
-      issued_any = true;
-      return true;
-    };
-    auto issue_grad = [&](int i) {
-      const int st = i % NST;
-      const uint32_t tP = tmem + colP, tDS = tmem + colDS;
-      if (elect_one()) {
-        if (DKV && Cfg::kBlockDiag) {
-          // [dV | dK] (128 columns) += [P^T | dS^T] x blockdiag(dO, Q): 16 N = 128 steps
-          constexpr uint32_t idesc_bd = idesc_bf16_f32(128, 128, 0, 1);
-          const uint64_t g1 = dG1 + st * kStageD, g2 = dG2 + st * kStageD;
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + Cfg::kKvColDV, tP + kk * 8, g1 + kk * 128, idesc_bd, (i > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + Cfg::kKvColDV, tDS + kk * 8, g2 + kk * 128, idesc_bd, 1u);
-        } else if (DKV) {
-          const uint64_t g1 = dG1 + st * kStageD, g2 = dG2 + st * kStageD;
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-            mma_ts(tmem + Cfg::kKvColDV, tP + kk * 8, g1 + kk * 128, idesc_g, acc);
-            mma_ts(tmem + Cfg::kKvColDK, tDS + kk * 8, g2 + kk * 128, idesc_g, acc);
-          }
-        } else {
-          const uint64_t g1 = dG1 + st * kTileD;
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + Cfg::kDqColAcc, tDS + kk * 8, g1 + kk * 128, idesc_g, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&bars.pds_free);
-        mma_commit(&bars.empty[st]);
-      }
-      __syncwarp();
-      issued_any = true;
-    };
-    auto commit = [&](uint64_t* bar) {
-      if (elect_one()) mma_commit(bar);
-      __syncwarp();
-    };
-
-    bool ok = true;
-    if (warp == 1) {
-      ok = warp_wait(&bars.fixed, 0, ctx, 10);
-      if (ok) {
-        tc_fence_after();
-        ok = issue_S(0, true);
-      }
-      if (ok) ok = issue_dP(0, !DKV);
-      if (ok) commit(&bars.sdp_full);
+    for (int s2 = 0; s2 < NK; ++s2) {
+      const int uses = q_used / NK + (s2 < q_used % NK ? 1 : 0);
+      if (uses > 0) mbar_wait_drain(&bars.k_full[s2], (uses - 1) & 1, p.budget_ns);
     }
-    if (kTwoIssuers && warp == 1) {
-      // S and dP of it+1 as soon as every compute thread holds S(it), dP(it)
-      for (int it = 0; it + 1 < n_it && ok; ++it) {
-        ok = warp_wait(&bars.sdp_free, it & 1, ctx, 14);
-        if (!ok) break;
-        ok = issue_S(it + 1, true);
-        if (ok) ok = issue_dP(it + 1, !DKV);
-        if (!ok) break;
-        commit(&bars.sdp_full);
-      }
-    } else if (kTwoIssuers) {
-      // gradient MMAs of it once its bf16 P/dS are in TMEM
-      for (int it = 0; it < n_it && ok; ++it) {
-        ok = warp_wait(&bars.pds_full, it & 1, ctx, 12);
-        if (!ok) break;
-        tc_fence_after();
-        issue_grad(it);
-      }
-      // every S/dP MMA completed before the last P/dS was written
-      if (ok) commit(&bars.fin);
-    } else {
-      for (int it = 0; it < n_it && ok; ++it) {
-        const bool has_next = it + 1 < n_it;
-        ok = warp_wait(&bars.sdp_free, it & 1, ctx, 14);
-        if (!ok) break;
-        if (has_next) {
-          ok = issue_dP(it + 1, true);
-          if (!ok) break;
-        }
-        ok = warp_wait(&bars.pds_full, it & 1, ctx, 12);
-        if (!ok) break;
-        tc_fence_after();
-        issue_grad(it);
-        if (has_next) {
-          // P/dS of it live in the S columns: S(it+1) after the gradient MMAs
-          ok = issue_S(it + 1, false);
-          if (!ok) break;
-          commit(&bars.sdp_full);
-        }
-      }
-      if (ok) commit(&bars.fin);
-    }
-    if (!ok && issued_any) {
-      uint64_t* dr = warp == 1 ? &bars.drain : &bars.drain2;
-      commit(dr);
-      mbar_wait_drain(dr, 0, p.budget_ns);
-    }
-  } else {
-    // ============================================================ compute warpgroups
-    const int wg = (warp - 2) >> 2;  // 0..3: score columns [wg*32, wg*32+32)
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_base + Cfg::kColS + wg * 32;
-    const uint32_t tDP = tmem + lane_base + Cfg::kColDP + wg * 32;
-    const uint32_t tP = tmem + lane_base + colP + wg * 16;
-    const uint32_t tDS = tmem + lane_base + colDS + wg * 16;
-    const float sl2 = p.scale_log2;
-    bool ok = true;
-    // One tile: S, dP -> registers -> sdp_free; P, dS -> TMEM -> pds_full.
-    auto tile = [&](int it, bool masked, int lo, int hi) -> bool {
-      if (!warp_wait(&bars.sdp_full, it & 1, ctx, 20)) return false;
-      tc_fence_after();
-      uint32_t s[32], dp[32];
-      tmem_ld32(tS, s);
-      tmem_ld32(tDP, dp);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars.sdp_free);
-      uint32_t pk[16], dk[16];
-      if (masked)
-        score_chunk<DKV, true>(s, dp, sl2, lo, hi, pk, dk);
-      else
-        score_chunk<DKV, false>(s, dp, sl2, lo, hi, pk, dk);
-      // The P/dS region must be free: read by the gradient MMAs of it-1 (separate
-      // region), or S(it) read by every warpgroup (region inside S).
-      if (kSep) {
-        if (it > 0 && !warp_wait(&bars.pds_free, (it - 1) & 1, ctx, 22)) return false;
-      } else {
-        if (!warp_wait(&bars.sdp_free, it & 1, ctx, 23)) return false;
-      }
-      tc_fence_after();
-      if (DKV) tmem_st16(tP, pk);
-      tmem_st16(tDS, dk);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars.pds_full);
-      return true;
-    };
-    if (DKV) {
-      const int k_idx = t.tile * kTile + row;
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int qt = t.i0 + it % t.ni;
-        // Query columns visible to this key row: [lo, hi) in this warpgroup's 32-column frame.
-        const int hi_tile = min(kTile, p.T - qt * kTile);
-        const bool diag = p.causal && qt == t.tile;
-        const int lo = (diag ? row : 0) - wg * 32;
-        const int hi = hi_tile - wg * 32;
-        ok = tile(it, diag || hi_tile < kTile, lo, hi);
-      }
-      if (ok) ok = warp_wait(&bars.fin, 0, ctx, 21);
-      if (ok) {
-        tc_fence_after();
-        const bool valid = k_idx < p.T;
-        const size_t off = ((static_cast<size_t>(t.b) * p.T + (valid ? k_idx : 0)) * p.Hkv + t.kvh) * D;
-        // warpgroups 0, 1: dV halves; 2, 3: dK halves
-        const int part = wg & 1;
-        if (wg < 2)
-          store_row_bf16<D / 2>(tmem + lane_base + Cfg::kKvColDV + part * (D / 2),
-                                reinterpret_cast<__nv_bfloat16*>(p.dv) + off + part * (D / 2), 1.f, valid);
-        else
-          store_row_bf16<D / 2>(tmem + lane_base + Cfg::kKvColDK + part * (D / 2),
-                                reinterpret_cast<__nv_bfloat16*>(p.dk) + off + part * (D / 2), p.scale, valid);
-      }
-    } else {
-      const int q_idx = t.tile * kTile + row;
-      const bool valid = q_idx < p.T;
-      const bool tile_ragged = (t.tile + 1) * kTile > p.T;
-      for (int j = 0; j < n_it && ok; ++j) {
-        // Key columns visible to this query row: [0, lim) in this warpgroup's 32-column frame.
-        const bool diag = p.causal && j == t.tile;
-        const bool kv_ragged = !p.causal && (j + 1) * kTile > p.T;
-        int lim_tile = kTile;
-        if (diag) lim_tile = row + 1;
-        if (kv_ragged) lim_tile = p.T - j * kTile;
-        const int lim = (valid ? lim_tile : 0) - wg * 32;
-        ok = tile(j, diag || kv_ragged || tile_ragged, 0, lim);
-      }
-      if (ok) ok = warp_wait(&bars.fin, 0, ctx, 21);
-      if (ok) {
-        tc_fence_after();
-        const size_t off = ((static_cast<size_t>(t.b) * p.T + (valid ? q_idx : 0)) * p.Hq + t.h) * D;
-        store_row_bf16<D / 4>(tmem + lane_base + Cfg::kDqColAcc + wg * (D / 4),
-                              reinterpret_cast<__nv_bfloat16*>(p.dq) + off + wg * (D / 4), p.scale, valid);
-      }
+    for (int s2 = 0; s2 < NV; ++s2) {
+      const int uses = q_used / NV + (s2 < q_used % NV ? 1 : 0);
+      if (uses > 0) mbar_wait_drain(&bars.v_full[s2], (uses - 1) & 1, p.budget_ns);
     }
   }
+}
+
+// ============================================================================ MMA issuers
+// All 32 lanes of an issuing warp run its loop; the elected lane (always lane 0
+// of the converged warp) issues every MMA and commit, so commits track its MMAs.
+template <int D>
+struct MmaCtx {
+  using Cfg = MainCfg<D>;
+  static constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: N = 128
+  static constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);    // gradients: N = D, B MN-major
+  static constexpr uint32_t idesc_bd = idesc_bf16_f32(128, 128, 0, 1);
+  static constexpr uint32_t kTileD = Cfg::kTileBytes >> 4;  // descriptor units (16 bytes)
+  // Per-stage steps of the dK/dV descriptors. With the shared zero tile, Q_s
+  // moves up and dO_s down by one tile per stage and the block-diagonal LBO
+  // (bits 16-29) grows by one tile; otherwise every operand moves by a stage.
+  static constexpr int64_t kStQ = Cfg::kBlockDiag ? (int64_t)kTileD : (int64_t)(Cfg::kStageBytes >> 4);
+  static constexpr int64_t kStDO = Cfg::kBlockDiag ? -(int64_t)kTileD : kStQ;
+  static constexpr int64_t kStX = Cfg::kBlockDiag ? (int64_t)((2 * Cfg::kAuxBytes) >> 4) : kStQ;
+  static constexpr int64_t kStG1 = Cfg::kBlockDiag ? -(int64_t)kTileD + ((int64_t)kTileD << 16) : kStQ;
+  static constexpr int64_t kStG2 = Cfg::kBlockDiag ? ((int64_t)kTileD << 16) : kStQ;
+  uint32_t tmem;
+  // dK/dV descriptors (fixed buffer 0, stage 0)
+  uint64_t kvA_S, kvA_P, kvB_S, kvB_P, kvG1, kvG2, kvXB_S, kvXB_P;
+  // dQ descriptors (fixed buffer 0, ring slot 0)
+  uint64_t qA_S, qA_P, qB_S, qB_P, qG1, qXA_S, qXA_P;
+  uint64_t ones;
+
+  __device__ __forceinline__ void init(uint8_t* smem, uint32_t tm) {
+    tmem = tm;
+    const uint32_t b = smem_u32(smem);
+    ones = sdesc_noswz(b + Cfg::kOffOnes, 128, 256);
+    kvA_S = sdesc_sw128(b + Cfg::kKvOffK, 16, 1024);  // K
+    kvA_P = sdesc_sw128(b + Cfg::kKvOffV, 16, 1024);  // V
+    kvB_S = sdesc_sw128(b + Cfg::st_q(0), 16, 1024);   // Q  (K-major)
+    kvB_P = sdesc_sw128(b + Cfg::st_do(0), 16, 1024);  // dO (K-major)
+    if (Cfg::kBlockDiag) {
+      kvG1 = sdesc_sw128(b + Cfg::st_do(0), Cfg::kTileBytes, 1024);  // [dO_0 | 0] (MN-major, N = 128)
+      kvG2 = sdesc_sw128(b + Cfg::kKvOffZ, Cfg::kTileBytes, 1024);   // [0 | Q_0]
+    } else {
+      kvG1 = sdesc_sw128(b + Cfg::st_do(0), kHalfTileBytes, 1024);  // dO (MN-major) for dV
+      kvG2 = sdesc_sw128(b + Cfg::st_q(0), kHalfTileBytes, 1024);   // Q  (MN-major) for dK
+    }
+    kvXB_S = sdesc_noswz(b + Cfg::st_qx(0), 128, 256);  // ONES x QX^T -> -LSE2/c
+    kvXB_P = sdesc_noswz(b + Cfg::st_dx(0), 128, 256);  // ONES x DX^T -> -D
+    qA_S = sdesc_sw128(b + Cfg::kDqOffQ, 16, 1024);             // Q
+    qA_P = sdesc_sw128(b + Cfg::kDqOffDO, 16, 1024);            // dO
+    qB_S = sdesc_sw128(b + Cfg::kDqOffK, 16, 1024);             // K slot 0 (K-major)
+    qB_P = sdesc_sw128(b + Cfg::kDqOffV, 16, 1024);             // V slot 0 (K-major)
+    qG1 = sdesc_sw128(b + Cfg::kDqOffK, kHalfTileBytes, 1024);  // K slot 0 (MN-major) for dQ
+    qXA_S = sdesc_noswz(b + Cfg::kDqOffQX, 128, 256);           // QX x ONES^T -> -LSE2/c
+    qXA_P = sdesc_noswz(b + Cfg::kDqOffDX, 128, 256);           // DX x ONES^T -> -D
+  }
+  // S = A_S B_S^T + aux into columns [0,128); f: fixed buffer, bslot: ring slot of B.
+  template <bool DKV>
+  __device__ __forceinline__ void s_mmas(int f, int bslot) const {
+    const uint32_t dst = tmem + Cfg::kColS;
+    if (DKV) {
+      const uint64_t a = kvA_S + f * (Cfg::kKvFixBytes >> 4);
+      const uint64_t b0 = kvB_S + bslot * kStQ;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) mma_ss(dst, a + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+      mma_ss(dst, ones, kvXB_S + bslot * kStX, idesc_s, 1u);
+    } else {
+      const uint64_t fo = f * (Cfg::kDqFixBytes >> 4);
+      const uint64_t b0 = qB_S + bslot * kTileD;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss(dst, qA_S + fo + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+      mma_ss(dst, qXA_S + fo, ones, idesc_s, 1u);
+    }
+  }
+  template <bool DKV>
+  __device__ __forceinline__ void dp_mmas(int f, int bslot) const {
+    const uint32_t dst = tmem + Cfg::kColDP;
+    if (DKV) {
+      const uint64_t a = kvA_P + f * (Cfg::kKvFixBytes >> 4);
+      const uint64_t b0 = kvB_P + bslot * kStDO;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) mma_ss(dst, a + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+      mma_ss(dst, ones, kvXB_P + bslot * kStX, idesc_s, 1u);
+    } else {
+      const uint64_t fo = f * (Cfg::kDqFixBytes >> 4);
+      const uint64_t b0 = qB_P + bslot * kTileD;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss(dst, qA_P + fo + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+      mma_ss(dst, qXA_P + fo, ones, idesc_s, 1u);
+    }
+  }
+  // Gradient MMAs of one tile; `first` starts the task's accumulators.
+  template <bool DKV>
+  __device__ __forceinline__ void grad_mmas(int bslot, bool first) const {
+    if (DKV) {
+      const uint32_t tP = tmem + Cfg::kKvColP, tDS = tmem + Cfg::kKvColDS;
+      const uint64_t g1 = kvG1 + bslot * kStG1, g2 = kvG2 + bslot * kStG2;
+      if (Cfg::kBlockDiag) {
+        // [dV | dK] (128 columns) += [P^T | dS^T] x blockdiag(dO, Q): 16 N = 128 steps
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + Cfg::kKvColDV, tP + kk * 8, g1 + kk * 128, idesc_bd, (!first || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) mma_ts(tmem + Cfg::kKvColDV, tDS + kk * 8, g2 + kk * 128, idesc_bd, 1u);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
+          mma_ts(tmem + Cfg::kKvColDV, tP + kk * 8, g1 + kk * 128, idesc_g, acc);
+          mma_ts(tmem + Cfg::kKvColDK, tDS + kk * 8, g2 + kk * 128, idesc_g, acc);
+        }
+      }
+    } else {
+      const uint32_t tDS = tmem + Cfg::kDqColDS;
+      const uint64_t g1 = qG1 + bslot * kTileD;
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_ts(tmem + Cfg::kDqColAcc, tDS + kk * 8, g1 + kk * 128, idesc_g, (!first || kk > 0) ? 1u : 0u);
+    }
+  }
+};
+
+__device__ __forceinline__ void commit_one(uint64_t* bar) {
+  if (elect_one()) mma_commit(bar);
+  __syncwarp();
+}
+
+// Position in an operand ring of N slots: slot and phase parity of the next use.
+template <int N>
+struct RingPos {
+  int slot, phase;
+  __device__ __forceinline__ explicit RingPos(int used) : slot(used % N), phase((used / N) & 1) {}
+  __device__ __forceinline__ void next() {
+    if (++slot == N) {
+      slot = 0;
+      phase ^= 1;
+    }
+  }
+};
+
+// Warp 1, one task: S and dP of every tile (only dP of dK/dV tiles at d = 128,
+// where the S MMA must follow the gradient MMAs of the previous tile and warp 18
+// issues it). sdp_full and fixed_free expect two arrivals per phase: warp 1 gives
+// both when it issued both S and dP, otherwise one each with warp 18.
+template <int D, bool DKV>
+__device__ __forceinline__ bool sdp_task(const MmaCtx<D>& m, MainBars& bars, const WaitCtx& ctx, int n_it, int f,
+                                         int& G, int used, bool& issued) {
+  using Cfg = MainCfg<D>;
+  constexpr bool s_too = !DKV || Cfg::kKvSepPdS;  // this warp issues S as well
+  RingPos<DKV ? Cfg::kKvStages : Cfg::kDqKStages> rb(used);
+  RingPos<Cfg::kDqVStages> rv(used);
+  bool ok = true;
+  for (int it = 0; it < n_it && ok; ++it, ++G, rb.next(), rv.next()) {
+    // S(G), dP(G) as soon as the compute warps hold S(G-1), dP(G-1). The K (or
+    // Q/dO stage) operand is waited for first; in dQ tasks V only before dP, so
+    // a late V tile (its ring is refilled only when dP(G-1) completes) does not
+    // hold up S.
+    ok = warp_wait(DKV ? &bars.kv_full[rb.slot] : &bars.k_full[rb.slot], rb.phase, ctx, 11);
+    if (ok && G > 0) ok = warp_wait(&bars.sdp_free, (G - 1) & 1, ctx, 14);
+    if (!ok) break;
+    tc_fence_after();
+    if (elect_one()) {
+      if (s_too) {
+        m.template s_mmas<DKV>(f, rb.slot);
+        mma_commit(&bars.sdp_full);
+      }
+      if (DKV) {
+        m.template dp_mmas<DKV>(f, rb.slot);
+        mma_commit(&bars.sdp_full);
+      }
+    }
+    __syncwarp();
+    if (!DKV) {
+      ok = warp_wait(&bars.v_full[rv.slot], rv.phase, ctx, 13);
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+        m.template dp_mmas<DKV>(f, rv.slot);
+        mma_commit(&bars.v_empty[rv.slot]);
+        mma_commit(&bars.sdp_full);
+      }
+      __syncwarp();
+    }
+    issued = true;
+  }
+  if (!ok) return false;
+  // every S/dP MMA of this warp for the task is issued: the fixed operands are
+  // free once they complete
+  if (elect_one()) {
+    mma_commit(&bars.fixed_free[f]);
+    if (s_too) mma_commit(&bars.fixed_free[f]);
+  }
+  __syncwarp();
+  return true;
+}
+
+template <int D>
+__device__ __forceinline__ void sdp_issuer_role(const BwdParams& p, uint8_t* smem, MainBars& bars,
+                                                const volatile int* slot, uint32_t tmem, const WaitCtx& ctx,
+                                                int lane) {
+  using Cfg = MainCfg<D>;
+  MmaCtx<D> m;
+  m.init(smem, tmem);
+  int n = 0, G = 0, kv_used = 0, q_used = 0;
+  bool ok = true, issued = false;
+  for (;; ++n) {
+    const int id = recv_task(bars, slot, n, ctx, lane, ok);
+    if (!ok || id < 0) break;
+    const TaskInfo t = decode_task(p, id);
+    const int f = n % Cfg::kNF;
+    ok = warp_wait(&bars.fixed_full[f], (n / Cfg::kNF) & 1, ctx, 10);
+    if (!ok) break;
+    tc_fence_after();
+    if (t.dkv) {
+      ok = sdp_task<D, true>(m, bars, ctx, t.n_it, f, G, kv_used, issued);
+      kv_used += t.n_it;
+    } else {
+      ok = sdp_task<D, false>(m, bars, ctx, t.n_it, f, G, q_used, issued);
+      q_used += t.n_it;
+    }
+    if (!ok) break;
+  }
+  if (!ok && issued) {
+    commit_one(&bars.drain);
+    mbar_wait_drain(&bars.drain, 0, p.budget_ns);
+  }
+}
+
+// Warp 18, one task: the gradient MMAs of every tile, and at d = 128 the S MMAs
+// of dK/dV tiles, issued right after the gradient MMAs of the previous tile that
+// read P and dS from the same TMEM columns. Steps it = 0..n_it: gradient MMAs of
+// tile it-1, then (S here) S of tile it.
+template <int D, bool DKV>
+__device__ __forceinline__ bool grad_task(const MmaCtx<D>& m, MainBars& bars, const WaitCtx& ctx, int n_it, int f,
+                                          int n, int G, int used, bool& issued) {
+  using Cfg = MainCfg<D>;
+  constexpr bool s_here = DKV && !Cfg::kKvSepPdS;
+  RingPos<DKV ? Cfg::kKvStages : Cfg::kDqKStages> rg(used);  // stage of tile it-1 (gradient operands)
+  RingPos<Cfg::kKvStages> rs(used);                          // stage of tile it (S operands)
+  bool ok = true;
+  if (s_here) {
+    ok = warp_wait(&bars.fixed_full[f], (n / Cfg::kNF) & 1, ctx, 17);
+    if (!ok) return false;
+  }
+  for (int it = 0; it <= n_it && ok; ++it) {
+    if (it > 0) {
+      const int g = G + it - 1;
+      ok = warp_wait(&bars.pds_full, g & 1, ctx, 12);
+      if (ok && it == 1 && n > 0) ok = warp_wait(&bars.acc_free, (n - 1) & 1, ctx, 15);
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+        m.template grad_mmas<DKV>(rg.slot, it == 1);
+        mma_commit(&bars.pds_free);
+        mma_commit(DKV ? &bars.kv_empty[rg.slot] : &bars.k_empty[rg.slot]);
+        if (it == n_it) mma_commit(&bars.acc_full);
+      }
+      __syncwarp();
+      issued = true;
+      rg.next();
+    }
+    if (ok && s_here && it < n_it) {
+      // S(it) overwrites the columns the gradient MMAs above read: same thread, in order
+      ok = warp_wait(&bars.kv_full[rs.slot], rs.phase, ctx, 18);
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+        m.template s_mmas<true>(f, rs.slot);
+        mma_commit(&bars.sdp_full);
+        if (it + 1 == n_it) mma_commit(&bars.fixed_free[f]);
+      }
+      __syncwarp();
+      issued = true;
+      rs.next();
+    }
+  }
+  return ok;
+}
+
+template <int D>
+__device__ __forceinline__ void grad_issuer_role(const BwdParams& p, uint8_t* smem, MainBars& bars,
+                                                 const volatile int* slot, uint32_t tmem, const WaitCtx& ctx,
+                                                 int lane) {
+  using Cfg = MainCfg<D>;
+  MmaCtx<D> m;
+  m.init(smem, tmem);
+  int n = 0, G = 0, kv_used = 0, q_used = 0;
+  bool ok = true, issued = false;
+  for (;; ++n) {
+    const int id = recv_task(bars, slot, n, ctx, lane, ok);
+    if (!ok || id < 0) break;
+    const TaskInfo t = decode_task(p, id);
+    const int f = n % Cfg::kNF;
+    if (t.dkv) {
+      ok = grad_task<D, true>(m, bars, ctx, t.n_it, f, n, G, kv_used, issued);
+      kv_used += t.n_it;
+    } else {
+      ok = grad_task<D, false>(m, bars, ctx, t.n_it, f, n, G, q_used, issued);
+      q_used += t.n_it;
+    }
+    if (!ok) break;
+    G += t.n_it;
+  }
+  if (!ok && issued) {
+    commit_one(&bars.drain2);
+    mbar_wait_drain(&bars.drain2, 0, p.budget_ns);
+  }
+}
+
+// ============================================================================ compute warpgroups
+// Score tiles [it0, it1) of task t (global index of tile 0: G0).
+template <int D, bool DKV>
+__device__ __forceinline__ bool compute_tiles(const BwdParams& p, MainBars& bars, uint32_t tmem, const WaitCtx& ctx,
+                                              const TaskInfo& t, int G0, int it0, int it1, int warp, int lane) {
+  using Cfg = MainCfg<D>;
+  constexpr bool kSep = DKV ? Cfg::kKvSepPdS : true;
+  constexpr uint32_t colP = DKV ? Cfg::kKvColP : 0;
+  constexpr uint32_t colDS = DKV ? Cfg::kKvColDS : Cfg::kDqColDS;
+  const int wg = (warp - 2) >> 2;  // 0..3: score columns [wg*32, wg*32+32)
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t tS = tmem + lane_base + Cfg::kColS + wg * 32;
+  const uint32_t tDP = tmem + lane_base + Cfg::kColDP + wg * 32;
+  const uint32_t tP = tmem + lane_base + colP + wg * 16;
+  const uint32_t tDS = tmem + lane_base + colDS + wg * 16;
+  const float sl2 = p.scale_log2;
+  // One tile: S, dP -> registers -> sdp_free; P, dS -> TMEM -> pds_full.
+  auto tile = [&](int g, bool masked, int lo, int hi) -> bool {
+    if (!warp_wait(&bars.sdp_full, g & 1, ctx, 20)) return false;
+    tc_fence_after();
+    uint32_t s[32], dp[32];
+    tmem_ld32(tS, s);
+    tmem_ld32(tDP, dp);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(&bars.sdp_free);
+    uint32_t pk[16], dk[16];
+    if (masked)
+      score_chunk<DKV, true>(s, dp, sl2, lo, hi, pk, dk);
+    else
+      score_chunk<DKV, false>(s, dp, sl2, lo, hi, pk, dk);
+    // The P/dS region must be free: read by the gradient MMAs of g-1 (separate
+    // region), or S(g) read by every warpgroup (region inside S; the gradient
+    // MMAs of g-1 are complete there, since S(g) was issued after them by the
+    // same thread and has completed).
+    if (kSep) {
+      if (g > 0 && !warp_wait(&bars.pds_free, (g - 1) & 1, ctx, 22)) return false;
+    } else {
+      if (!warp_wait(&bars.sdp_free, g & 1, ctx, 23)) return false;
+    }
+    tc_fence_after();
+    if (DKV) tmem_st16(tP, pk);
+    tmem_st16(tDS, dk);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&bars.pds_full);
+    return true;
+  };
+  bool ok = true;
+  if (DKV) {
+    for (int it = it0; it < it1 && ok; ++it) {
+      const int qt = t.i0 + it % t.ni;
+      // Query columns visible to this key row: [lo, hi) in this warpgroup's 32-column frame.
+      const int hi_tile = min(kTile, p.T - qt * kTile);
+      const bool diag = p.causal && qt == t.tile;
+      const int lo = (diag ? row : 0) - wg * 32;
+      const int hi = hi_tile - wg * 32;
+      ok = tile(G0 + it, diag || hi_tile < kTile, lo, hi);
+    }
+  } else {
+    const int q_idx = t.tile * kTile + row;
+    const bool valid = q_idx < p.T;
+    const bool tile_ragged = (t.tile + 1) * kTile > p.T;
+    for (int j = it0; j < it1 && ok; ++j) {
+      // Key columns visible to this query row: [0, lim) in this warpgroup's 32-column frame.
+      const bool diag = p.causal && j == t.tile;
+      const bool kv_ragged = !p.causal && (j + 1) * kTile > p.T;
+      int lim_tile = kTile;
+      if (diag) lim_tile = row + 1;
+      if (kv_ragged) lim_tile = p.T - j * kTile;
+      const int lim = (valid ? lim_tile : 0) - wg * 32;
+      ok = tile(G0 + j, diag || kv_ragged || tile_ragged, 0, lim);
+    }
+  }
+  return ok;
+}
+
+// Epilogue of task t (the n-th of this CTA): accumulators -> registers, released
+// to the next task's gradient MMAs, then bf16 to memory.
+template <int D, bool DKV>
+__device__ __forceinline__ bool compute_epilogue(const BwdParams& p, MainBars& bars, uint32_t tmem,
+                                                 const WaitCtx& ctx, const TaskInfo& t, int n, int warp, int lane) {
+  using Cfg = MainCfg<D>;
+  const int wg = (warp - 2) >> 2;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+  if (!warp_wait(&bars.acc_full, n & 1, ctx, 21)) return false;
+  tc_fence_after();
+  if (DKV) {
+    constexpr int NC = D / 2;  // warpgroups 0, 1: dV halves; 2, 3: dK halves
+    const int part = wg & 1;
+    uint32_t r[NC];
+    load_acc<NC>(tmem + lane_base + (wg < 2 ? Cfg::kKvColDV : Cfg::kKvColDK) + part * NC, r);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(&bars.acc_free);
+    const int k_idx = t.tile * kTile + row;
+    if (k_idx < p.T) {
+      const size_t off = ((static_cast<size_t>(t.b) * p.T + k_idx) * p.Hkv + t.kvh) * D + part * NC;
+      store_acc_bf16<NC>(r, reinterpret_cast<__nv_bfloat16*>(wg < 2 ? p.dv : p.dk) + off, wg < 2 ? 1.f : p.scale);
+    }
+  } else {
+    constexpr int NC = D / 4;
+    uint32_t r[NC];
+    load_acc<NC>(tmem + lane_base + Cfg::kDqColAcc + wg * NC, r);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(&bars.acc_free);
+    const int q_idx = t.tile * kTile + row;
+    if (q_idx < p.T) {
+      const size_t off = ((static_cast<size_t>(t.b) * p.T + q_idx) * p.Hq + t.h) * D + wg * NC;
+      store_acc_bf16<NC>(r, reinterpret_cast<__nv_bfloat16*>(p.dq) + off, p.scale);
+    }
+  }
+  return true;
 }
 
 template <int D>
@@ -730,28 +977,37 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
   __shared__ MainBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  __shared__ volatile int task_slot[2];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_dkv = p.n_dkv_tasks;
-  const bool is_dkv = static_cast<int>(blockIdx.x) < n_dkv;
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
-    mbar_init(&bars.fixed, 2);  // TMA bytes + the producer warp's aux operands
-    for (int s = 0; s < 3; ++s) {
-      mbar_init(&bars.full[s], is_dkv ? 2 : 1);  // dK/dV stages also carry aux operands
-      mbar_init(&bars.empty[s], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.task_full[s], 1);
+      mbar_init(&bars.task_empty[s], kTaskConsumers);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars.vfull[s], 1);
-      mbar_init(&bars.vempty[s], 1);
+      mbar_init(&bars.fixed_full[s], 2);  // TMA bytes + the producer warp's own operands
+      mbar_init(&bars.fixed_free[s], 2);  // one commit from each MMA issuer
     }
-    mbar_init(&bars.sdp_full, 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&bars.kv_full[s], 2);  // TMA bytes + the producer warp's aux operands
+      mbar_init(&bars.kv_empty[s], 1);
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
+    }
+    mbar_init(&bars.sdp_full, 2);  // one commit from each MMA issuer (or two from warp 1)
     mbar_init(&bars.sdp_free, kComputeThreads);
     mbar_init(&bars.pds_full, kComputeThreads);
     mbar_init(&bars.pds_free, 1);
-    mbar_init(&bars.fin, 1);
+    mbar_init(&bars.acc_full, 1);
+    mbar_init(&bars.acc_free, kComputeThreads);
     mbar_init(&bars.drain, 1);
     mbar_init(&bars.drain2, 1);
     abort_sh = 0;
@@ -768,33 +1024,47 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
   const WaitCtx ctx{&abort_sh, p.status, p.budget_ns, kKidBwdMain};
   pdl_wait_previous();  // the workspace is written by the preprocess kernel
 
-  TaskInfo t;
-  t.h = 0;
-  t.i0 = 0;
-  t.ni = 1;
-  if (is_dkv) {
-    const int nbk = p.B * p.Hkv;
-    t.tile = static_cast<int>(blockIdx.x) / nbk;
-    const int bk = static_cast<int>(blockIdx.x) % nbk;
-    t.b = bk / p.Hkv;
-    t.kvh = bk % p.Hkv;
-    t.i0 = p.causal ? t.tile : 0;
-    t.ni = p.nT - t.i0;
-    t.n_it = p.G * t.ni;
+  if (warp == 0) {
+    producer_role<D>(p, smem, bars, task_slot, ctx, lane);
+  } else if (warp == 1) {
+    sdp_issuer_role<D>(p, smem, bars, task_slot, tmem, ctx, lane);
+  } else if (warp == kGradWarp) {
+    grad_issuer_role<D>(p, smem, bars, task_slot, tmem, ctx, lane);
   } else {
-    const int q = static_cast<int>(blockIdx.x) - n_dkv;
-    const int nbh = p.B * p.Hq;
-    t.tile = p.nT - 1 - q / nbh;
-    const int bh = q % nbh;
-    t.b = bh / p.Hq;
-    t.h = bh % p.Hq;
-    t.kvh = t.h / p.G;
-    t.n_it = p.causal ? t.tile + 1 : p.nT;
+    // With one fixed buffer (d = 128) each task's epilogue runs after the next
+    // task's first tile, so its wait for the last gradient MMAs overlaps the next
+    // task's first score MMAs; at a change of kind it runs first (the dQ dS
+    // columns hold dV of dK/dV tasks). With two fixed buffers the next task's
+    // operands are already loaded and the epilogue simply runs first.
+    int n = 0, G = 0, prev_id = -1;  // the previous task is decoded again for its epilogue (registers)
+    bool ok = true;
+    auto epilogue = [&](int pid, int tn) {
+      const TaskInfo t = decode_task(p, pid);
+      return t.dkv ? compute_epilogue<D, true>(p, bars, tmem, ctx, t, tn, warp, lane)
+                   : compute_epilogue<D, false>(p, bars, tmem, ctx, t, tn, warp, lane);
+    };
+    auto tiles = [&](const TaskInfo& t, int i0, int i1) {
+      return t.dkv ? compute_tiles<D, true>(p, bars, tmem, ctx, t, G, i0, i1, warp, lane)
+                   : compute_tiles<D, false>(p, bars, tmem, ctx, t, G, i0, i1, warp, lane);
+    };
+    for (;; ++n) {
+      const int id = recv_task(bars, task_slot, n, ctx, lane, ok);
+      if (!ok) break;
+      if (id < 0) {
+        if (prev_id >= 0) ok = epilogue(prev_id, n - 1);
+        break;
+      }
+      const TaskInfo t = decode_task(p, id);
+      const bool early = prev_id >= 0 && (MainCfg<D>::kNF > 1 || (prev_id < p.n_dkv_tasks) != (t.dkv != 0));
+      if (early) ok = epilogue(prev_id, n - 1);
+      if (ok) ok = tiles(t, 0, 1);
+      if (ok && prev_id >= 0 && !early) ok = epilogue(prev_id, n - 1);
+      if (ok) ok = tiles(t, 1, t.n_it);
+      if (!ok) break;
+      prev_id = id;
+      G += t.n_it;
+    }
   }
-  if (is_dkv)
-    run_task<D, true>(p, smem, bars, tmem, ctx, t, warp, lane);
-  else
-    run_task<D, false>(p, smem, bars, tmem, ctx, t, warp, lane);
 
   tc_fence_before();
   __syncthreads();
@@ -803,9 +1073,19 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
     __syncwarp();
     tmem_dealloc(tmem, kBwdTmemCols);
   }
+  if (threadIdx.x == 0) {
+    // The last CTA to finish (every CTA has taken its last task by then) leaves
+    // the task counters at zero for the next launch.
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(p.sched, 0u);
+      atomicExch(p.sched + 1, 0u);
+    }
+  }
 }
 
 int g_attr_done[64][4] = {};
+int g_sm_count[64] = {};
 
 template <typename K>
 cudaError_t ensure_smem_attr(K kernel, int smem, int slot) {
@@ -817,6 +1097,20 @@ cudaError_t ensure_smem_attr(K kernel, int smem, int slot) {
     if (e != cudaSuccess) return e;
     g_attr_done[dev][slot] = 1;
   }
+  return cudaSuccess;
+}
+
+cudaError_t sm_count(int* n) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && g_sm_count[dev] > 0) {
+    *n = g_sm_count[dev];
+    return cudaSuccess;
+  }
+  e = cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) g_sm_count[dev] = *n;
   return cudaSuccess;
 }
 
@@ -834,9 +1128,12 @@ cudaError_t launch_bwd_pre(const BwdPreParams& p, int d, cudaStream_t stream) {
 }
 
 cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream) {
-  const unsigned grid = static_cast<unsigned>(p.n_dkv_tasks + p.n_dq_tasks);
-  if (grid == 0) return cudaSuccess;
-  cudaError_t e;
+  const int n_tasks = p.n_dkv_tasks + p.n_dq_tasks;
+  if (n_tasks == 0) return cudaSuccess;
+  int sms = 0;
+  cudaError_t e = sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(n_tasks < sms ? n_tasks : sms);
   if (d == 64) {
     if ((e = ensure_smem_attr(bwd_main_kernel<64>, MainCfg<64>::kSmemBytes, 0)) != cudaSuccess) return e;
     e = launch_pdl(bwd_main_kernel<64>, grid, kMainThreads, MainCfg<64>::kSmemBytes, stream, p);

@@ -45,10 +45,11 @@ struct BwdPreParams {
   const float* lse;
   float* Dvec;   // [B,Hq,Tpad]
   float* lse2;   // [B,Hq,Tpad]
+  unsigned* sched;  // [2] task counters of the dQ / dK/dV launch, zeroed here
   int B, T, Hq, Tpad;
 };
 
-// Backward dQ (one CTA per query tile) and dK/dV (one CTA per key tile).
+// Backward dQ (one task per query tile) and dK/dV (one task per key tile), one persistent launch.
 struct BwdParams {
   CUtensorMap tmap_q;
   CUtensorMap tmap_k;
@@ -56,13 +57,14 @@ struct BwdParams {
   CUtensorMap tmap_do;
   const float* Dvec;   // [B,Hq,Tpad]
   const float* lse2;   // [B,Hq,Tpad]
+  unsigned* sched;     // [2] next task, finished CTAs; zero on entry, left zero on exit
   void* dq;            // [B,T,Hq,d]
   void* dk;            // [B,T,Hkv,d]
   void* dv;            // [B,T,Hkv,d]
   int B, T, Hq, Hkv, G, nT, Tpad;
   int causal;
-  int n_dkv_tasks;     // blocks [0, n_dkv_tasks) compute dK/dV (0 = none)
-  int n_dq_tasks;      // the next n_dq_tasks blocks compute dQ (0 = none)
+  int n_dkv_tasks;     // tasks [0, n_dkv_tasks) compute dK/dV (0 = none)
+  int n_dq_tasks;      // the next n_dq_tasks tasks compute dQ (0 = none)
   float scale;         // 1/sqrt(d)
   float scale_log2;    // scale * log2(e)
   DevStatusWord* status;

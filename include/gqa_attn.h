@@ -62,16 +62,17 @@ gqa_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, floa
 
 /*
  * Bytes of scratch the backward needs: two fp32 arrays [B, Hq, T rounded up
- * to 128] (D_i = rowsum(dO * O) and the LSE in log2 units). The caller
- * allocates it; nothing in it needs to be initialised or preserved.
+ * to 128] (D_i = rowsum(dO * O) and the LSE in log2 units) followed by 256
+ * bytes of task counters. The caller allocates it; nothing in it needs to be
+ * initialised (the preprocess writes all of it) or preserved.
  */
 size_t attn_bwd_workspace_bytes(int B, int T, int Hq);
 
 /*
  * Backward pass of L = sum(O * dO) ("A transformer in PTX", §The same bits
- * every time): a rowsum(dO * O) preprocess, then a dQ kernel per block of
- * queries and a dK/dV kernel per block of keys that loops over the query heads
- * of its kv head in ascending order.
+ * every time): a rowsum(dO * O) preprocess, then dQ tasks (one per block of
+ * queries) and dK/dV tasks (one per block of keys, looping over the query heads
+ * of its kv head in ascending order), run by one persistent launch.
  *   q, k, v, o, lse: as produced/consumed by attn_fwd; dO [B,T,Hq,d] bf16 in;
  *   dq [B,T,Hq,d], dk/dv [B,T,Hkv,d] bf16 out.
  *   workspace: device memory of at least attn_bwd_workspace_bytes(B,T,Hq)
@@ -85,14 +86,17 @@ gqa_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o
 /*
  * The stages of attn_bwd, callable one by one: attn_bwd is exactly
  * attn_bwd_preprocess followed by attn_bwd_dq_dkv on one stream. The dQ and
- * dK/dV passes only read the workspace; attn_bwd_dq_dkv runs both in one
- * launch (heaviest tasks first), attn_bwd_dq and attn_bwd_dkv run one each.
+ * dK/dV passes read D and the LSE from the workspace and take their tasks from
+ * its counters, which the preprocess zeroes and each pass leaves at zero (so
+ * the pointer is declared const although those counters change during the
+ * call); attn_bwd_dq_dkv runs both kinds of task in one launch (heaviest
+ * first), attn_bwd_dq and attn_bwd_dkv one kind each.
  *
  * attn_bwd_preprocess: workspace <- D_i = rowsum(dO_i * O_i) and LSE_i*log2(e),
- *   fp32 [B, Hq, T rounded up to 128] each, rows past T set to 0.
- * attn_bwd_dq:  dq [B,T,Hq,d] <- scale * sum_j dS_ij k_j, one CTA per query tile.
+ *   fp32 [B, Hq, T rounded up to 128] each, rows past T set to 0; counters 0.
+ * attn_bwd_dq:  dq [B,T,Hq,d] <- scale * sum_j dS_ij k_j, one task per query tile.
  * attn_bwd_dkv: dk, dv [B,T,Hkv,d] <- sums over the query heads sharing each kv
- *   head, one CTA per key tile, heads and query tiles in ascending order.
+ *   head, one task per key tile, heads and query tiles in ascending order.
  * Arguments mean what they mean in attn_bwd.
  */
 gqa_status_t attn_bwd_preprocess(const void* o, const float* lse, const void* dO, void* workspace,
@@ -118,7 +122,7 @@ gqa_status_t attn_bwd_dq_dkv(const void* q, const void* k, const void* v, const 
  * GQA_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library holds until the process exits.
  *  - Limit: attn_bwd_workspace_bytes(B, T, Hq) must not exceed
- *    GQA_NOALLOC_SCRATCH_BYTES (B * Hq * roundup(T, 128) <= 1,048,576);
+ *    GQA_NOALLOC_SCRATCH_BYTES (B * Hq * roundup(T, 128) <= 1,048,544);
  *    larger problems get GQA_ERR_INVALID_ARG before anything is launched.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call

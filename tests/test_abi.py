@@ -36,9 +36,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_workspace(lib):
     assert gqa.attn_version() == "0.1.0"
-    # two fp32 arrays [B, Hq, T rounded up to 128]
-    assert gqa.attn_bwd_workspace_bytes(2, 3000, 6) == 2 * 2 * 6 * 3072 * 4
-    assert gqa.attn_bwd_workspace_bytes(1, 128, 1) == 2 * 128 * 4
+    # two fp32 arrays [B, Hq, T rounded up to 128] and 256 bytes of task counters
+    assert gqa.attn_bwd_workspace_bytes(2, 3000, 6) == 2 * 2 * 6 * 3072 * 4 + 256  # two fp32 arrays + task counters
+    assert gqa.attn_bwd_workspace_bytes(1, 128, 1) == 2 * 128 * 4 + 256
     assert gqa.attn_bwd_workspace_bytes(0, 128, 1) == 0
 
 
