@@ -167,32 +167,20 @@ struct MainCfg {
   static constexpr int kDqOffK = kAuxBytes + kNF * kDqFixBytes;
   static constexpr int kDqOffV = kDqOffK + kDqKStages * kTileBytes;
   static constexpr int kDqBytes = kDqOffV + kDqVStages * kTileBytes;
-  // dK/dV task: fixed buffers [K][V], then the Q/dO stage ring. At d = 64 the
-  // gradient MMAs compute [dV | dK] as one N = 128 chain over the block-diagonal
-  // operands [dO_s | 0] (P steps) and [0 | Q_s] (dS steps): one zero tile Z is
-  // shared by all stages, with dO_s = Z - (s+1) tiles and Q_s = Z + (s+1) tiles,
-  // so the LBO of stage s, (s+1) tiles, spans both. At d = 128 a stage is
-  // [Q][dO][QX][DX].
-  static constexpr bool kBlockDiag = (D == 64);
+  // dK/dV task: fixed buffers [K][V], then the ring of stages [Q][dO][QX][DX].
+  // The two gradient chains (dV += P^T dO, dK += dS^T Q) are separate N = D MMAs:
+  // at d = 64 a single N = 128 chain over block-diagonal operands (half of it
+  // multiplying zeros) measured 8-10% slower overall.
   static constexpr int kKvStages = (D == 64) ? 3 : 2;   // Q/dO stages
   static constexpr int kKvFixBytes = 2 * kTileBytes;
   static constexpr int kKvOffK = kAuxBytes;             // buffer 0; buffer f adds f * kKvFixBytes
   static constexpr int kKvOffV = kKvOffK + kTileBytes;
   static constexpr int kKvOffStages = kAuxBytes + kNF * kKvFixBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kAuxBytes;  // d = 128 stage stride
-  static constexpr int kKvOffZ = kKvOffStages + kKvStages * kTileBytes;  // d = 64
-  static constexpr int kKvOffAux = kKvOffStages + (2 * kKvStages + 1) * kTileBytes;  // d = 64: [QX_s][DX_s]
-  static constexpr int kKvBytes =
-      kBlockDiag ? kKvOffAux + kKvStages * 2 * kAuxBytes : kKvOffStages + kKvStages * kStageBytes;
-  __host__ __device__ static constexpr int st_q(int s) {
-    return kBlockDiag ? kKvOffZ + (s + 1) * kTileBytes : kKvOffStages + s * kStageBytes;
-  }
-  __host__ __device__ static constexpr int st_do(int s) {
-    return kBlockDiag ? kKvOffZ - (s + 1) * kTileBytes : kKvOffStages + s * kStageBytes + kTileBytes;
-  }
-  __host__ __device__ static constexpr int st_qx(int s) {
-    return kBlockDiag ? kKvOffAux + s * 2 * kAuxBytes : kKvOffStages + s * kStageBytes + 2 * kTileBytes;
-  }
+  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kAuxBytes;
+  static constexpr int kKvBytes = kKvOffStages + kKvStages * kStageBytes;
+  __host__ __device__ static constexpr int st_q(int s) { return kKvOffStages + s * kStageBytes; }
+  __host__ __device__ static constexpr int st_do(int s) { return st_q(s) + kTileBytes; }
+  __host__ __device__ static constexpr int st_qx(int s) { return st_q(s) + 2 * kTileBytes; }
   __host__ __device__ static constexpr int st_dx(int s) { return st_qx(s) + kAuxBytes; }
   static constexpr int kUsed = (kDqBytes > kKvBytes ? kDqBytes : kKvBytes) + 1024;
   static constexpr int kSmemBytes = kUsed > kOneCtaPerSmSmem ? kUsed : kOneCtaPerSmSmem;
@@ -412,12 +400,6 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
           tma_load_4d(fix + Cfg::kKvOffK + hf * kHalfTileBytes, &p.tmap_k, fbar, hf * 64, t.kvh, t.tile * kTile, t.b);
           tma_load_4d(fix + Cfg::kKvOffV + hf * kHalfTileBytes, &p.tmap_v, fbar, hf * 64, t.kvh, t.tile * kTile, t.b);
         }
-      if (Cfg::kBlockDiag && prev_kind != 1) {
-        // the shared zero tile of the stages (never written by TMA; dK/dV tasks come first)
-        uint4* z = reinterpret_cast<uint4*>(smem + Cfg::kKvOffZ);
-        for (int i = lane; i < Cfg::kTileBytes / 16; i += 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
-        fence_proxy_async_smem();
-      }
       __syncwarp();
       if (lane == 0) mbar_arrive(fbar);
       // -LSE2 and D of the next stage's 128 query rows, 4 per lane, fetched one
@@ -553,16 +535,9 @@ struct MmaCtx {
   using Cfg = MainCfg<D>;
   static constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: N = 128
   static constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);    // gradients: N = D, B MN-major
-  static constexpr uint32_t idesc_bd = idesc_bf16_f32(128, 128, 0, 1);
   static constexpr uint32_t kTileD = Cfg::kTileBytes >> 4;  // descriptor units (16 bytes)
-  // Per-stage steps of the dK/dV descriptors. With the shared zero tile, Q_s
-  // moves up and dO_s down by one tile per stage and the block-diagonal LBO
-  // (bits 16-29) grows by one tile; otherwise every operand moves by a stage.
-  static constexpr int64_t kStQ = Cfg::kBlockDiag ? (int64_t)kTileD : (int64_t)(Cfg::kStageBytes >> 4);
-  static constexpr int64_t kStDO = Cfg::kBlockDiag ? -(int64_t)kTileD : kStQ;
-  static constexpr int64_t kStX = Cfg::kBlockDiag ? (int64_t)((2 * Cfg::kAuxBytes) >> 4) : kStQ;
-  static constexpr int64_t kStG1 = Cfg::kBlockDiag ? -(int64_t)kTileD + ((int64_t)kTileD << 16) : kStQ;
-  static constexpr int64_t kStG2 = Cfg::kBlockDiag ? ((int64_t)kTileD << 16) : kStQ;
+  // every dK/dV stage operand moves by one stage stride
+  static constexpr uint32_t kStQ = Cfg::kStageBytes >> 4, kStDO = kStQ, kStX = kStQ, kStG1 = kStQ, kStG2 = kStQ;
   uint32_t tmem;
   // dK/dV descriptors (fixed buffer 0, stage 0)
   uint64_t kvA_S, kvA_P, kvB_S, kvB_P, kvG1, kvG2, kvXB_S, kvXB_P;
@@ -578,13 +553,8 @@ struct MmaCtx {
     kvA_P = sdesc_sw128(b + Cfg::kKvOffV, 16, 1024);  // V
     kvB_S = sdesc_sw128(b + Cfg::st_q(0), 16, 1024);   // Q  (K-major)
     kvB_P = sdesc_sw128(b + Cfg::st_do(0), 16, 1024);  // dO (K-major)
-    if (Cfg::kBlockDiag) {
-      kvG1 = sdesc_sw128(b + Cfg::st_do(0), Cfg::kTileBytes, 1024);  // [dO_0 | 0] (MN-major, N = 128)
-      kvG2 = sdesc_sw128(b + Cfg::kKvOffZ, Cfg::kTileBytes, 1024);   // [0 | Q_0]
-    } else {
-      kvG1 = sdesc_sw128(b + Cfg::st_do(0), kHalfTileBytes, 1024);  // dO (MN-major) for dV
-      kvG2 = sdesc_sw128(b + Cfg::st_q(0), kHalfTileBytes, 1024);   // Q  (MN-major) for dK
-    }
+    kvG1 = sdesc_sw128(b + Cfg::st_do(0), kHalfTileBytes, 1024);  // dO (MN-major) for dV
+    kvG2 = sdesc_sw128(b + Cfg::st_q(0), kHalfTileBytes, 1024);   // Q  (MN-major) for dK
     kvXB_S = sdesc_noswz(b + Cfg::st_qx(0), 128, 256);  // ONES x QX^T -> -LSE2/c
     kvXB_P = sdesc_noswz(b + Cfg::st_dx(0), 128, 256);  // ONES x DX^T -> -D
     qA_S = sdesc_sw128(b + Cfg::kDqOffQ, 16, 1024);             // Q
@@ -638,20 +608,11 @@ struct MmaCtx {
     if (DKV) {
       const uint32_t tP = tmem + Cfg::kKvColP, tDS = tmem + Cfg::kKvColDS;
       const uint64_t g1 = kvG1 + bslot * kStG1, g2 = kvG2 + bslot * kStG2;
-      if (Cfg::kBlockDiag) {
-        // [dV | dK] (128 columns) += [P^T | dS^T] x blockdiag(dO, Q): 16 N = 128 steps
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + Cfg::kKvColDV, tP + kk * 8, g1 + kk * 128, idesc_bd, (!first || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) mma_ts(tmem + Cfg::kKvColDV, tDS + kk * 8, g2 + kk * 128, idesc_bd, 1u);
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + Cfg::kKvColDV, tP + kk * 8, g1 + kk * 128, idesc_g, acc);
-          mma_ts(tmem + Cfg::kKvColDK, tDS + kk * 8, g2 + kk * 128, idesc_g, acc);
-        }
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
+        mma_ts(tmem + Cfg::kKvColDV, tP + kk * 8, g1 + kk * 128, idesc_g, acc);
+        mma_ts(tmem + Cfg::kKvColDK, tDS + kk * 8, g2 + kk * 128, idesc_g, acc);
       }
     } else {
       const uint32_t tDS = tmem + Cfg::kDqColDS;
