@@ -143,17 +143,21 @@ gqa_status_t check_ptr(const char* fn, const char* name, const void* p) {
   return GQA_OK;
 }
 
-// 4D tiled map over a [B, T, H, d] bf16 tensor: box = 64 (d) x 1 (head) x 128 (rows) x 1 (batch),
-// 128-byte swizzle; rows past T read as zero.
+// 4D tiled map over a [B, T, H, d] bf16 tensor: box = box_c (d) x 1 (head) x box_rows x 1 (batch),
+// swizzled over the box's inner bytes (box_c = 64: 128-byte swizzle, 32: 64-byte, 16: 32-byte);
+// loads read rows past T as zero, stores skip them. The operand loads use 64 x 128 boxes.
 gqa_status_t make_map(const char* fn, const char* name, CUtensorMap* m, const void* ptr, int B, int T, int H,
-                      int d) {
+                      int d, int box_c = 64, int box_rows = kTile) {
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)T * H * d * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
+  cuuint32_t box[4] = {(cuuint32_t)box_c, 1, (cuuint32_t)box_rows, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle swz = box_c == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : box_c == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_32B;
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(GQA_ERR_INVALID_ARG, "%s: cuTensorMapEncodeTiled(%s) failed (%d)", fn, name, (int)r);
   return GQA_OK;
 }
@@ -309,6 +313,14 @@ gqa_status_t bwd_main_impl(const char* fn, int which, const void* q, const void*
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
+  if (d == 64) {
+    // d = 64 epilogues store through TMA, one 32-row box per compute warp: dQ 16
+    // columns of a warpgroup, dK / dV 32 columns.
+    if ((which & 1) && (s = make_map(fn, "dq", &p.tmap_dq, dq, B, T, Hq, d, 16, 32))) return s;
+    if ((which & 2) && ((s = make_map(fn, "dk", &p.tmap_dk, dk, B, T, Hkv, d, 32, 32)) ||
+                        (s = make_map(fn, "dv", &p.tmap_dv, dv, B, T, Hkv, d, 32, 32))))
+      return s;
+  }
   p.n_dkv_tasks = (which & 2) ? B * Hkv * p.nT : 0;
   p.n_dq_tasks = (which & 1) ? B * Hq * p.nT : 0;
   cudaError_t e = launch_bwd_main(p, d, st);

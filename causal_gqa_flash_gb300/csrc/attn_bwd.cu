@@ -182,7 +182,15 @@ struct MainCfg {
   __host__ __device__ static constexpr int st_do(int s) { return st_q(s) + kTileBytes; }
   __host__ __device__ static constexpr int st_qx(int s) { return st_q(s) + 2 * kTileBytes; }
   __host__ __device__ static constexpr int st_dx(int s) { return st_qx(s) + kAuxBytes; }
-  static constexpr int kUsed = (kDqBytes > kKvBytes ? kDqBytes : kKvBytes) + 1024;
+  // d = 64 epilogue: each compute warp stages its 32 rows of bf16 output (dK/dV:
+  // 32 columns, dQ: 16) in a region of its own and stores them with one TMA box.
+  // At d = 128 there is no room for the 64 KB this would take; rows are stored
+  // directly from registers.
+  static constexpr bool kTmaStore = (D == 64);
+  static constexpr int kOutWarpBytes = 2048;
+  static constexpr int kOffOut = ((kDqBytes > kKvBytes ? kDqBytes : kKvBytes) + 1023) / 1024 * 1024;
+  static constexpr int kOutBytes = kTmaStore ? 16 * kOutWarpBytes : 0;
+  static constexpr int kUsed = kOffOut + kOutBytes + 1024;
   static constexpr int kSmemBytes = kUsed > kOneCtaPerSmSmem ? kUsed : kOneCtaPerSmSmem;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   // TMEM columns
@@ -892,8 +900,38 @@ __device__ __forceinline__ bool compute_tiles(const BwdParams& p, MainBars& bars
 
 // Epilogue of task t (the n-th of this CTA): accumulators -> registers, released
 // to the next task's gradient MMAs, then bf16 to memory.
+// d = 64: this warp's 32 rows of NC bf16 columns (NC/8 16-byte chunks a row, 64 or
+// 32 bytes) into its staging region, swizzled as its store map expects (chunk c of
+// row r at c ^ ((r >> 1) & 3) with 64-byte rows, c ^ ((r >> 2) & 1) with 32-byte
+// rows), then one TMA store of the box at column x, row r0. The warp's previous
+// store must have read the region first.
+template <int NC>
+__device__ __forceinline__ void tma_store_rows(const uint32_t (&r)[NC], float scale, uint8_t* stg,
+                                               const CUtensorMap* map, int x, int h, int r0, int b, int T,
+                                               int lane) {
+  constexpr int NCH = NC / 8;
+  static_assert(NCH == 2 || NCH == 4, "row bytes");
+  if (lane == 0) tma_store_wait_read();
+  __syncwarp();
+  const int sw = NCH == 4 ? ((lane >> 1) & 3) : ((lane >> 2) & 1);
+#pragma unroll
+  for (int v = 0; v < NCH; ++v) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = pack_bf16x2(__uint_as_float(r[8 * v + 2 * i]) * scale, __uint_as_float(r[8 * v + 2 * i + 1]) * scale);
+    *reinterpret_cast<uint4*>(stg + lane * (NCH * 16) + ((v ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && r0 < T) {
+    tma_store_4d(map, stg, x, h, r0, b);
+    tma_store_commit();
+  }
+}
+
 template <int D, bool DKV>
-__device__ __forceinline__ bool compute_epilogue(const BwdParams& p, MainBars& bars, uint32_t tmem,
+__device__ __forceinline__ bool compute_epilogue(const BwdParams& p, MainBars& bars, uint32_t tmem, uint8_t* smem,
                                                  const WaitCtx& ctx, const TaskInfo& t, int n, int warp, int lane) {
   using Cfg = MainCfg<D>;
   const int wg = (warp - 2) >> 2;
@@ -910,6 +948,12 @@ __device__ __forceinline__ bool compute_epilogue(const BwdParams& p, MainBars& b
     tmem_wait_ld();
     tc_fence_before();
     mbar_arrive(&bars.acc_free);
+    if constexpr (Cfg::kTmaStore) {
+      tma_store_rows<NC>(r, wg < 2 ? 1.f : p.scale, smem + Cfg::kOffOut + (warp - 2) * Cfg::kOutWarpBytes,
+                         wg < 2 ? &p.tmap_dv : &p.tmap_dk, part * NC, t.kvh, t.tile * kTile + quarter * 32, t.b,
+                         p.T, lane);
+      return true;
+    }
     const int k_idx = t.tile * kTile + row;
     if (k_idx < p.T) {
       const size_t off = ((static_cast<size_t>(t.b) * p.T + k_idx) * p.Hkv + t.kvh) * D + part * NC;
@@ -922,6 +966,11 @@ __device__ __forceinline__ bool compute_epilogue(const BwdParams& p, MainBars& b
     tmem_wait_ld();
     tc_fence_before();
     mbar_arrive(&bars.acc_free);
+    if constexpr (Cfg::kTmaStore) {
+      tma_store_rows<NC>(r, p.scale, smem + Cfg::kOffOut + (warp - 2) * Cfg::kOutWarpBytes, &p.tmap_dq, wg * NC,
+                         t.h, t.tile * kTile + quarter * 32, t.b, p.T, lane);
+      return true;
+    }
     const int q_idx = t.tile * kTile + row;
     if (q_idx < p.T) {
       const size_t off = ((static_cast<size_t>(t.b) * p.T + q_idx) * p.Hq + t.h) * D + wg * NC;
@@ -1001,8 +1050,8 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
     bool ok = true;
     auto epilogue = [&](int pid, int tn) {
       const TaskInfo t = decode_task(p, pid);
-      return t.dkv ? compute_epilogue<D, true>(p, bars, tmem, ctx, t, tn, warp, lane)
-                   : compute_epilogue<D, false>(p, bars, tmem, ctx, t, tn, warp, lane);
+      return t.dkv ? compute_epilogue<D, true>(p, bars, tmem, smem, ctx, t, tn, warp, lane)
+                   : compute_epilogue<D, false>(p, bars, tmem, smem, ctx, t, tn, warp, lane);
     };
     auto tiles = [&](const TaskInfo& t, int i0, int i1) {
       return t.dkv ? compute_tiles<D, true>(p, bars, tmem, ctx, t, G, i0, i1, warp, lane)
@@ -1025,6 +1074,8 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
       prev_id = id;
       G += t.n_it;
     }
+    // the staging regions must stay until the TMA stores have finished
+    if (MainCfg<D>::kTmaStore && lane == 0) tma_store_wait_all();
   }
 
   tc_fence_before();

@@ -55,6 +55,9 @@ struct BwdParams {
   CUtensorMap tmap_k;
   CUtensorMap tmap_v;
   CUtensorMap tmap_do;
+  CUtensorMap tmap_dq;  // d = 64 only: epilogue stores (32-row boxes)
+  CUtensorMap tmap_dk;
+  CUtensorMap tmap_dv;
   const float* Dvec;   // [B,Hq,Tpad]
   const float* lse2;   // [B,Hq,Tpad]
   unsigned* sched;     // [2] next task, finished CTAs; zero on entry, left zero on exit
