@@ -1097,7 +1097,6 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
 }
 
 int g_attr_done[64][4] = {};
-int g_sm_count[64] = {};
 
 template <typename K>
 cudaError_t ensure_smem_attr(K kernel, int smem, int slot) {
@@ -1112,19 +1111,6 @@ cudaError_t ensure_smem_attr(K kernel, int smem, int slot) {
   return cudaSuccess;
 }
 
-cudaError_t sm_count(int* n) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && g_sm_count[dev] > 0) {
-    *n = g_sm_count[dev];
-    return cudaSuccess;
-  }
-  e = cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64) g_sm_count[dev] = *n;
-  return cudaSuccess;
-}
 
 }  // namespace
 

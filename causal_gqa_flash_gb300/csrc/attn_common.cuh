@@ -24,11 +24,12 @@ enum KernelId : unsigned int {
   kKidSelfTest = 9,
 };
 
-// Forward: one CTA per (128-query tile, query head, batch).
+// Forward: work items of one 128-query tile of one (query head, batch).
 struct FwdParams {
   CUtensorMap tmap_q;  // [B,T,Hq,d] bf16, box 64 x 1 x 128 x 1, 128B swizzle
   CUtensorMap tmap_k;  // [B,T,Hkv,d]
   CUtensorMap tmap_v;  // [B,T,Hkv,d]
+  CUtensorMap tmap_o;  // d = 64 only: [B,T,Hq,d], box 64 x 1 x 32 x 1 (epilogue stores)
   void* o;             // [B,T,Hq,d] bf16
   float* lse;          // [B,Hq,T] fp32, natural log
   int B, T, Hq, Hkv, G, nT;
@@ -73,6 +74,22 @@ struct BwdParams {
   DevStatusWord* status;
   unsigned long long budget_ns;
 };
+
+// Number of SMs of the current device (cached per device).
+inline cudaError_t sm_count(int* n) {
+  static int cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+    *n = cache[dev];
+    return cudaSuccess;
+  }
+  e = cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) cache[dev] = *n;
+  return cudaSuccess;
+}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));

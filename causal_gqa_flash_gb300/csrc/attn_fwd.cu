@@ -7,19 +7,27 @@
 // log-sum-exp is saved for the backward.
 //
 // GB300 design (not the page's mma.sync/ldmatrix/cp.async design):
-//  * one CTA = one 128-query tile of one (batch, query head); two CTAs share
-//    an SM so one's softmax overlaps the other's tensor-core work;
-//  * warp 0 issues TMA loads (Q once, a K ring and a V ring, 128B swizzle),
-//    warp 1 issues tcgen05 MMAs (all lanes run the loop, one elected lane
-//    issues) and owns the TMEM allocation, warps 2-5 are the softmax
-//    warpgroup: one thread per query row, which is one TMEM lane, so row max
-//    and row sum need no shuffles;
+//  * work item = one 128-query tile of one (batch, query head), heaviest first;
+//    two CTAs per SM. At d = 64 the launch is persistent: each CTA runs a fixed
+//    list of items in a snake order over the CTAs (CTA c takes items c,
+//    2C-1-c, 2C+c, ...), so the causal cost evens out and the light items fill
+//    the end of every list. At d = 128 each CTA runs one item;
+//  * warp 0 issues TMA loads (Q per item, a K ring and a V ring that run on
+//    across items, 128B swizzle), warp 1 issues tcgen05 MMAs (all lanes run the
+//    loop, one elected lane issues) and owns the TMEM allocation, warps 2-5 are
+//    the softmax warpgroup: one thread per query row, which is one TMEM lane, so
+//    row max and row sum need no shuffles;
 //  * S = Q K^T (SS MMA, fp32 in TMEM columns [0,128)) and O += P V (TS MMA, P
 //    as bf16 pairs from TMEM, V as an MN-major smem operand). At d = 64, P has
 //    columns of its own: the softmax loads the whole S row into registers and
 //    releases S at once, so S(j+1) is computed while P(j) is; at d = 128 (no
 //    TMEM room for two CTAs otherwise) P is written over S's first 64 columns
 //    and S(j+1) follows PV(j);
+//  * item boundaries overlap: the next item's Q is loaded once the last S MMA
+//    of the current one has read Q, its first S is computed while the softmax
+//    warps run the epilogue, and only its first PV waits for the epilogue to
+//    have read O out of TMEM; at d = 64 the epilogue stages O in shared memory
+//    and each softmax warp stores its 32 rows with one TMA box;
 //  * the running max is rescaled lazily: O and l are only rescaled when a
 //    row's max grows by more than 2^8, otherwise p = 2^(s - m_stale) <= 256;
 //  * causal tiles past the diagonal are never visited; only the diagonal tile
@@ -30,6 +38,7 @@ namespace gqa {
 namespace {
 
 constexpr int kFwdThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kFwdCtasPerSm = 2;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0;     // S fp32 [128 x 128]
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -49,7 +58,16 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-  static constexpr int kSmemBytes = kOffV + kVStages * kTileBytes + 1024;  // + alignment slack
+  // d = 64: per softmax warp, 32 rows x 128 bytes of bf16 O for its TMA store
+  // (at d = 128 two CTAs leave no room for it and rows are stored directly).
+  static constexpr bool kTmaStore = (D == 64);
+  // d = 64: persistent CTAs with lists of items; d = 128: one item per CTA.
+  static constexpr bool kPersistent = (D == 64);
+  static constexpr int kMaxRounds = kPersistent ? 0x7fffffff : 1;
+  static_assert(kTmaStore || !kPersistent, "only the staged epilogue releases O for a next item");
+  static constexpr int kOffOut = kOffV + kVStages * kTileBytes;
+  static constexpr int kOutBytes = kTmaStore ? 4 * 32 * 128 : 0;
+  static constexpr int kSmemBytes = kOffOut + kOutBytes + 1024;  // + alignment slack
 };
 
 // Wait with a warp-uniform outcome.
@@ -58,8 +76,30 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
+// Work item of round r for CTA c of C: snake order over the heaviest-first items.
+__device__ __forceinline__ int item_of(int r, unsigned c, unsigned C) {
+  return r * static_cast<int>(C) + ((r & 1) ? static_cast<int>(C - 1 - c) : static_cast<int>(c));
+}
+
+struct FwdItem {
+  int qt, b, h, kvh, n_kv;
+};
+
+__device__ __forceinline__ FwdItem decode_item(const FwdParams& p, int id) {
+  // heaviest query tiles first (causal cost grows with the tile index)
+  const int nbh = p.B * p.Hq;
+  FwdItem it;
+  it.qt = p.nT - 1 - id / nbh;
+  const int bh = id % nbh;
+  it.b = bh / p.Hq;
+  it.h = bh % p.Hq;
+  it.kvh = it.h / p.G;
+  it.n_kv = p.causal ? it.qt + 1 : p.nT;
+  return it;
+}
+
 template <int D>
-__global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using Cfg = FwdCfg<D>;
   constexpr int KS = Cfg::kKStages;
   constexpr int VS = Cfg::kVStages;
@@ -67,28 +107,26 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
   uint8_t* smem = align1024(smem_raw);
   constexpr bool kSepP = Cfg::kSepP;
   constexpr uint32_t kColP = Cfg::kColP, kColO = Cfg::kColO;
-  // bar_s: S(j) in TMEM (MMA commit); bar_sfree: every softmax thread holds S(j)
-  // in registers (d = 64 only); bar_p: P(j) in TMEM; bar_pfree: PV(j) done (d = 64).
-  __shared__ uint64_t bar_q, bar_kf[KS], bar_ke[KS], bar_vf[VS], bar_ve[VS], bar_s, bar_sfree, bar_p, bar_pfree, bar_o,
-      bar_drain;
+  // Per item: bar_q (Q loaded), bar_qfree (its last S MMA is done), bar_o (its
+  // last PV is done), bar_ofree (the softmax holds O in registers). Per tile,
+  // counted over the CTA's items: bar_s (S in TMEM), bar_sfree (every softmax
+  // thread holds S; d = 64), bar_p (P in TMEM), bar_pfree (PV done; d = 64).
+  __shared__ uint64_t bar_q, bar_qfree, bar_kf[KS], bar_ke[KS], bar_vf[VS], bar_ve[VS], bar_s, bar_sfree, bar_p,
+      bar_pfree, bar_o, bar_ofree, bar_drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // Work item: heaviest query tiles first (causal cost grows with the tile index).
-  const int nbh = p.B * p.Hq;
-  const int qt = p.nT - 1 - static_cast<int>(blockIdx.x) / nbh;
-  const int bh = static_cast<int>(blockIdx.x) % nbh;
-  const int b = bh / p.Hq;
-  const int h = bh % p.Hq;
-  const int kvh = h / p.G;
-  const int n_kv = p.causal ? qt + 1 : p.nT;
+  // This CTA's items: item_of(r) for r = 0, 1, ... while below n_items (a prefix:
+  // item_of grows with r). Roles re-derive an item's fields from its index when
+  // they need them, which keeps the softmax loop's live registers down.
+  const int n_items = p.B * p.Hq * p.nT;
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_qfree, 1);
     for (int s = 0; s < KS; ++s) { mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1); }
     for (int s = 0; s < VS; ++s) { mbar_init(&bar_vf[s], 1); mbar_init(&bar_ve[s], 1); }
     mbar_init(&bar_s, 1);
@@ -96,6 +134,7 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
     mbar_init(&bar_p, 128);
     mbar_init(&bar_pfree, 1);
     mbar_init(&bar_o, 1);
+    mbar_init(&bar_ofree, 128);
     mbar_init(&bar_drain, 1);
     abort_sh = 0;
     fence_mbar_init();
@@ -117,40 +156,52 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
       tma_prefetch_desc(&p.tmap_q);
       tma_prefetch_desc(&p.tmap_k);
       tma_prefetch_desc(&p.tmap_v);
-      mbar_arrive_expect_tx(&bar_q, Cfg::kTileBytes);
-      for (int hf = 0; hf < Cfg::kHalves; ++hf)
-        tma_load_4d(smem + Cfg::kOffQ + hf * kHalfTileBytes, &p.tmap_q, &bar_q, hf * 64, h, qt * kTile, b);
-      int issued_k[KS] = {}, issued_v[VS] = {};
+      int issued_k[KS] = {}, issued_v[VS] = {}, n_q = 0;
       bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int ks = j % KS, kn = j / KS;
-        if (kn > 0) ok = mbar_wait(&bar_ke[ks], (kn - 1) & 1, ctx, 1);
+      int gk = 0;  // K/V tiles loaded so far, over all items
+      for (int r = 0; r < Cfg::kMaxRounds && ok; ++r) {
+        const int id = item_of(r, blockIdx.x, gridDim.x);
+        if (id >= n_items) break;
+        const FwdItem it = decode_item(p, id);
+        // Q of the previous item is read until its last S MMA is done
+        if (r > 0) ok = mbar_wait(&bar_qfree, (r - 1) & 1, ctx, 5);
         if (!ok) break;
-        mbar_arrive_expect_tx(&bar_kf[ks], Cfg::kTileBytes);
+        mbar_arrive_expect_tx(&bar_q, Cfg::kTileBytes);
         for (int hf = 0; hf < Cfg::kHalves; ++hf)
-          tma_load_4d(smem + Cfg::kOffK + ks * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_k, &bar_kf[ks],
-                      hf * 64, kvh, j * kTile, b);
-        issued_k[ks]++;
-        const int vs = j % VS, vn = j / VS;
-        if (vn > 0) ok = mbar_wait(&bar_ve[vs], (vn - 1) & 1, ctx, 2);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bar_vf[vs], Cfg::kTileBytes);
-        for (int hf = 0; hf < Cfg::kHalves; ++hf)
-          tma_load_4d(smem + Cfg::kOffV + vs * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v, &bar_vf[vs],
-                      hf * 64, kvh, j * kTile, b);
-        issued_v[vs]++;
+          tma_load_4d(smem + Cfg::kOffQ + hf * kHalfTileBytes, &p.tmap_q, &bar_q, hf * 64, it.h, it.qt * kTile,
+                      it.b);
+        ++n_q;
+        for (int j = 0; j < it.n_kv && ok; ++j, ++gk) {
+          const int ks = gk % KS, kn = gk / KS;
+          if (kn > 0) ok = mbar_wait(&bar_ke[ks], (kn - 1) & 1, ctx, 1);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bar_kf[ks], Cfg::kTileBytes);
+          for (int hf = 0; hf < Cfg::kHalves; ++hf)
+            tma_load_4d(smem + Cfg::kOffK + ks * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_k, &bar_kf[ks],
+                        hf * 64, it.kvh, j * kTile, it.b);
+          issued_k[ks]++;
+          const int vs = gk % VS, vn = gk / VS;
+          if (vn > 0) ok = mbar_wait(&bar_ve[vs], (vn - 1) & 1, ctx, 2);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bar_vf[vs], Cfg::kTileBytes);
+          for (int hf = 0; hf < Cfg::kHalves; ++hf)
+            tma_load_4d(smem + Cfg::kOffV + vs * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v, &bar_vf[vs],
+                        hf * 64, it.kvh, j * kTile, it.b);
+          issued_v[vs]++;
+        }
       }
       if (ok) {
-        // Wait for the MMA side to release every stage, so that no commit
-        // arrives on a barrier of this CTA after it has left.
+        // Wait for the MMA side to release every stage and the last Q, so that no
+        // commit arrives on a barrier of this CTA after it has left.
         for (int s = 0; s < KS && ok; ++s)
           if (issued_k[s] > 0) ok = mbar_wait(&bar_ke[s], (issued_k[s] - 1) & 1, ctx, 3);
         for (int s = 0; s < VS && ok; ++s)
           if (issued_v[s] > 0) ok = mbar_wait(&bar_ve[s], (issued_v[s] - 1) & 1, ctx, 4);
+        if (Cfg::kPersistent && ok && n_q > 0) ok = mbar_wait(&bar_qfree, (n_q - 1) & 1, ctx, 6);
       }
       if (!ok) {
         // Abort path: let every load already issued land before the CTA exits.
-        mbar_wait_drain(&bar_q, 0, p.budget_ns);
+        if (n_q > 0) mbar_wait_drain(&bar_q, (n_q - 1) & 1, p.budget_ns);
         for (int s = 0; s < KS; ++s)
           if (issued_k[s] > 0) mbar_wait_drain(&bar_kf[s], (issued_k[s] - 1) & 1, p.budget_ns);
         for (int s = 0; s < VS; ++s)
@@ -170,9 +221,11 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
       if (elect_one()) mma_commit(bar);
       __syncwarp();
     };
-    auto issue_s = [&](int j) -> bool {
-      const int ks = j % KS;
-      if (!warp_wait(&bar_kf[ks], (j / KS) & 1, ctx, 11)) return false;
+    // S(g) into columns [0,128); d = 64: once the softmax holds S(g-1).
+    auto issue_s = [&](int g, bool last_of_item) -> bool {
+      if (kSepP && g > 0 && !warp_wait(&bar_sfree, (g - 1) & 1, ctx, 14)) return false;
+      const int ks = g % KS;
+      if (!warp_wait(&bar_kf[ks], (g / KS) & 1, ctx, 11)) return false;
       tc_fence_after();
       const uint64_t kb = dK + ks * kTileD;
       if (elect_one()) {
@@ -183,21 +236,24 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
         }
         mma_commit(&bar_s);
         mma_commit(&bar_ke[ks]);
+        if (Cfg::kPersistent && last_of_item) mma_commit(&bar_qfree);
       }
       __syncwarp();
       issued = true;
       return true;
     };
-    auto issue_pv = [&](int jj) -> bool {
-      const int vs = jj % VS;
-      if (!warp_wait(&bar_p, jj & 1, ctx, 12)) return false;
-      if (!warp_wait(&bar_vf[vs], (jj / VS) & 1, ctx, 13)) return false;
+    // PV(g); the first of item r overwrites O once the epilogue of item r-1 has read it.
+    auto issue_pv = [&](int g, bool first_of_item, int r) -> bool {
+      const int vs = g % VS;
+      if (!warp_wait(&bar_p, g & 1, ctx, 12)) return false;
+      if (first_of_item && r > 0 && !warp_wait(&bar_ofree, (r - 1) & 1, ctx, 15)) return false;
+      if (!warp_wait(&bar_vf[vs], (g / VS) & 1, ctx, 13)) return false;
       tc_fence_after();
       const uint64_t vb = dV + vs * kTileD;
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + kColO, tmem + kColP + kk * 8, vb + kk * 128, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + kColO, tmem + kColP + kk * 8, vb + kk * 128, idesc_o, (!first_of_item || kk > 0) ? 1u : 0u);
         if (kSepP) mma_commit(&bar_pfree);
         mma_commit(&bar_ve[vs]);
       }
@@ -205,32 +261,33 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
       issued = true;
       return true;
     };
-    bool ok = warp_wait(&bar_q, 0, ctx, 10);
-    if (kSepP) {
-      // S(j+1) as soon as the softmax holds S(j); PV(j) once P(j) is written.
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        if (j + 1 < n_kv) {
-          ok = warp_wait(&bar_sfree, j & 1, ctx, 14);
-          if (ok) ok = issue_s(j + 1);
-          if (!ok) break;
+    bool ok = true;
+    int g0 = 0;  // global index of the item's first tile
+    for (int r = 0; r < Cfg::kMaxRounds && ok; ++r) {
+      const int id = item_of(r, blockIdx.x, gridDim.x);
+      if (id >= n_items) break;
+      const int n_kv = decode_item(p, id).n_kv;
+      ok = warp_wait(&bar_q, r & 1, ctx, 10);
+      if (!ok) break;
+      if (kSepP) {
+        // S(j+1) as soon as the softmax holds S(j); PV(j) once P(j) is written.
+        ok = issue_s(g0, n_kv == 1);
+        for (int j = 0; j < n_kv && ok; ++j) {
+          if (j + 1 < n_kv) ok = issue_s(g0 + j + 1, j + 2 == n_kv);
+          if (ok) ok = issue_pv(g0 + j, j == 0, r);
         }
-        ok = issue_pv(j);
-      }
-    } else {
-      for (int j = 0; j < n_kv && ok; ++j) {
-        // O += P_{j-1} V_{j-1} must be issued before S_j overwrites P_{j-1}.
-        if (j > 0) {
-          ok = issue_pv(j - 1);
-          if (!ok) break;
+      } else {
+        for (int j = 0; j < n_kv && ok; ++j) {
+          // O += P_{j-1} V_{j-1} must be issued before S_j overwrites P_{j-1}.
+          if (j > 0) ok = issue_pv(g0 + j - 1, j == 1, r);
+          if (ok) ok = issue_s(g0 + j, j + 1 == n_kv);
         }
-        ok = issue_s(j);
+        if (ok) ok = issue_pv(g0 + n_kv - 1, n_kv == 1, r);
       }
-      if (ok) ok = issue_pv(n_kv - 1);
+      if (ok) commit(&bar_o);
+      g0 += n_kv;
     }
-    if (ok) {
-      commit(&bar_o);
-    } else if (issued) {
+    if (!ok && issued) {
       commit(&bar_drain);
       mbar_wait_drain(&bar_drain, 0, p.budget_ns);
     }
@@ -238,134 +295,175 @@ __global__ void __launch_bounds__(kFwdThreads, 2) attn_fwd_kernel(const __grid_c
     // ------------------------------------------------------------ softmax warpgroup
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int q_idx = qt * kTile + row;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_base + kColS;
     const uint32_t tP = tmem + lane_base + kColP;
     const uint32_t tO = tmem + lane_base + kColO;
     const float sl2 = p.scale_log2;
-    float m_used = -INFINITY;  // running max in log2 units (possibly stale by <= 8)
-    float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      ok = warp_wait(&bar_s, j & 1, ctx, 20);
-      if (!ok) break;
-      tc_fence_after();
-      float s[kTile];
-      {
-        // one batched load of the whole row, one wait
-        uint32_t r[kTile];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < kTile; ++i) s[i] = __uint_as_float(r[i]);
-      }
-      if (kSepP) {
-        // S is in registers: the MMA may compute S(j+1) into the same columns.
-        tc_fence_before();
-        mbar_arrive(&bar_sfree);
-      }
-      if (p.causal && j == qt) {
-#pragma unroll
-        for (int c = 0; c < kTile; ++c)
-          if (c > row) s[c] = -INFINITY;
-      } else if (!p.causal && (j + 1) * kTile > p.T) {
-        const int lim = p.T - j * kTile;
-#pragma unroll
-        for (int c = 0; c < kTile; ++c)
-          if (c >= lim) s[c] = -INFINITY;
-      }
-      // row max: a tree of 3-input maxima (independent chains, half the instructions)
-      float m8[8];
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        float a = max3(s[g * 16 + 0], s[g * 16 + 1], s[g * 16 + 2]);
-        float b = max3(s[g * 16 + 3], s[g * 16 + 4], s[g * 16 + 5]);
-        float c = max3(s[g * 16 + 6], s[g * 16 + 7], s[g * 16 + 8]);
-        float d = max3(s[g * 16 + 9], s[g * 16 + 10], s[g * 16 + 11]);
-        float e = max3(s[g * 16 + 12], s[g * 16 + 13], s[g * 16 + 14]);
-        m8[g] = max3(max3(a, b, c), max3(d, e, s[g * 16 + 15]), a);
-      }
-      const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-      const float m_tile = mx * sl2;
-      const bool need = m_tile > m_used + kRescaleThreshold;
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2_approx(m_used - m_tile);
-        m_used = m_tile;
-        l *= alpha;
-      }
-      // p = 2^(s*c - m) two columns at a time (packed fp32 FMA and add), bf16 pairs kept
-      // in registers until the P columns are free.
-      const uint64_t c2 = f2_make(sl2, sl2), nm2 = f2_make(-m_used, -m_used);
-      uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};  // independent partial sums of pairs
-      uint32_t pk[kTile / 2];
-#pragma unroll
-      for (int i = 0; i < kTile / 2; ++i) {
-        float x0, x1;
-        f2_split(f2_fma(f2_make(s[2 * i], s[2 * i + 1]), c2, nm2), x0, x1);
-        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-        lsum[i & 3] = f2_add(lsum[i & 3], f2_make(p0, p1));
-        pk[i] = pack_bf16x2(p0, p1);
-      }
-      {
-        float a0, a1, b0, b1;
-        f2_split(f2_add(f2_add(lsum[0], lsum[1]), f2_add(lsum[2], lsum[3])), a0, a1);
-        l += a0 + a1;
-        (void)b0;
-        (void)b1;
-      }
-      // d = 64: P(j-1) and O must no longer be read by PV(j-1).
-      if (kSepP && j > 0) {
-        ok = warp_wait(&bar_pfree, (j - 1) & 1, ctx, 22);
+    int g = 0;  // tiles seen so far, over all items
+    for (int r = 0; r < Cfg::kMaxRounds && ok; ++r) {
+      const int id = item_of(r, blockIdx.x, gridDim.x);
+      if (id >= n_items) break;
+      const int qt = p.nT - 1 - id / (p.B * p.Hq);
+      const int n_kv = p.causal ? qt + 1 : p.nT;
+      float m_used = -INFINITY;  // running max in log2 units (possibly stale by <= 8)
+      float l = 0.f;
+      for (int j = 0; j < n_kv; ++j, ++g) {
+        ok = warp_wait(&bar_s, g & 1, ctx, 20);
         if (!ok) break;
         tc_fence_after();
-      }
+        float s[kTile];
+        {
+          // one batched load of the whole row, one wait
+          uint32_t rr[kTile];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c * 16]));
-      // Rescale O (complete: PV_{j-1} has finished) when any row of this warp needs it.
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tO + c * 32, r);
+          for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[cc * 32]));
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st32(tO + c * 32, r);
+          for (int i = 0; i < kTile; ++i) s[i] = __uint_as_float(rr[i]);
         }
+        if (kSepP) {
+          // S is in registers: the MMA may compute S(g+1) into the same columns.
+          tc_fence_before();
+          mbar_arrive(&bar_sfree);
+        }
+        if (p.causal && j == qt) {
+#pragma unroll
+          for (int cc = 0; cc < kTile; ++cc)
+            if (cc > row) s[cc] = -INFINITY;
+        } else if (!p.causal && (j + 1) * kTile > p.T) {
+          const int lim = p.T - j * kTile;
+#pragma unroll
+          for (int cc = 0; cc < kTile; ++cc)
+            if (cc >= lim) s[cc] = -INFINITY;
+        }
+        // row max: a tree of 3-input maxima (independent chains, half the instructions)
+        float m8[8];
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+          float a = max3(s[q8 * 16 + 0], s[q8 * 16 + 1], s[q8 * 16 + 2]);
+          float b = max3(s[q8 * 16 + 3], s[q8 * 16 + 4], s[q8 * 16 + 5]);
+          float cc = max3(s[q8 * 16 + 6], s[q8 * 16 + 7], s[q8 * 16 + 8]);
+          float d = max3(s[q8 * 16 + 9], s[q8 * 16 + 10], s[q8 * 16 + 11]);
+          float e = max3(s[q8 * 16 + 12], s[q8 * 16 + 13], s[q8 * 16 + 14]);
+          m8[q8] = max3(max3(a, b, cc), max3(d, e, s[q8 * 16 + 15]), a);
+        }
+        const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        const float m_tile = mx * sl2;
+        const bool need = m_tile > m_used + kRescaleThreshold;
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2_approx(m_used - m_tile);
+          m_used = m_tile;
+          l *= alpha;
+        }
+        // p = 2^(s*c - m) two columns at a time (packed fp32 FMA and add), bf16 pairs kept
+        // in registers until the P columns are free.
+        const uint64_t c2 = f2_make(sl2, sl2), nm2 = f2_make(-m_used, -m_used);
+        uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};  // independent partial sums of pairs
+        uint32_t pk[kTile / 2];
+#pragma unroll
+        for (int i = 0; i < kTile / 2; ++i) {
+          float x0, x1;
+          f2_split(f2_fma(f2_make(s[2 * i], s[2 * i + 1]), c2, nm2), x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          lsum[i & 3] = f2_add(lsum[i & 3], f2_make(p0, p1));
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        {
+          float a0, a1;
+          f2_split(f2_add(f2_add(lsum[0], lsum[1]), f2_add(lsum[2], lsum[3])), a0, a1);
+          l += a0 + a1;
+        }
+        // d = 64: P(g-1) (possibly of the previous item) must no longer be read by PV(g-1).
+        if (kSepP && g > 0) {
+          ok = warp_wait(&bar_pfree, (g - 1) & 1, ctx, 22);
+          if (!ok) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tmem_st16(tP + cc * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[cc * 16]));
+        // Rescale O (complete: PV_{j-1} has finished) when any row of this warp needs it.
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t rr[32];
+            tmem_ld32(tO + cc * 32, rr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st32(tO + cc * 32, rr);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar_p);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bar_p);
-    }
-    if (ok) ok = warp_wait(&bar_o, 0, ctx, 21);
-    if (ok) {
+      if (ok) ok = warp_wait(&bar_o, r & 1, ctx, 21);
+      if (!ok) break;
+      // ---- epilogue: O / l as bf16, and the row's log-sum-exp
       tc_fence_after();
+      const FwdItem it = decode_item(p, id);
+      const int q_idx = qt * kTile + row;
       const float inv_l = 1.f / l;
       const bool valid = q_idx < p.T;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                            ((static_cast<size_t>(b) * p.T + (valid ? q_idx : 0)) * p.Hq + h) * D;
+      if constexpr (Cfg::kTmaStore) {
+        // O / l as bf16 pairs, then O's columns are free; 32 rows x 128 bytes per
+        // warp staged with the 128-byte swizzle (chunk c of row r at c ^ (r & 7))
+        // and stored with one TMA box
+        uint32_t o_pk[D / 2];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tO + c * 32, r);
-        tmem_wait_ld();
-        uint32_t pk[16];
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t rr[32];
+          tmem_ld32(tO + cc * 32, rr);
+          tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          for (int i = 0; i < 16; ++i)
+            o_pk[cc * 16 + i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l, __uint_as_float(rr[2 * i + 1]) * inv_l);
         }
+        tc_fence_before();
+        mbar_arrive(&bar_ofree);  // the next item's first PV may overwrite O
+        uint8_t* stg = smem + Cfg::kOffOut + (warp - 2) * 32 * 128;
+        if (lane == 0) tma_store_wait_read();
+        __syncwarp();
+#pragma unroll
+        for (int v = 0; v < D / 8; ++v)
+          *reinterpret_cast<uint4*>(stg + lane * 128 + ((v ^ (lane & 7)) * 16)) =
+              make_uint4(o_pk[4 * v], o_pk[4 * v + 1], o_pk[4 * v + 2], o_pk[4 * v + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int r0 = qt * kTile + quarter * 32;
+        if (lane == 0 && r0 < p.T) {
+          tma_store_4d(&p.tmap_o, stg, 0, it.h, r0, it.b);
+          tma_store_commit();
+        }
+      } else {
+        // 32 columns at a time straight to memory
+        uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                               ((static_cast<size_t>(it.b) * p.T + (valid ? q_idx : 0)) * p.Hq + it.h) * D);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t rr[32];
+          tmem_ld32(tO + cc * 32, rr);
+          tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l, __uint_as_float(rr[2 * i + 1]) * inv_l);
+          if (valid) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) orow[cc * 4 + v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+          }
+        }
+        // one item per CTA: no next item waits for O (and an arrive queued behind
+        // these stores would hold the warp until they drain)
       }
       if (valid)
-        p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.T + q_idx] = (m_used + log2f(l)) * 0.69314718055994531f;
+        p.lse[(static_cast<size_t>(it.b) * p.Hq + it.h) * p.T + q_idx] = (m_used + log2f(l)) * 0.69314718055994531f;
     }
+    // the staging rows must stay until the TMA stores have finished
+    if (Cfg::kTmaStore && lane == 0) tma_store_wait_all();
   }
 
   tc_fence_before();
@@ -389,7 +487,19 @@ cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const unsigned grid = static_cast<unsigned>(p.B) * p.Hq * p.nT;
+  // d = 64: persistent, two CTAs per SM. d = 128: one item per CTA (the grid
+  // covers every item, so each CTA's list is its own index): without room for
+  // the staged epilogue its item boundaries gain little from persistence, and
+  // the hardware's dispatch of CTAs to whichever SM frees first balanced the
+  // per-SM speed differences better than the fixed lists (measured 5% faster).
+  const long long n_items = static_cast<long long>(p.B) * p.Hq * p.nT;
+  long long slots = n_items;
+  if (FwdCfg<D>::kPersistent) {
+    int sms = 0;
+    if ((e = sm_count(&sms)) != cudaSuccess) return e;
+    slots = static_cast<long long>(sms) * kFwdCtasPerSm;
+  }
+  const unsigned grid = static_cast<unsigned>(n_items < slots ? n_items : slots);
   e = launch_pdl(attn_fwd_kernel<D>, grid, kFwdThreads, smem, stream, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
