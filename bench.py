@@ -143,6 +143,19 @@ def gpu_bus_id(torch, dev):
 
 
 # ----------------------------------------------------------------------------- traffic record
+def packed_buffer(torch, specs, device=None, pin=False):
+    """One flat uint8 buffer holding tensors of the given (shape, dtype), each at a
+    256-byte aligned offset; returns the buffer and the tensor views."""
+    offs, total = [], 0
+    for shape, dt in specs:
+        nbytes = int(torch.Size(shape).numel()) * torch.empty((), dtype=dt).element_size()
+        offs.append((total, nbytes))
+        total += (nbytes + 255) // 256 * 256
+    buf = torch.empty(total, dtype=torch.uint8, device=device, pin_memory=pin)
+    views = [buf[o:o + n].view(dt).view(shape) for (o, n), (shape, dt) in zip(offs, specs)]
+    return buf, views
+
+
 def kernel_source_hash(files):
     h = hashlib.sha256()
     for f in files:
@@ -254,11 +267,18 @@ def run_ours(args, w):
     gqa.load()
     peaks, peak_src = load_peaks()
 
-    q_h, k_h, v_h, do_h = (x.pin_memory() for x in workload_inputs(w))
-    q, k, v, dout = (x.to(dev) for x in (q_h, k_h, v_h, do_h))
-    o = torch.empty_like(q)
-    lse = torch.empty((w.B, w.Hq, w.T), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    # Inputs and outputs each live in one contiguous buffer (views at 256-byte
+    # aligned offsets), so the end-to-end leg moves them with one copy each way.
+    q_c, k_c, v_c, do_c = workload_inputs(w)
+    in_specs = [(x.shape, x.dtype) for x in (q_c, k_c, v_c, do_c)]
+    out_specs = [(q_c.shape, torch.bfloat16), ((w.B, w.Hq, w.T), torch.float32), (q_c.shape, torch.bfloat16),
+                 (k_c.shape, torch.bfloat16), (v_c.shape, torch.bfloat16)]
+    in_d, (q, k, v, dout) = packed_buffer(torch, in_specs, device=dev)
+    in_h, host_in = packed_buffer(torch, in_specs, pin=True)
+    for dst, src in zip(host_in, (q_c, k_c, v_c, do_c)):
+        dst.copy_(src)
+    in_d.copy_(in_h)
+    out_d, (o, lse, dq, dk, dv) = packed_buffer(torch, out_specs, device=dev)
     ws = torch.empty(gqa.attn_bwd_workspace_bytes(w.B, w.T, w.Hq), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -353,26 +373,15 @@ def run_ours(args, w):
     kernel_ms = {n: per_kernel[n] / args.steps for n in names}
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
-    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-    dq_h = torch.empty(dq.shape, dtype=dq.dtype, pin_memory=True)
-    dk_h = torch.empty(dk.shape, dtype=dk.dtype, pin_memory=True)
-    dv_h = torch.empty(dv.shape, dtype=dv.dtype, pin_memory=True)
-    h2d = sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h, do_h))
-    d2h = sum(x.numel() * x.element_size() for x in (o_h, lse_h, dq_h, dk_h, dv_h))
+    out_h, _ = packed_buffer(torch, out_specs, pin=True)
+    h2d = in_h.numel()
+    d2h = out_h.numel()
 
     def e2e_step():
-        q.copy_(q_h, non_blocking=True)
-        k.copy_(k_h, non_blocking=True)
-        v.copy_(v_h, non_blocking=True)
-        dout.copy_(do_h, non_blocking=True)
+        in_d.copy_(in_h, non_blocking=True)
         gqa.attn_fwd(q, k, v, causal=causal, o=o, lse=lse, stream=stream)
         gqa.attn_bwd(q, k, v, o, lse, dout, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
-        o_h.copy_(o, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-        dq_h.copy_(dq, non_blocking=True)
-        dk_h.copy_(dk, non_blocking=True)
-        dv_h.copy_(dv, non_blocking=True)
+        out_h.copy_(out_d, non_blocking=True)
 
     for _ in range(0 if args.profile_run else 3):
         e2e_step()
