@@ -74,6 +74,10 @@ CASES = [
     (1, 200, 4, 2, 64, False, 1.0),    # full attention, ragged
     (1, 256, 2, 2, 128, False, 1.0),   # full attention, d=128
     (1, 333, 6, 3, 64, False, 2.0),    # full attention, ragged, large logits
+    # more 128-query items than the d = 64 forward's persistent CTAs (2 per SM), so
+    # CTAs run several items back to back
+    (4, 1500, 8, 2, 64, True, 1.0),    # causal, ragged, 384 items
+    (4, 1000, 12, 4, 64, False, 1.0),  # full attention, ragged, 384 items of equal cost
 ]
 
 
