@@ -261,16 +261,22 @@ __device__ __forceinline__ void store_acc_bf16(const uint32_t (&r)[NC], __nv_bfl
 template <bool DKV, bool MASKED>
 __device__ __forceinline__ void score_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32], float sl2, int lo,
                                             int hi, uint32_t (&pk)[16], uint32_t (&dk)[16]) {
+  // column pairs through packed fp32 multiplies (same rounding as scalar ones)
+  const uint64_t c2 = f2_make(sl2, sl2);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    float p0 = ex2_approx(__uint_as_float(s[2 * i]) * sl2);
-    float p1 = ex2_approx(__uint_as_float(s[2 * i + 1]) * sl2);
+    float x0, x1;
+    f2_split(f2_mul(f2_make(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2), x0, x1);
+    float p0 = ex2_approx(x0);
+    float p1 = ex2_approx(x1);
     if (MASKED) {
       p0 = (2 * i >= lo && 2 * i < hi) ? p0 : 0.f;
       p1 = (2 * i + 1 >= lo && 2 * i + 1 < hi) ? p1 : 0.f;
     }
     if (DKV) pk[i] = pack_bf16x2(p0, p1);
-    dk[i] = pack_bf16x2(p0 * __uint_as_float(dp[2 * i]), p1 * __uint_as_float(dp[2 * i + 1]));
+    float d0, d1;
+    f2_split(f2_mul(f2_make(p0, p1), f2_make(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1]))), d0, d1);
+    dk[i] = pack_bf16x2(d0, d1);
   }
 }
 
