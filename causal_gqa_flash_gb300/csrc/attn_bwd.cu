@@ -877,8 +877,9 @@ __device__ __forceinline__ bool compute_tiles(const BwdParams& p, MainBars& bars
   };
   bool ok = true;
   if (DKV) {
-    for (int it = it0; it < it1 && ok; ++it) {
-      const int qt = t.i0 + it % t.ni;
+    // query tile of step it: i0 + it % ni, kept as a running counter (ni = nT - i0)
+    int qt = t.i0 + it0 % t.ni;
+    for (int it = it0; it < it1 && ok; ++it, qt = (qt + 1 == p.nT) ? t.i0 : qt + 1) {
       // Query columns visible to this key row: [lo, hi) in this warpgroup's 32-column frame.
       const int hi_tile = min(kTile, p.T - qt * kTile);
       const bool diag = p.causal && qt == t.tile;
