@@ -361,6 +361,7 @@ __device__ __forceinline__ int recv_task(MainBars& bars, const volatile int* slo
 // ============================================================================ producer
 template <int D>
 __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem, MainBars& bars, volatile int* slot,
+                                              TaskInfo* ring,
                                               const WaitCtx& ctx, int lane) {
   using Cfg = MainCfg<D>;
   constexpr int NKV = Cfg::kKvStages, NK = Cfg::kDqKStages, NV = Cfg::kDqVStages, NF = Cfg::kNF;
@@ -384,6 +385,10 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
       id = x < n_tasks ? x : -1;
     }
     id = __shfl_sync(0xffffffffu, id, 0);
+    // Decoded once here (integer divisions by runtime sizes); the other warps read
+    // it from the ring.
+    TaskInfo t{};
+    if (id >= 0) t = decode_task(p, id);
     if (n >= 2) ok = lane0_wait(&bars.task_empty[n & 1], ((n - 2) >> 1) & 1, ctx, 41, lane);
     // Pace on acc_free: the compute warps finish the epilogue of n-1 only after
     // they received task n, so waiting for epilogue n-2 here keeps this warp in
@@ -391,11 +396,11 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
     if (ok && n >= 2) ok = lane0_wait(&bars.acc_free, (n - 2) & 1, ctx, 44, lane);
     if (!ok) break;
     if (lane == 0) {
+      if (id >= 0) ring[n & 3] = t;
       slot[n & 1] = id;
       mbar_arrive(&bars.task_full[n & 1]);
     }
     if (id < 0) break;
-    const TaskInfo t = decode_task(p, id);
     // Fixed buffer f held task n-NF, free once that task's last S/dP MMAs are
     // done; a change of layout needs every MMA of the previous task done (its
     // epilogue has read the accumulators, so they are).
@@ -419,23 +424,22 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
       // -LSE2 and D of the next stage's 128 query rows, 4 per lane, fetched one
       // stage ahead so their latency hides behind the wait for a free stage.
       float vnl[4], vd[4];
-      auto fetch = [&](int it) {
-        const int hq = t.kvh * p.G + it / t.ni;
-        const int qt = t.i0 + it % t.ni;
-        const size_t vec = vec_bh0 + static_cast<size_t>(hq) * p.Tpad + static_cast<size_t>(qt) * kTile + lane;
+      // (query head, query tile) of stages it and it + 1 as running counters:
+      // it = (hq - kvh * G) * ni + (qt - i0)
+      int hq = t.kvh * p.G, qt = t.i0, hq_n = hq, qt_n = qt;
+      auto fetch = [&]() {
+        const size_t vec = vec_bh0 + static_cast<size_t>(hq_n) * p.Tpad + static_cast<size_t>(qt_n) * kTile + lane;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           vnl[k] = __ldg(p.lse2 + vec + 32 * k);
           vd[k] = __ldg(p.Dvec + vec + 32 * k);
         }
       };
-      fetch(0);
+      fetch();
       for (int it = 0; it < t.n_it && ok; ++it, ++kv_used) {
         const int st = kv_used % NKV, u = kv_used / NKV;
         if (u > 0) ok = lane0_wait(&bars.kv_empty[st], (u - 1) & 1, ctx, 1, lane);
         if (!ok) break;
-        const int hq = t.kvh * p.G + it / t.ni;
-        const int qt = t.i0 + it % t.ni;
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars.kv_full[st], 2 * Cfg::kTileBytes);
           for (int hf = 0; hf < Cfg::kHalves; ++hf) {
@@ -450,7 +454,13 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
           write_aux_row(smem + Cfg::st_qx(st), lane + 32 * k, vnl[k] * inv_sl2);
           write_aux_row(smem + Cfg::st_dx(st), lane + 32 * k, -vd[k]);
         }
-        if (it + 1 < t.n_it) fetch(it + 1);
+        if (++qt_n == p.nT) {
+          qt_n = t.i0;
+          ++hq_n;
+        }
+        if (it + 1 < t.n_it) fetch();
+        hq = hq_n;
+        qt = qt_n;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.kv_full[st]);
@@ -714,8 +724,8 @@ __device__ __forceinline__ bool sdp_task(const MmaCtx<D>& m, MainBars& bars, con
 
 template <int D>
 __device__ __forceinline__ void sdp_issuer_role(const BwdParams& p, uint8_t* smem, MainBars& bars,
-                                                const volatile int* slot, uint32_t tmem, const WaitCtx& ctx,
-                                                int lane) {
+                                                const volatile int* slot, const TaskInfo* ring, uint32_t tmem,
+                                                const WaitCtx& ctx, int lane) {
   using Cfg = MainCfg<D>;
   MmaCtx<D> m;
   m.init(smem, tmem);
@@ -724,7 +734,7 @@ __device__ __forceinline__ void sdp_issuer_role(const BwdParams& p, uint8_t* sme
   for (;; ++n) {
     const int id = recv_task(bars, slot, n, ctx, lane, ok);
     if (!ok || id < 0) break;
-    const TaskInfo t = decode_task(p, id);
+    const TaskInfo t = ring[n & 3];
     const int f = n % Cfg::kNF;
     ok = warp_wait(&bars.fixed_full[f], (n / Cfg::kNF) & 1, ctx, 10);
     if (!ok) break;
@@ -797,8 +807,8 @@ __device__ __forceinline__ bool grad_task(const MmaCtx<D>& m, MainBars& bars, co
 
 template <int D>
 __device__ __forceinline__ void grad_issuer_role(const BwdParams& p, uint8_t* smem, MainBars& bars,
-                                                 const volatile int* slot, uint32_t tmem, const WaitCtx& ctx,
-                                                 int lane) {
+                                                 const volatile int* slot, const TaskInfo* ring, uint32_t tmem,
+                                                 const WaitCtx& ctx, int lane) {
   using Cfg = MainCfg<D>;
   MmaCtx<D> m;
   m.init(smem, tmem);
@@ -807,7 +817,7 @@ __device__ __forceinline__ void grad_issuer_role(const BwdParams& p, uint8_t* sm
   for (;; ++n) {
     const int id = recv_task(bars, slot, n, ctx, lane, ok);
     if (!ok || id < 0) break;
-    const TaskInfo t = decode_task(p, id);
+    const TaskInfo t = ring[n & 3];
     const int f = n % Cfg::kNF;
     if (t.dkv) {
       ok = grad_task<D, true>(m, bars, ctx, t.n_it, f, n, G, kv_used, issued);
@@ -995,6 +1005,10 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ volatile int task_slot[2];
+  // Decoded tasks by per-CTA task index n (entry n & 3): written by the producer
+  // before it publishes task n, which needs every consumer to have received task
+  // n - 2, so the compute warps can still read task n - 1 for its epilogue.
+  __shared__ TaskInfo task_ring[4];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1042,21 +1056,21 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
   pdl_wait_previous();  // the workspace is written by the preprocess kernel
 
   if (warp == 0) {
-    producer_role<D>(p, smem, bars, task_slot, ctx, lane);
+    producer_role<D>(p, smem, bars, task_slot, task_ring, ctx, lane);
   } else if (warp == 1) {
-    sdp_issuer_role<D>(p, smem, bars, task_slot, tmem, ctx, lane);
+    sdp_issuer_role<D>(p, smem, bars, task_slot, task_ring, tmem, ctx, lane);
   } else if (warp == kGradWarp) {
-    grad_issuer_role<D>(p, smem, bars, task_slot, tmem, ctx, lane);
+    grad_issuer_role<D>(p, smem, bars, task_slot, task_ring, tmem, ctx, lane);
   } else {
     // With one fixed buffer (d = 128) each task's epilogue runs after the next
     // task's first tile, so its wait for the last gradient MMAs overlaps the next
     // task's first score MMAs; at a change of kind it runs first (the dQ dS
     // columns hold dV of dK/dV tasks). With two fixed buffers the next task's
     // operands are already loaded and the epilogue simply runs first.
-    int n = 0, G = 0, prev_id = -1;  // the previous task is decoded again for its epilogue (registers)
+    int n = 0, G = 0, prev_id = -1;  // the previous task is read again from the ring for its epilogue
     bool ok = true;
-    auto epilogue = [&](int pid, int tn) {
-      const TaskInfo t = decode_task(p, pid);
+    auto epilogue = [&](int tn) {
+      const TaskInfo t = task_ring[tn & 3];
       return t.dkv ? compute_epilogue<D, true>(p, bars, tmem, smem, ctx, t, tn, warp, lane)
                    : compute_epilogue<D, false>(p, bars, tmem, smem, ctx, t, tn, warp, lane);
     };
@@ -1068,14 +1082,14 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
       const int id = recv_task(bars, task_slot, n, ctx, lane, ok);
       if (!ok) break;
       if (id < 0) {
-        if (prev_id >= 0) ok = epilogue(prev_id, n - 1);
+        if (prev_id >= 0) ok = epilogue(n - 1);
         break;
       }
-      const TaskInfo t = decode_task(p, id);
+      const TaskInfo t = task_ring[n & 3];
       const bool early = prev_id >= 0 && (MainCfg<D>::kNF > 1 || (prev_id < p.n_dkv_tasks) != (t.dkv != 0));
-      if (early) ok = epilogue(prev_id, n - 1);
+      if (early) ok = epilogue(n - 1);
       if (ok) ok = tiles(t, 0, 1);
-      if (ok && prev_id >= 0 && !early) ok = epilogue(prev_id, n - 1);
+      if (ok && prev_id >= 0 && !early) ok = epilogue(n - 1);
       if (ok) ok = tiles(t, 1, t.n_it);
       if (!ok) break;
       prev_id = id;
