@@ -199,7 +199,7 @@ gqa_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, floa
   if ((s = make_map(fn, "q", &p.tmap_q, q, B, T, Hq, d)) || (s = make_map(fn, "k", &p.tmap_k, k, B, T, Hkv, d)) ||
       (s = make_map(fn, "v", &p.tmap_v, v, B, T, Hkv, d)))
     return s;
-  if (d == 64 && (s = make_map(fn, "o", &p.tmap_o, o, B, T, Hq, d, 64, 32))) return s;
+  if ((s = make_map(fn, "o", &p.tmap_o, o, B, T, Hq, d, 64, 32))) return s;  // epilogue stores (32-row boxes)
   p.o = o;
   p.lse = lse;
   p.B = B;

@@ -29,7 +29,7 @@ struct FwdParams {
   CUtensorMap tmap_q;  // [B,T,Hq,d] bf16, box 64 x 1 x 128 x 1, 128B swizzle
   CUtensorMap tmap_k;  // [B,T,Hkv,d]
   CUtensorMap tmap_v;  // [B,T,Hkv,d]
-  CUtensorMap tmap_o;  // d = 64 only: [B,T,Hq,d], box 64 x 1 x 32 x 1 (epilogue stores)
+  CUtensorMap tmap_o;  // [B,T,Hq,d], box 64 x 1 x 32 x 1 (epilogue stores)
   void* o;             // [B,T,Hq,d] bf16
   float* lse;          // [B,Hq,T] fp32, natural log
   int B, T, Hq, Hkv, G, nT;

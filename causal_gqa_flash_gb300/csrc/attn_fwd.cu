@@ -58,9 +58,12 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-  // d = 64: per softmax warp, 32 rows x 128 bytes of bf16 O for its TMA store
-  // (at d = 128 two CTAs leave no room for it and rows are stored directly).
+  // d = 64: per softmax warp, 32 rows x 128 bytes of bf16 O for its TMA store.
+  // d = 128: two CTAs leave no room for a region of its own; each CTA runs one
+  // item, so the epilogue stages its rows (32 x 256 bytes per warp, two 64-column
+  // halves) in the Q buffer, which no MMA reads once the item's last PV is done.
   static constexpr bool kTmaStore = (D == 64);
+  static constexpr bool kStageInQ = (D == 128);
   // d = 64: persistent CTAs with lists of items; d = 128: one item per CTA.
   static constexpr bool kPersistent = (D == 64);
   static constexpr int kMaxRounds = kPersistent ? 0x7fffffff : 1;
@@ -438,6 +441,35 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
           tma_store_4d(&p.tmap_o, stg, 0, it.h, r0, it.b);
           tma_store_commit();
         }
+      } else if constexpr (Cfg::kStageInQ) {
+        static_assert(!Cfg::kPersistent, "the Q buffer is reloaded by persistent CTAs");
+        // 32 rows per warp, each 64-column half a 128-byte-swizzled 4 KB box
+        uint8_t* stg = smem + Cfg::kOffQ + (warp - 2) * (32 * 256);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t rr[32];
+          tmem_ld32(tO + cc * 32, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              w[i] = pack_bf16x2(__uint_as_float(rr[8 * v + 2 * i]) * inv_l,
+                                 __uint_as_float(rr[8 * v + 2 * i + 1]) * inv_l);
+            const int ch = cc * 4 + v;  // 16-byte chunk of the row, 0..15
+            *reinterpret_cast<uint4*>(stg + (ch >> 3) * 4096 + lane * 128 + (((ch & 7) ^ (lane & 7)) * 16)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int r0 = qt * kTile + quarter * 32;
+        if (lane == 0 && r0 < p.T) {
+          tma_store_4d(&p.tmap_o, stg, 0, it.h, r0, it.b);
+          tma_store_4d(&p.tmap_o, stg + 4096, 64, it.h, r0, it.b);
+          tma_store_commit();
+        }
       } else {
         // 32 columns at a time straight to memory
         uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
@@ -463,7 +495,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
         p.lse[(static_cast<size_t>(it.b) * p.Hq + it.h) * p.T + q_idx] = (m_used + log2f(l)) * 0.69314718055994531f;
     }
     // the staging rows must stay until the TMA stores have finished
-    if (Cfg::kTmaStore && lane == 0) tma_store_wait_all();
+    if ((Cfg::kTmaStore || Cfg::kStageInQ) && lane == 0) tma_store_wait_all();
   }
 
   tc_fence_before();
