@@ -143,6 +143,23 @@ def gpu_bus_id(torch, dev):
 
 
 # ----------------------------------------------------------------------------- traffic record
+def max_over_ranks(torch, dist, value: float, world: int, device=None) -> float:
+    """The largest `value` over all ranks (the slowest rank's time); the value
+    itself when there is one rank. Works with NCCL on CUDA tensors and with
+    gloo on CPU tensors."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_step: float, steps: int, ms_total: float) -> float:
+    """Work of all ranks (weak scaling: every rank runs the same steps) over the
+    slowest rank's total time, in TFLOP/s."""
+    return world * flops_per_step * steps / (ms_total * 1e-3) / 1e12
+
+
 def packed_buffer(torch, specs, device=None, pin=False):
     """One flat uint8 buffer holding tensors of the given (shape, dtype), each at a
     256-byte aligned offset; returns the buffer and the tensor views."""
@@ -345,12 +362,9 @@ def run_ours(args, w):
     per_kernel = {n: sum(events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps))
                   for j, n in enumerate(names)}
     step_ms_total = sum(step_ev[i][0].elapsed_time(step_ev[i][1]) for i in range(args.steps))
-    t = torch.tensor([step_ms_total], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    step_ms_total = float(t.item())
+    step_ms_total = max_over_ranks(torch, dist, step_ms_total, world, dev)
     ms_per_step = step_ms_total / args.steps
-    value = world * step_flops(w) * args.steps / (step_ms_total * 1e-3) / 1e12
+    value = whole_job_tflops(world, step_flops(w), args.steps, step_ms_total)
     per_gpu = value / world
 
     # roofline of the dominant kernel (largest share of the step)
@@ -395,10 +409,8 @@ def run_ours(args, w):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    te = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = world * step_flops(w) * e_steps / (float(te.item()) * 1e-3) / 1e12 if e_steps else None
+    te_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1), world, dev)
+    e2e_value = whole_job_tflops(world, step_flops(w), e_steps, te_ms) if e_steps else None
 
     cpu = None
     if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.profile_run):
