@@ -389,6 +389,22 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
     // it from the ring.
     TaskInfo t{};
     if (id >= 0) t = decode_task(p, id);
+    // Row terms (-LSE2, D; 4 rows per lane) of the task's first query tile: of its
+    // own tile in a dQ task, of the first stage in a dK/dV task. Their loads are
+    // issued here so the latency overlaps the waits below instead of holding up
+    // the task's first operand loads.
+    float vnl[4], vd[4];
+    const size_t vec_bh0 = (static_cast<size_t>(t.b) * p.Hq) * p.Tpad;
+    if (id >= 0) {
+      const int hq0 = t.dkv ? t.kvh * p.G : t.h;
+      const int qt0 = t.dkv ? t.i0 : t.tile;
+      const size_t vec = vec_bh0 + static_cast<size_t>(hq0) * p.Tpad + static_cast<size_t>(qt0) * kTile + lane;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        vnl[k] = __ldg(p.lse2 + vec + 32 * k);
+        vd[k] = __ldg(p.Dvec + vec + 32 * k);
+      }
+    }
     if (n >= 2) ok = lane0_wait(&bars.task_empty[n & 1], ((n - 2) >> 1) & 1, ctx, 41, lane);
     // Pace on acc_free: the compute warps finish the epilogue of n-1 only after
     // they received task n, so waiting for epilogue n-2 here keeps this warp in
@@ -408,7 +424,6 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
     if (fu > 0) ok = lane0_wait(&bars.fixed_free[f], (fu - 1) & 1, ctx, 42, lane);
     if (ok && n > 0 && t.dkv != prev_kind) ok = lane0_wait(&bars.acc_free, (n - 1) & 1, ctx, 43, lane);
     if (!ok) break;
-    const size_t vec_bh0 = (static_cast<size_t>(t.b) * p.Hq) * p.Tpad;
     uint64_t* fbar = &bars.fixed_full[f];
     if (lane == 0) mbar_arrive_expect_tx(fbar, 2 * Cfg::kTileBytes);
     ++n_fixed;
@@ -422,8 +437,8 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
       __syncwarp();
       if (lane == 0) mbar_arrive(fbar);
       // -LSE2 and D of the next stage's 128 query rows, 4 per lane, fetched one
-      // stage ahead so their latency hides behind the wait for a free stage.
-      float vnl[4], vd[4];
+      // stage ahead so their latency hides behind the wait for a free stage (the
+      // first stage's above).
       // (query head, query tile) of stages it and it + 1 as running counters:
       // it = (hq - kvh * G) * ni + (qt - i0)
       int hq = t.kvh * p.G, qt = t.i0, hq_n = hq, qt_n = qt;
@@ -435,7 +450,6 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
           vd[k] = __ldg(p.Dvec + vec + 32 * k);
         }
       };
-      fetch();
       for (int it = 0; it < t.n_it && ok; ++it, ++kv_used) {
         const int st = kv_used % NKV, u = kv_used / NKV;
         if (u > 0) ok = lane0_wait(&bars.kv_empty[st], (u - 1) & 1, ctx, 1, lane);
@@ -472,21 +486,6 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
           tma_load_4d(fix + Cfg::kDqOffQ + hf * kHalfTileBytes, &p.tmap_q, fbar, hf * 64, t.h, t.tile * kTile, t.b);
           tma_load_4d(fix + Cfg::kDqOffDO + hf * kHalfTileBytes, &p.tmap_do, fbar, hf * 64, t.h, t.tile * kTile, t.b);
         }
-      const size_t vec = vec_bh0 + static_cast<size_t>(t.h) * p.Tpad + static_cast<size_t>(t.tile) * kTile + lane;
-      float vnl[4], vd[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        vnl[k] = __ldg(p.lse2 + vec + 32 * k);
-        vd[k] = __ldg(p.Dvec + vec + 32 * k);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        write_aux_row(fix + Cfg::kDqOffQX, lane + 32 * k, vnl[k] * inv_sl2);
-        write_aux_row(fix + Cfg::kDqOffDX, lane + 32 * k, -vd[k]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(fbar);
       for (int j = 0; j < t.n_it && ok; ++j, ++q_used) {
         const int ks = q_used % NK, ku = q_used / NK;
         if (ku > 0) ok = lane0_wait(&bars.k_empty[ks], (ku - 1) & 1, ctx, 1, lane);
@@ -505,6 +504,17 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
           for (int hf = 0; hf < Cfg::kHalves; ++hf)
             tma_load_4d(smem + Cfg::kDqOffV + vs * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v,
                         &bars.v_full[vs], hf * 64, t.kvh, j * kTile, t.b);
+        }
+        if (j == 0) {
+          // the row terms, once the first K and V tiles are on their way
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            write_aux_row(fix + Cfg::kDqOffQX, lane + 32 * k, vnl[k] * inv_sl2);
+            write_aux_row(fix + Cfg::kDqOffDX, lane + 32 * k, -vd[k]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(fbar);
         }
       }
     }
