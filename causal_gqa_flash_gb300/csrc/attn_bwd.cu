@@ -125,8 +125,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
 //   MMA:     S(G+1), dP(G+1) as soon as sdp_free(G) | gradient MMAs of G on
 //            pds_full(G).
 // so the tensor core computes the scores of G+1 while the compute warps work on
-// G, across task boundaries too: the next task's operands are loaded and its
-// first scores computed while this task's last tile and epilogue run.
+// G. Across a task boundary the next task is published (and its operands start
+// loading) while this task's last tiles run; its first scores follow its fixed
+// operands and first K (or Q/dO) tile.
 // Per task: fixed_full (its fixed operands are in shared memory), fixed_free
 // (its last S/dP MMAs are done, the fixed operands may be replaced), acc_full
 // (its last gradient MMAs are done), acc_free (the epilogue has read its
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
 //   dK/dV 128: S [0,128) dP [128,256) dV [256,384) dK [384,512); no room for a separate
 //              P/dS region, so P goes to S columns [0,64) and dS to [64,128) once every
 //              warpgroup has read S (sdp_free), and S(G+1) follows the gradient MMAs
-//              (warp 1 then issues every MMA of the task).
+//              of G (warp 18 issues it right after them; warp 1 issues dP).
 // Warpgroup g writes the bf16 pairs of its score columns [32g, 32g+32) to columns
 // [16g, 16g+16) of the P (dS) region, so the A operand of K-step kk is at 8*kk.
 // ============================================================================

@@ -23,11 +23,13 @@
 //    releases S at once, so S(j+1) is computed while P(j) is; at d = 128 (no
 //    TMEM room for two CTAs otherwise) P is written over S's first 64 columns
 //    and S(j+1) follows PV(j);
-//  * item boundaries overlap: the next item's Q is loaded once the last S MMA
-//    of the current one has read Q, its first S is computed while the softmax
-//    warps run the epilogue, and only its first PV waits for the epilogue to
-//    have read O out of TMEM; at d = 64 the epilogue stages O in shared memory
-//    and each softmax warp stores its 32 rows with one TMA box;
+//  * item boundaries overlap (d = 64): the next item's Q is loaded once the
+//    last S MMA of the current one has read Q, its first S is computed while
+//    the softmax warps run the epilogue, and only its first PV waits for the
+//    epilogue to have read O out of TMEM;
+//  * the epilogue stages bf16 O in shared memory, 32 rows per softmax warp with
+//    the 128-byte swizzle, and stores them with TMA boxes: in a region of its
+//    own at d = 64, in the item's dead Q buffer at d = 128;
 //  * the running max is rescaled lazily: O and l are only rescaled when a
 //    row's max grows by more than 2^8, otherwise p = 2^(s - m_stale) <= 256;
 //  * causal tiles past the diagonal are never visited; only the diagonal tile
