@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -174,10 +175,16 @@ def packed_buffer(torch, specs, device=None, pin=False):
 
 
 def kernel_source_hash(files):
+    """Hash of the kernel sources' code: comments, blank lines and indentation
+    are left out, so an edit to comments alone keeps the recorded counters."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "causal_gqa_flash_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "causal_gqa_flash_gb300", "csrc", f), encoding="utf-8") as fh:
+            text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        for line in text.splitlines():
+            code = line.split("//", 1)[0].strip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 
