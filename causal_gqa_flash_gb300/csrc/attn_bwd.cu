@@ -43,60 +43,72 @@ __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x &
 
 // ============================================================================
 // Preprocess: D = rowsum(dO * O), -LSE2 = -LSE * log2(e); padded rows get 0.
-// Rows are visited in (b, h, t) order: D/8 threads read one 128- or 256-byte
-// row of O and dO with 16-byte loads, and the LSE read and the D / -LSE2
-// writes of consecutive rows are consecutive in memory.
+// A block covers kPreRows consecutive rows t of one (b, h), a row being read as
+// D/8 16-byte chunks by as many threads (each thread takes two rows, so four
+// loads are in flight), so the block's rows of D / -LSE2 are consecutive in
+// memory; the rows [T, Tpad) of the last block are written as zeros.
 // ============================================================================
+constexpr int kPreThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
-  constexpr int TPR = D / 8;
+struct PreCfg {
+  static constexpr int kTPR = D / 8;                        // threads per row
+  static constexpr int kRows = 2 * (kPreThreads / kTPR);    // rows per block
+};
+
+template <int D>
+__global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const BwdPreParams p) {
+  constexpr int TPR = PreCfg<D>::kTPR;
+  constexpr int RPB = PreCfg<D>::kRows;
   pdl_launch_dependents();
   pdl_wait_previous();
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     p.sched[0] = 0u;  // task counters of the dQ / dK/dV launch
     p.sched[1] = 0u;
   }
-  const long long nrows = static_cast<long long>(p.B) * p.Hq * p.T;
-  const long long gtid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long r = gtid / TPR;  // ((b * Hq + h) * T + t)
-  const int part = static_cast<int>(gtid % TPR);
-  float acc = 0.f;
-  int t = 0;
-  long long bh = 0;
-  if (r < nrows) {
-    t = static_cast<int>(r % p.T);
-    bh = r / p.T;
-    const int h = static_cast<int>(bh % p.Hq);
-    const long long b = bh / p.Hq;
-    const long long row = (b * p.T + t) * p.Hq + h;  // memory row of O / dO
-    const uint4 a = reinterpret_cast<const uint4*>(p.o)[row * TPR + part];
-    const uint4 c = reinterpret_cast<const uint4*>(p.dO)[row * TPR + part];
-    acc = bf16lo(a.x) * bf16lo(c.x);
-    acc = fmaf(bf16hi(a.x), bf16hi(c.x), acc);
-    acc = fmaf(bf16lo(a.y), bf16lo(c.y), acc);
-    acc = fmaf(bf16hi(a.y), bf16hi(c.y), acc);
-    acc = fmaf(bf16lo(a.z), bf16lo(c.z), acc);
-    acc = fmaf(bf16hi(a.z), bf16hi(c.z), acc);
-    acc = fmaf(bf16lo(a.w), bf16lo(c.w), acc);
-    acc = fmaf(bf16hi(a.w), bf16hi(c.w), acc);
+  const int n_tb = (p.Tpad + RPB - 1) / RPB;  // row blocks per (b, h)
+  const int bh = static_cast<int>(blockIdx.x) / n_tb;
+  const int t0 = (static_cast<int>(blockIdx.x) - bh * n_tb) * RPB + static_cast<int>(threadIdx.x) / TPR;
+  const int part = static_cast<int>(threadIdx.x) % TPR;
+  const int b = bh / p.Hq, h = bh - b * p.Hq;
+  constexpr int kHalf = RPB / 2;  // a thread's second row is kHalf further
+  uint4 a[2], c[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int t = t0 + i * kHalf;
+    a[i] = c[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (t < p.T) {
+      const size_t row = (static_cast<size_t>(b) * p.T + t) * p.Hq + h;  // memory row of O / dO
+      a[i] = reinterpret_cast<const uint4*>(p.o)[row * TPR + part];
+      c[i] = reinterpret_cast<const uint4*>(p.dO)[row * TPR + part];
+    }
+  }
+  float lse[2] = {0.f, 0.f};
+  if (part == 0) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int t = t0 + i * kHalf;
+      if (t < p.T) lse[i] = p.lse[static_cast<size_t>(bh) * p.T + t];
+    }
   }
 #pragma unroll
-  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (part == 0 && r < nrows) {
-    const size_t idx = static_cast<size_t>(bh) * p.Tpad + t;
-    p.Dvec[idx] = acc;
-    p.lse2[idx] = -p.lse[static_cast<size_t>(r)] * 1.4426950408889634f;
-  }
-  // Zero the padding rows [T, Tpad) of every (b, h).
-  const int pad = p.Tpad - p.T;
-  if (pad > 0) {
-    const long long npad = static_cast<long long>(p.B) * p.Hq * pad;
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long x = gtid; x < npad; x += stride) {
-      const long long pbh = x / pad;
-      const size_t idx = static_cast<size_t>(pbh) * p.Tpad + p.T + static_cast<int>(x % pad);
-      p.Dvec[idx] = 0.f;
-      p.lse2[idx] = 0.f;
+  for (int i = 0; i < 2; ++i) {
+    float acc = bf16lo(a[i].x) * bf16lo(c[i].x);
+    acc = fmaf(bf16hi(a[i].x), bf16hi(c[i].x), acc);
+    acc = fmaf(bf16lo(a[i].y), bf16lo(c[i].y), acc);
+    acc = fmaf(bf16hi(a[i].y), bf16hi(c[i].y), acc);
+    acc = fmaf(bf16lo(a[i].z), bf16lo(c[i].z), acc);
+    acc = fmaf(bf16hi(a[i].z), bf16hi(c[i].z), acc);
+    acc = fmaf(bf16lo(a[i].w), bf16lo(c[i].w), acc);
+    acc = fmaf(bf16hi(a[i].w), bf16hi(c[i].w), acc);
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const int t = t0 + i * kHalf;
+    if (part == 0 && t < p.Tpad) {
+      // rows past T: zeros (acc is 0 there, and so is lse)
+      const size_t idx = static_cast<size_t>(bh) * p.Tpad + t;
+      p.Dvec[idx] = acc;
+      p.lse2[idx] = t < p.T ? -lse[i] * 1.4426950408889634f : 0.f;
     }
   }
 }
@@ -1147,12 +1159,11 @@ cudaError_t ensure_smem_attr(K kernel, int smem, int slot) {
 }  // namespace
 
 cudaError_t launch_bwd_pre(const BwdPreParams& p, int d, cudaStream_t stream) {
-  const long long nrows = static_cast<long long>(p.B) * p.T * p.Hq;
-  const int tpr = d / 8;
-  const long long threads = nrows * tpr;
-  const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
-  cudaError_t e = d == 64 ? launch_pdl(bwd_pre_kernel<64>, grid, 256, 0, stream, p)
-                          : launch_pdl(bwd_pre_kernel<128>, grid, 256, 0, stream, p);
+  const int rpb = d == 64 ? PreCfg<64>::kRows : PreCfg<128>::kRows;
+  const long long n_tb = (p.Tpad + rpb - 1) / rpb;
+  const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.B) * p.Hq * n_tb);
+  cudaError_t e = d == 64 ? launch_pdl(bwd_pre_kernel<64>, grid, kPreThreads, 0, stream, p)
+                          : launch_pdl(bwd_pre_kernel<128>, grid, kPreThreads, 0, stream, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
