@@ -47,6 +47,9 @@ def parse_args():
     ap.add_argument("--workload", default="c2", help="c1..c5 (default c2, the trainer's dev-preset shape)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--layout", default="separate", choices=["separate", "fused"],
+                    help="fused: q, k, v are views of one [B,T,Hq+2*Hkv,d] projection buffer and the gradients "
+                         "go to one such buffer (attn_fwd_strided / attn_bwd_strided)")
     ap.add_argument("--profile-run", action="store_true",
                     help="timed steps only (no clock soak, e2e or oracle leg): the command profiled under ncu")
     return ap.parse_args()
@@ -297,18 +300,52 @@ def run_ours(args, w):
     in_specs = [(x.shape, x.dtype) for x in (q_c, k_c, v_c, do_c)]
     out_specs = [(q_c.shape, torch.bfloat16), ((w.B, w.Hq, w.T), torch.float32), (q_c.shape, torch.bfloat16),
                  (k_c.shape, torch.bfloat16), (v_c.shape, torch.bfloat16)]
-    in_d, (q, k, v, dout) = packed_buffer(torch, in_specs, device=dev)
+    fused = args.layout == "fused"
+    if fused:
+        # one [B,T,Hq+2*Hkv,d] projection buffer in, one gradient buffer of that shape out
+        H3 = w.Hq + 2 * w.Hkv
+        qkv_shape = (w.B, w.T, H3, w.d)
+        in_specs = [(qkv_shape, torch.bfloat16), (do_c.shape, do_c.dtype)]
+        out_specs = [(q_c.shape, torch.bfloat16), ((w.B, w.Hq, w.T), torch.float32), (qkv_shape, torch.bfloat16)]
+    in_d, in_views = packed_buffer(torch, in_specs, device=dev)
     in_h, host_in = packed_buffer(torch, in_specs, pin=True)
-    for dst, src in zip(host_in, (q_c, k_c, v_c, do_c)):
-        dst.copy_(src)
+    if fused:
+        host_in[0][:, :, :w.Hq].copy_(q_c)
+        host_in[0][:, :, w.Hq:w.Hq + w.Hkv].copy_(k_c)
+        host_in[0][:, :, w.Hq + w.Hkv:].copy_(v_c)
+        host_in[1].copy_(do_c)
+    else:
+        for dst, src in zip(host_in, (q_c, k_c, v_c, do_c)):
+            dst.copy_(src)
     in_d.copy_(in_h)
-    out_d, (o, lse, dq, dk, dv) = packed_buffer(torch, out_specs, device=dev)
+    out_d, out_views = packed_buffer(torch, out_specs, device=dev)
+    if fused:
+        qkv, dout = in_views
+        o, lse, dqkv = out_views
+        cut = (slice(0, w.Hq), slice(w.Hq, w.Hq + w.Hkv), slice(w.Hq + w.Hkv, H3))
+        q, k, v = (qkv[:, :, c] for c in cut)
+        dq, dk, dv = (dqkv[:, :, c] for c in cut)
+    else:
+        q, k, v, dout = in_views
+        o, lse, dq, dk, dv = out_views
     ws = torch.empty(gqa.attn_bwd_workspace_bytes(w.B, w.T, w.Hq), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     causal = w.causal
 
     def step(ev=None):
+        if fused:
+            # the strided backward is one call: its preprocess and main kernel share one interval
+            if ev is not None:
+                ev[0].record(stream)
+            gqa.attn_fwd_strided(q, k, v, o, causal=causal, lse=lse, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+                ev[2].record(stream)
+            gqa.attn_bwd_strided(q, k, v, o, lse, dout, dq, dk, dv, causal=causal, workspace=ws, stream=stream)
+            if ev is not None:
+                ev[3].record(stream)
+            return
         if ev is not None:
             ev[0].record(stream)
         gqa.attn_fwd(q, k, v, causal=causal, o=o, lse=lse, stream=stream)
@@ -368,6 +405,9 @@ def run_ours(args, w):
     names = ["attn_fwd_kernel", "bwd_pre_kernel", "bwd_main_kernel"]
     per_kernel = {n: sum(events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps))
                   for j, n in enumerate(names)}
+    if fused:  # one strided backward call: its two kernels are timed as one interval
+        per_kernel = {"attn_fwd_kernel": per_kernel["attn_fwd_kernel"],
+                      "bwd_pre_kernel+bwd_main_kernel": per_kernel["bwd_main_kernel"]}
     step_ms_total = sum(step_ev[i][0].elapsed_time(step_ev[i][1]) for i in range(args.steps))
     step_ms_total = max_over_ranks(torch, dist, step_ms_total, world, dev)
     ms_per_step = step_ms_total / args.steps
@@ -377,7 +417,8 @@ def run_ours(args, w):
     # roofline of the dominant kernel (largest share of the step)
     pairs = causal_pairs(w.T, w.causal)
     mm = 2.0 * w.B * w.Hq * pairs * w.d  # one causal matmul over all heads
-    kflops = {"attn_fwd_kernel": 2 * mm, "bwd_main_kernel": 7 * mm}  # dQ tasks 3 matmuls, dK/dV tasks 4
+    kflops = {"attn_fwd_kernel": 2 * mm, "bwd_main_kernel": 7 * mm,  # dQ tasks 3 matmuls, dK/dV tasks 4
+              "bwd_pre_kernel+bwd_main_kernel": 7 * mm}
     pre_bytes = 2 * w.B * w.T * w.Hq * w.d * 2 + w.B * w.Hq * w.T * 4 + 2 * w.B * w.Hq * w.T * 4
     dom = max(per_kernel, key=per_kernel.get)
     avg_ms = per_kernel[dom] / args.steps
@@ -390,8 +431,10 @@ def run_ours(args, w):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_src} burst" if roof["bound"] == "tensor" else peak_src
-    roof["traffic"] = recorded_traffic(dom, w.name)
-    kernel_ms = {n: per_kernel[n] / args.steps for n in names}
+    roof["traffic"] = None if fused else recorded_traffic(dom, w.name)
+    kernel_ms = {n: t / args.steps for n, t in per_kernel.items()}
+    bwd_ms = kernel_ms["bwd_pre_kernel+bwd_main_kernel"] if fused else (
+        kernel_ms["bwd_pre_kernel"] + kernel_ms["bwd_main_kernel"])
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     out_h, _ = packed_buffer(torch, out_specs, pin=True)
@@ -400,8 +443,12 @@ def run_ours(args, w):
 
     def e2e_step():
         in_d.copy_(in_h, non_blocking=True)
-        gqa.attn_fwd(q, k, v, causal=causal, o=o, lse=lse, stream=stream)
-        gqa.attn_bwd(q, k, v, o, lse, dout, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+        if fused:
+            gqa.attn_fwd_strided(q, k, v, o, causal=causal, lse=lse, stream=stream)
+            gqa.attn_bwd_strided(q, k, v, o, lse, dout, dq, dk, dv, causal=causal, workspace=ws, stream=stream)
+        else:
+            gqa.attn_fwd(q, k, v, causal=causal, o=o, lse=lse, stream=stream)
+            gqa.attn_bwd(q, k, v, o, lse, dout, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
         out_h.copy_(out_d, non_blocking=True)
 
     for _ in range(0 if args.profile_run else 3):
@@ -431,12 +478,13 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_dict(w, {"l2": "flushed between timed steps (256 MB write, outside the events)",
+                                      "layout": "fused qkv / dqkv buffers, strided views" if fused
+                                      else "separate contiguous q, k, v, dq, dk, dv",
                                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
             "pct_of_peak": 100.0 * per_gpu / peaks["bf16_tflops"],
             "peak_tflops": peaks["bf16_tflops"], "peak_source": f"{peak_src} burst",
             "fwd_tflops": fwd_flops(w) / (kernel_ms["attn_fwd_kernel"] * 1e-3) / 1e12,
-            "bwd_tflops": 2.5 * fwd_flops(w) / ((kernel_ms["bwd_pre_kernel"] + kernel_ms["bwd_main_kernel"]) * 1e-3)
-            / 1e12,
+            "bwd_tflops": 2.5 * fwd_flops(w) / (bwd_ms * 1e-3) / 1e12,
             "kernel_ms": kernel_ms,
             "roofline": roof,
             "cpu_baseline": cpu,

@@ -14,11 +14,12 @@ import os
 from ._build import build, library_path
 
 __all__ = [
-    "AttnError", "build", "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
+    "AttnError", "build", "library_path", "load", "attn_fwd", "attn_bwd", "attn_fwd_strided", "attn_bwd_strided",
+    "attn_bwd_workspace_bytes",
     "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_dq_dkv", "attn_bwd_noalloc",
     "NOALLOC_SCRATCH_BYTES",
     "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_last_error", "attn_version",
-    "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
+    "GqaView", "view_of", "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
     "GQA_ERR_TIMEOUT",
 ]
 
@@ -32,11 +33,16 @@ NOALLOC_SCRATCH_BYTES = 8 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_attn
 # Every function include/gqa_attn.h declares.
 EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv",
-    "attn_bwd_dq_dkv", "attn_bwd_noalloc", "attn_last_error", "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns",
-    "attn_version",
+    "attn_bwd_dq_dkv", "attn_bwd_noalloc", "attn_fwd_strided", "attn_bwd_strided", "attn_last_error",
+    "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_version",
 )
 
 _lib = None
+
+
+class GqaView(ctypes.Structure):
+    """gqa_view_t: a bf16 [B, T, H, d] tensor with packed heads and free token / batch strides (elements)."""
+    _fields_ = [("ptr", ctypes.c_void_p), ("stride_t", ctypes.c_longlong), ("stride_b", ctypes.c_longlong)]
 
 
 class AttnError(RuntimeError):
@@ -71,6 +77,11 @@ def load():
     lib.attn_bwd_dq_dkv.restype = i
     lib.attn_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, i, i, vp]
     lib.attn_bwd_noalloc.restype = i
+    gv = GqaView
+    lib.attn_fwd_strided.argtypes = [gv, gv, gv, gv, vp, i, i, i, i, i, i, vp]
+    lib.attn_fwd_strided.restype = i
+    lib.attn_bwd_strided.argtypes = [gv, gv, gv, gv, vp, gv, gv, gv, gv, vp, sz, i, i, i, i, i, i, vp]
+    lib.attn_bwd_strided.restype = i
     lib.attn_last_error.argtypes = []
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_sync_status.argtypes = [vp]
@@ -135,6 +146,46 @@ def attn_fwd(q, k, v, causal: bool = True, o=None, lse=None, stream=None):
     _check(lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, T, Hq, Hkv, d, int(bool(causal)),
                         _stream_handle(stream)))
     return o, lse
+
+
+def view_of(t, name: str = "tensor") -> GqaView:
+    """The gqa_view_t of a bf16 CUDA tensor [B, T, H, d] whose heads are packed
+    (stride(3) == 1, stride(2) == d); token and batch strides are passed as they are."""
+    import torch
+    if t.dim() != 4 or t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise ValueError(f"{name} must be a bf16 CUDA tensor [B, T, H, d]")
+    B, T, H, d = t.shape
+    if t.stride(3) != 1 or (H > 1 and t.stride(2) != d):
+        raise ValueError(f"{name}: the heads of a token must be packed (strides {tuple(t.stride())})")
+    return GqaView(t.data_ptr(), t.stride(1), t.stride(0))
+
+
+def attn_fwd_strided(q, k, v, o, causal: bool = True, lse=None, stream=None):
+    """attn_fwd over strided views, e.g. q, k, v sliced out of one fused [B, T, Hq+2*Hkv, d]
+    projection; o (a view too) is written in place. Returns (o, lse)."""
+    import torch
+    lib = load()
+    B, T, Hq, Hkv, d = _dims(q, k)
+    if lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    _check(lib.attn_fwd_strided(view_of(q, "q"), view_of(k, "k"), view_of(v, "v"), view_of(o, "o"), _ptr(lse), B, T,
+                                Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
+    return o, lse
+
+
+def attn_bwd_strided(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = True, workspace=None, stream=None):
+    """attn_bwd over strided views; dq, dk, dv (views too, e.g. of one fused gradient
+    buffer) are written in place. Returns (dq, dk, dv)."""
+    import torch
+    lib = load()
+    B, T, Hq, Hkv, d = _dims(q, k)
+    if workspace is None:
+        workspace = torch.empty(attn_bwd_workspace_bytes(B, T, Hq), dtype=torch.uint8, device=q.device)
+    _check(lib.attn_bwd_strided(view_of(q, "q"), view_of(k, "k"), view_of(v, "v"), view_of(o, "o"), _ptr(lse),
+                                view_of(dout, "dO"), view_of(dq, "dq"), view_of(dk, "dk"), view_of(dv, "dv"),
+                                _ptr(workspace), _ws_bytes(workspace), B, T, Hq, Hkv, d, int(bool(causal)),
+                                _stream_handle(stream)))
+    return dq, dk, dv
 
 
 def attn_bwd_workspace_bytes(B: int, T: int, Hq: int) -> int:

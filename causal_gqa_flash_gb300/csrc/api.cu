@@ -143,13 +143,51 @@ gqa_status_t check_ptr(const char* fn, const char* name, const void* p) {
   return GQA_OK;
 }
 
-// 4D tiled map over a [B, T, H, d] bf16 tensor: box = box_c (d) x 1 (head) x box_rows x 1 (batch),
+// A bf16 [B, T, H, d] tensor with packed heads: element (b, t, h, c) at
+// ptr + b*sb + t*st + h*d + c (elements).
+struct View {
+  const void* ptr;
+  long long st, sb;
+};
+
+View packed(const void* ptr, int T, int H, int d) {
+  return View{ptr, (long long)H * d, (long long)T * H * d};
+}
+
+// Checks a caller's strided view (see gqa_view_t) and fills `out`; strides of a
+// dimension of size 1 are replaced by the packed ones, since they are never used.
+gqa_status_t check_view(const char* fn, const char* name, const gqa_view_t& v, int B, int T, int H, int d,
+                        bool output, View* out) {
+  gqa_status_t s;
+  if ((s = check_ptr(fn, name, v.ptr))) return s;
+  const long long row = (long long)H * d;
+  long long st = T == 1 ? row : v.stride_t;
+  long long sb = B == 1 ? st * T : v.stride_b;
+  const long long kMax = 1LL << 39;
+  for (long long x : {st, sb})
+    if (x <= 0 || x % 8 != 0 || x >= kMax)
+      return fail(GQA_ERR_INVALID_ARG,
+                  "%s: %s strides (t %lld, b %lld) must be positive multiples of 8 elements below 2^39", fn, name,
+                  v.stride_t, v.stride_b);
+  if (output) {
+    const bool t_major = st >= row && sb >= st * T;  // [B, T, H, d]-like
+    const bool b_major = sb >= row && st >= sb * B;  // [T, B, H, d]-like
+    if (!t_major && !b_major)
+      return fail(GQA_ERR_INVALID_ARG, "%s: output %s overlaps itself (stride_t %lld, stride_b %lld, H*d %lld)", fn,
+                  name, v.stride_t, v.stride_b, row);
+  }
+  *out = View{v.ptr, st, sb};
+  return GQA_OK;
+}
+
+// 4D tiled map over a [B, T, H, d] bf16 view: box = box_c (d) x 1 (head) x box_rows x 1 (batch),
 // swizzled over the box's inner bytes (box_c = 64: 128-byte swizzle, 32: 64-byte, 16: 32-byte);
 // loads read rows past T as zero, stores skip them. The operand loads use 64 x 128 boxes.
-gqa_status_t make_map(const char* fn, const char* name, CUtensorMap* m, const void* ptr, int B, int T, int H,
+gqa_status_t make_map(const char* fn, const char* name, CUtensorMap* m, const View& t, int B, int T, int H,
                       int d, int box_c = 64, int box_rows = kTile) {
+  const void* ptr = t.ptr;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)T * H * d * 2};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)t.st * 2, (cuuint64_t)t.sb * 2};
   cuuint32_t box[4] = {(cuuint32_t)box_c, 1, (cuuint32_t)box_rows, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   const CUtensorMapSwizzle swz = box_c == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
@@ -183,15 +221,14 @@ size_t attn_bwd_workspace_bytes(int B, int T, int Hq) {
   return 2 * (size_t)B * (size_t)Hq * round_up_tile(T) * sizeof(float) + kSchedBytes;
 }
 
-gqa_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int Hq,
-                      int Hkv, int d, int causal, void* stream) {
-  const char* fn = "attn_fwd";
-  t_last_error.clear();
+}  // extern "C"
+
+namespace {
+
+// Shape, pointers and views already checked.
+gqa_status_t fwd_impl(const char* fn, const View& q, const View& k, const View& v, const View& o, float* lse, int B,
+                      int T, int Hq, int Hkv, int d, int causal, cudaStream_t stream) {
   gqa_status_t s;
-  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
-  if ((s = check_ptr(fn, "q", q)) || (s = check_ptr(fn, "k", k)) || (s = check_ptr(fn, "v", v)) ||
-      (s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)))
-    return s;
   DeviceState* ds = nullptr;
   if ((s = device_state(fn, &ds))) return s;
   FwdParams p;
@@ -200,7 +237,6 @@ gqa_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, floa
       (s = make_map(fn, "v", &p.tmap_v, v, B, T, Hkv, d)))
     return s;
   if ((s = make_map(fn, "o", &p.tmap_o, o, B, T, Hq, d, 64, 32))) return s;  // epilogue stores (32-row boxes)
-  p.o = o;
   p.lse = lse;
   p.B = B;
   p.T = T;
@@ -212,9 +248,40 @@ gqa_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, floa
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
   p.status = ds->status;
   p.budget_ns = g_budget_ns.load();
-  cudaError_t e = launch_fwd(p, d, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_fwd(p, d, stream);
   if (e != cudaSuccess) return cuda_fail(fn, "kernel launch", e);
   return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T, int Hq,
+                      int Hkv, int d, int causal, void* stream) {
+  const char* fn = "attn_fwd";
+  t_last_error.clear();
+  gqa_status_t s;
+  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
+  if ((s = check_ptr(fn, "q", q)) || (s = check_ptr(fn, "k", k)) || (s = check_ptr(fn, "v", v)) ||
+      (s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)))
+    return s;
+  return fwd_impl(fn, packed(q, T, Hq, d), packed(k, T, Hkv, d), packed(v, T, Hkv, d), packed(o, T, Hq, d), lse, B,
+                  T, Hq, Hkv, d, causal, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t attn_fwd_strided(gqa_view_t q, gqa_view_t k, gqa_view_t v, gqa_view_t o, float* lse, int B, int T,
+                              int Hq, int Hkv, int d, int causal, void* stream) {
+  const char* fn = "attn_fwd_strided";
+  t_last_error.clear();
+  gqa_status_t s;
+  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
+  View vq, vk, vv, vo;
+  if ((s = check_view(fn, "q", q, B, T, Hq, d, false, &vq)) || (s = check_view(fn, "k", k, B, T, Hkv, d, false, &vk)) ||
+      (s = check_view(fn, "v", v, B, T, Hkv, d, false, &vv)) || (s = check_view(fn, "o", o, B, T, Hq, d, true, &vo)) ||
+      (s = check_ptr(fn, "lse", lse)))
+    return s;
+  return fwd_impl(fn, vq, vk, vv, vo, lse, B, T, Hq, Hkv, d, causal, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
@@ -237,8 +304,8 @@ gqa_status_t check_workspace(const char* fn, const void* workspace, size_t works
 }
 
 // Parameters of the dQ and dK/dV kernels (shape, pointers and tensor maps already checked by the caller).
-gqa_status_t make_bwd_params(const char* fn, BwdParams* p, const void* q, const void* k, const void* v,
-                             const void* dO, float* Dvec, float* lse2, unsigned* sched, int Tpad, int B, int T,
+gqa_status_t make_bwd_params(const char* fn, BwdParams* p, const View& q, const View& k, const View& v,
+                             const View& dO, float* Dvec, float* lse2, unsigned* sched, int Tpad, int B, int T,
                              int Hq, int Hkv,
                              int d, int causal, DeviceState* ds) {
   memset(p, 0, sizeof(*p));
@@ -265,11 +332,10 @@ gqa_status_t make_bwd_params(const char* fn, BwdParams* p, const void* q, const 
   return GQA_OK;
 }
 
-gqa_status_t bwd_preprocess_impl(const char* fn, const void* o, const float* lse, const void* dO, void* workspace,
+// Shape and pointers of o, lse, dO already checked.
+gqa_status_t bwd_preprocess_impl(const char* fn, const View& o, const float* lse, const View& dO, void* workspace,
                                  size_t workspace_bytes, int B, int T, int Hq, int d, cudaStream_t st) {
   gqa_status_t s;
-  if ((s = check_shape(fn, B, T, Hq, 1, d))) return s;
-  if ((s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)) || (s = check_ptr(fn, "dO", dO))) return s;
   float *Dvec, *lse2;
   unsigned* sched;
   int Tpad;
@@ -277,8 +343,12 @@ gqa_status_t bwd_preprocess_impl(const char* fn, const void* o, const float* lse
   DeviceState* ds = nullptr;
   if ((s = device_state(fn, &ds))) return s;
   BwdPreParams pp;
-  pp.o = o;
-  pp.dO = dO;
+  pp.o = o.ptr;
+  pp.dO = dO.ptr;
+  pp.o_st = o.st;
+  pp.o_sb = o.sb;
+  pp.do_st = dO.st;
+  pp.do_sb = dO.sb;
   pp.lse = lse;
   pp.Dvec = Dvec;
   pp.lse2 = lse2;
@@ -292,17 +362,12 @@ gqa_status_t bwd_preprocess_impl(const char* fn, const void* o, const float* lse
   return GQA_OK;
 }
 
-// which: 1 = dQ tasks, 2 = dK/dV tasks, 3 = both (one launch)
-gqa_status_t bwd_main_impl(const char* fn, int which, const void* q, const void* k, const void* v, const void* dO,
-                           void* dq, void* dk, void* dv, const void* workspace, size_t workspace_bytes, int B, int T,
-                           int Hq, int Hkv, int d, int causal, cudaStream_t st) {
+// which: 1 = dQ tasks, 2 = dK/dV tasks, 3 = both (one launch). Shape and the
+// pointers of the views it uses already checked.
+gqa_status_t bwd_main_impl(const char* fn, int which, const View& q, const View& k, const View& v, const View& dO,
+                           const View& dq, const View& dk, const View& dv, const void* workspace,
+                           size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, int causal, cudaStream_t st) {
   gqa_status_t s;
-  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
-  if ((s = check_ptr(fn, "q", q)) || (s = check_ptr(fn, "k", k)) || (s = check_ptr(fn, "v", v)) ||
-      (s = check_ptr(fn, "dO", dO)))
-    return s;
-  if ((which & 1) && (s = check_ptr(fn, "dq", dq))) return s;
-  if ((which & 2) && ((s = check_ptr(fn, "dk", dk)) || (s = check_ptr(fn, "dv", dv)))) return s;
   float *Dvec, *lse2;
   unsigned* sched;
   int Tpad;
@@ -311,9 +376,15 @@ gqa_status_t bwd_main_impl(const char* fn, int which, const void* q, const void*
   if ((s = device_state(fn, &ds))) return s;
   BwdParams p;
   if ((s = make_bwd_params(fn, &p, q, k, v, dO, Dvec, lse2, sched, Tpad, B, T, Hq, Hkv, d, causal, ds))) return s;
-  p.dq = dq;
-  p.dk = dk;
-  p.dv = dv;
+  p.dq = const_cast<void*>(dq.ptr);
+  p.dk = const_cast<void*>(dk.ptr);
+  p.dv = const_cast<void*>(dv.ptr);
+  p.dq_st = dq.st;
+  p.dq_sb = dq.sb;
+  p.dk_st = dk.st;
+  p.dk_sb = dk.sb;
+  p.dv_st = dv.st;
+  p.dv_sb = dv.sb;
   if (d == 64) {
     // d = 64 epilogues store through TMA, one 32-row box per compute warp: dQ 16
     // columns of a warpgroup, dK / dV 32 columns.
@@ -335,39 +406,41 @@ extern "C" {
 
 gqa_status_t attn_bwd_preprocess(const void* o, const float* lse, const void* dO, void* workspace,
                                  size_t workspace_bytes, int B, int T, int Hq, int d, void* stream) {
-  t_last_error.clear();
-  return bwd_preprocess_impl("attn_bwd_preprocess", o, lse, dO, workspace, workspace_bytes, B, T, Hq, d,
-                             static_cast<cudaStream_t>(stream));
-}
-
-gqa_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
-                         const void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
-                         int causal, void* stream) {
-  t_last_error.clear();
-  return bwd_main_impl("attn_bwd_dq", 1, q, k, v, dO, dq, nullptr, nullptr, workspace, workspace_bytes, B, T, Hq,
-                       Hkv, d, causal, static_cast<cudaStream_t>(stream));
-}
-
-gqa_status_t attn_bwd_dkv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
-                          const void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
-                          int causal, void* stream) {
-  t_last_error.clear();
-  return bwd_main_impl("attn_bwd_dkv", 2, q, k, v, dO, nullptr, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv,
-                       d, causal, static_cast<cudaStream_t>(stream));
-}
-
-gqa_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
-                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int T, int Hq,
-                      int Hkv, int d, int causal, void* stream) {
-  const char* fn = "attn_bwd";
+  const char* fn = "attn_bwd_preprocess";
   t_last_error.clear();
   gqa_status_t s;
-  // Validate everything before the first launch.
+  if ((s = check_shape(fn, B, T, Hq, 1, d))) return s;
+  if ((s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)) || (s = check_ptr(fn, "dO", dO))) return s;
+  return bwd_preprocess_impl(fn, packed(o, T, Hq, d), lse, packed(dO, T, Hq, d), workspace, workspace_bytes, B, T,
+                             Hq, d, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace {
+
+// attn_bwd_dq, attn_bwd_dkv and attn_bwd_dq_dkv on contiguous tensors.
+gqa_status_t bwd_stage(const char* fn, int which, const void* q, const void* k, const void* v, const void* dO,
+                       void* dq, void* dk, void* dv, const void* workspace, size_t workspace_bytes, int B, int T,
+                       int Hq, int Hkv, int d, int causal, void* stream) {
+  t_last_error.clear();
+  gqa_status_t s;
   if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
   if ((s = check_ptr(fn, "q", q)) || (s = check_ptr(fn, "k", k)) || (s = check_ptr(fn, "v", v)) ||
-      (s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)) || (s = check_ptr(fn, "dO", dO)) ||
-      (s = check_ptr(fn, "dq", dq)) || (s = check_ptr(fn, "dk", dk)) || (s = check_ptr(fn, "dv", dv)))
+      (s = check_ptr(fn, "dO", dO)))
     return s;
+  if ((which & 1) && (s = check_ptr(fn, "dq", dq))) return s;
+  if ((which & 2) && ((s = check_ptr(fn, "dk", dk)) || (s = check_ptr(fn, "dv", dv)))) return s;
+  return bwd_main_impl(fn, which, packed(q, T, Hq, d), packed(k, T, Hkv, d), packed(v, T, Hkv, d),
+                       packed(dO, T, Hq, d), packed(dq, T, Hq, d), packed(dk, T, Hkv, d), packed(dv, T, Hkv, d),
+                       workspace, workspace_bytes, B, T, Hq, Hkv, d, causal, static_cast<cudaStream_t>(stream));
+}
+
+// The whole backward on checked views: everything is validated before the first launch.
+gqa_status_t bwd_impl(const char* fn, const View& q, const View& k, const View& v, const View& o, const float* lse,
+                      const View& dO, const View& dq, const View& dk, const View& dv, void* workspace,
+                      size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, int causal, void* stream) {
+  gqa_status_t s;
   float *Dvec, *lse2;
   unsigned* sched;
   int Tpad;
@@ -377,12 +450,65 @@ gqa_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o
   return bwd_main_impl(fn, 3, q, k, v, dO, dq, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv, d, causal, st);
 }
 
+}  // namespace
+
+extern "C" {
+
+gqa_status_t attn_bwd_dq(const void* q, const void* k, const void* v, const void* dO, void* dq,
+                         const void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                         int causal, void* stream) {
+  return bwd_stage("attn_bwd_dq", 1, q, k, v, dO, dq, nullptr, nullptr, workspace, workspace_bytes, B, T, Hq, Hkv,
+                   d, causal, stream);
+}
+
+gqa_status_t attn_bwd_dkv(const void* q, const void* k, const void* v, const void* dO, void* dk, void* dv,
+                          const void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d,
+                          int causal, void* stream) {
+  return bwd_stage("attn_bwd_dkv", 2, q, k, v, dO, nullptr, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv, d,
+                   causal, stream);
+}
+
 gqa_status_t attn_bwd_dq_dkv(const void* q, const void* k, const void* v, const void* dO, void* dq, void* dk,
                              void* dv, const void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv,
                              int d, int causal, void* stream) {
+  return bwd_stage("attn_bwd_dq_dkv", 3, q, k, v, dO, dq, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv, d,
+                   causal, stream);
+}
+
+gqa_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int T, int Hq,
+                      int Hkv, int d, int causal, void* stream) {
+  const char* fn = "attn_bwd";
   t_last_error.clear();
-  return bwd_main_impl("attn_bwd_dq_dkv", 3, q, k, v, dO, dq, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv, d,
-                       causal, static_cast<cudaStream_t>(stream));
+  gqa_status_t s;
+  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
+  if ((s = check_ptr(fn, "q", q)) || (s = check_ptr(fn, "k", k)) || (s = check_ptr(fn, "v", v)) ||
+      (s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)) || (s = check_ptr(fn, "dO", dO)) ||
+      (s = check_ptr(fn, "dq", dq)) || (s = check_ptr(fn, "dk", dk)) || (s = check_ptr(fn, "dv", dv)))
+    return s;
+  return bwd_impl(fn, packed(q, T, Hq, d), packed(k, T, Hkv, d), packed(v, T, Hkv, d), packed(o, T, Hq, d), lse,
+                  packed(dO, T, Hq, d), packed(dq, T, Hq, d), packed(dk, T, Hkv, d), packed(dv, T, Hkv, d), workspace,
+                  workspace_bytes, B, T, Hq, Hkv, d, causal, stream);
+}
+
+gqa_status_t attn_bwd_strided(gqa_view_t q, gqa_view_t k, gqa_view_t v, gqa_view_t o, const float* lse,
+                              gqa_view_t dO, gqa_view_t dq, gqa_view_t dk, gqa_view_t dv, void* workspace,
+                              size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, int causal,
+                              void* stream) {
+  const char* fn = "attn_bwd_strided";
+  t_last_error.clear();
+  gqa_status_t s;
+  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
+  View vq, vk, vv, vo, vdo, vdq, vdk, vdv;
+  if ((s = check_view(fn, "q", q, B, T, Hq, d, false, &vq)) || (s = check_view(fn, "k", k, B, T, Hkv, d, false, &vk)) ||
+      (s = check_view(fn, "v", v, B, T, Hkv, d, false, &vv)) || (s = check_view(fn, "o", o, B, T, Hq, d, false, &vo)) ||
+      (s = check_ptr(fn, "lse", lse)) || (s = check_view(fn, "dO", dO, B, T, Hq, d, false, &vdo)) ||
+      (s = check_view(fn, "dq", dq, B, T, Hq, d, true, &vdq)) ||
+      (s = check_view(fn, "dk", dk, B, T, Hkv, d, true, &vdk)) ||
+      (s = check_view(fn, "dv", dv, B, T, Hkv, d, true, &vdv)))
+    return s;
+  return bwd_impl(fn, vq, vk, vv, vo, lse, vdo, vdq, vdk, vdv, workspace, workspace_bytes, B, T, Hq, Hkv, d, causal,
+                  stream);
 }
 
 gqa_status_t attn_sync_status(void* stream) {

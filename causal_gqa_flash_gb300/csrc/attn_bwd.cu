@@ -43,10 +43,11 @@ __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x &
 
 // ============================================================================
 // Preprocess: D = rowsum(dO * O), -LSE2 = -LSE * log2(e); padded rows get 0.
-// A block covers kPreRows consecutive rows t of one (b, h), a row being read as
-// D/8 16-byte chunks by as many threads (each thread takes two rows, so four
-// loads are in flight), so the block's rows of D / -LSE2 are consecutive in
-// memory; the rows [T, Tpad) of the last block are written as zeros.
+// A block covers PreCfg<D>::kRows consecutive rows t of one (b, h), a row being
+// read as D/8 16-byte chunks by as many threads (each thread takes two rows, so
+// four loads are in flight; O and dO are addressed through their token and batch
+// strides), so the block's rows of D / -LSE2 are consecutive in memory; the rows
+// [T, Tpad) of the last block are written as zeros.
 // ============================================================================
 constexpr int kPreThreads = 256;
 
@@ -78,9 +79,11 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const BwdPreParams
     const int t = t0 + i * kHalf;
     a[i] = c[i] = make_uint4(0u, 0u, 0u, 0u);
     if (t < p.T) {
-      const size_t row = (static_cast<size_t>(b) * p.T + t) * p.Hq + h;  // memory row of O / dO
-      a[i] = reinterpret_cast<const uint4*>(p.o)[row * TPR + part];
-      c[i] = reinterpret_cast<const uint4*>(p.dO)[row * TPR + part];
+      // element offsets of row (b, t, h) of O and dO: multiples of 8 (16 bytes)
+      const long long eo = b * p.o_sb + t * p.o_st + h * D;
+      const long long ed = b * p.do_sb + t * p.do_st + h * D;
+      a[i] = reinterpret_cast<const uint4*>(p.o)[(eo >> 3) + part];
+      c[i] = reinterpret_cast<const uint4*>(p.dO)[(ed >> 3) + part];
     }
   }
   float lse[2] = {0.f, 0.f};
@@ -996,7 +999,8 @@ __device__ __forceinline__ bool compute_epilogue(const BwdParams& p, MainBars& b
     }
     const int k_idx = t.tile * kTile + row;
     if (k_idx < p.T) {
-      const size_t off = ((static_cast<size_t>(t.b) * p.T + k_idx) * p.Hkv + t.kvh) * D + part * NC;
+      const long long st = wg < 2 ? p.dv_st : p.dk_st, sb = wg < 2 ? p.dv_sb : p.dk_sb;
+      const long long off = t.b * sb + k_idx * st + t.kvh * D + part * NC;
       store_acc_bf16<NC>(r, reinterpret_cast<__nv_bfloat16*>(wg < 2 ? p.dv : p.dk) + off, wg < 2 ? 1.f : p.scale);
     }
   } else {
@@ -1013,7 +1017,7 @@ __device__ __forceinline__ bool compute_epilogue(const BwdParams& p, MainBars& b
     }
     const int q_idx = t.tile * kTile + row;
     if (q_idx < p.T) {
-      const size_t off = ((static_cast<size_t>(t.b) * p.T + q_idx) * p.Hq + t.h) * D + wg * NC;
+      const long long off = t.b * p.dq_sb + q_idx * p.dq_st + t.h * D + wg * NC;
       store_acc_bf16<NC>(r, reinterpret_cast<__nv_bfloat16*>(p.dq) + off, p.scale);
     }
   }

@@ -25,12 +25,13 @@ enum KernelId : unsigned int {
 };
 
 // Forward: work items of one 128-query tile of one (query head, batch).
+// Tensors [B,T,H,d] bf16 are reached through TMA maps or through element strides
+// (token, batch) with the heads of one token packed (head stride d).
 struct FwdParams {
   CUtensorMap tmap_q;  // [B,T,Hq,d] bf16, box 64 x 1 x 128 x 1, 128B swizzle
   CUtensorMap tmap_k;  // [B,T,Hkv,d]
   CUtensorMap tmap_v;  // [B,T,Hkv,d]
   CUtensorMap tmap_o;  // [B,T,Hq,d], box 64 x 1 x 32 x 1 (epilogue stores)
-  void* o;             // [B,T,Hq,d] bf16
   float* lse;          // [B,Hq,T] fp32, natural log
   int B, T, Hq, Hkv, G, nT;
   int causal;
@@ -41,8 +42,10 @@ struct FwdParams {
 
 // Backward preprocess: D = rowsum(dO * O), LSE2 = LSE * log2(e), both [B,Hq,Tpad].
 struct BwdPreParams {
-  const void* o;
-  const void* dO;
+  const void* o;             // [B,T,Hq,d] bf16
+  const void* dO;            // [B,T,Hq,d] bf16
+  long long o_st, o_sb;      // element strides of O between tokens / batch entries (multiples of 8)
+  long long do_st, do_sb;    // the same for dO
   const float* lse;
   float* Dvec;   // [B,Hq,Tpad]
   float* lse2;   // [B,Hq,Tpad]
@@ -65,6 +68,7 @@ struct BwdParams {
   void* dq;            // [B,T,Hq,d]
   void* dk;            // [B,T,Hkv,d]
   void* dv;            // [B,T,Hkv,d]
+  long long dq_st, dq_sb, dk_st, dk_sb, dv_st, dv_sb;  // element strides (token, batch) of the outputs
   int B, T, Hq, Hkv, G, nT, Tpad;
   int causal;
   int n_dkv_tasks;     // tasks [0, n_dkv_tasks) compute dK/dV (0 = none)

@@ -70,6 +70,7 @@ struct FwdCfg {
   static constexpr bool kPersistent = (D == 64);
   static constexpr int kMaxRounds = kPersistent ? 0x7fffffff : 1;
   static_assert(kTmaStore || !kPersistent, "only the staged epilogue releases O for a next item");
+  static_assert(kTmaStore || kStageInQ, "O leaves through TMA stores");
   static constexpr int kOffOut = kOffV + kVStages * kTileBytes;
   static constexpr int kOutBytes = kTmaStore ? 4 * 32 * 128 : 0;
   static constexpr int kSmemBytes = kOffOut + kOutBytes + 1024;  // + alignment slack
@@ -472,26 +473,6 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
           tma_store_4d(&p.tmap_o, stg + 4096, 64, it.h, r0, it.b);
           tma_store_commit();
         }
-      } else {
-        // 32 columns at a time straight to memory
-        uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
-                                               ((static_cast<size_t>(it.b) * p.T + (valid ? q_idx : 0)) * p.Hq + it.h) * D);
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t rr[32];
-          tmem_ld32(tO + cc * 32, rr);
-          tmem_wait_ld();
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l, __uint_as_float(rr[2 * i + 1]) * inv_l);
-          if (valid) {
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) orow[cc * 4 + v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
-          }
-        }
-        // one item per CTA: no next item waits for O (and an arrive queued behind
-        // these stores would hold the warp until they drain)
       }
       if (valid)
         p.lse[(static_cast<size_t>(it.b) * p.Hq + it.h) * p.T + q_idx] = (m_used + log2f(l)) * 0.69314718055994531f;

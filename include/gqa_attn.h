@@ -16,7 +16,8 @@
  *    one order, so repeated calls give identical bits.
  *
  * Conventions shared by every entry point:
- *  - Tensors are device pointers, row-major, contiguous, 16-byte aligned:
+ *  - Tensors are device pointers, row-major, contiguous, 16-byte aligned
+ *    (the *_strided entry points take views with free token and batch strides):
  *      q, o, dO, dq     bf16 [B, T, Hq,  d]
  *      k, v, dk, dv     bf16 [B, T, Hkv, d]
  *      lse              fp32 [B, Hq, T]   natural-log log-sum-exp of each query row
@@ -136,6 +137,46 @@ gqa_status_t attn_bwd_dq_dkv(const void* q, const void* k, const void* v, const 
 gqa_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                               const void* dO, void* dq, void* dk, void* dv, int B, int T, int Hq, int Hkv, int d,
                               int causal, void* stream);
+
+/*
+ * Strided views ("A transformer in PTX", §The model: one fused matmul computes
+ * the queries, keys and values of a layer into one buffer, which attention
+ * reads, and attention's output is the input of the output projection).
+ *
+ * A gqa_view_t describes a bf16 [B, T, H, d] tensor whose element (b, t, h, c)
+ * lives at ptr + b*stride_b + t*stride_t + h*d + c (counted in elements): the
+ * H heads of one token are packed, while the token and batch strides are free.
+ * So q, k and v can be the three parts of a fused [B, T, Hq + 2*Hkv, d]
+ * projection (stride_t = (Hq + 2*Hkv)*d; k starting at head Hq, v at head
+ * Hq + Hkv), a sequence-first [T, B, H, d] tensor can be read in place
+ * (stride_b = H*d, stride_t = B*H*d), and o or the gradients can be written
+ * into parts of wider buffers.
+ *  - ptr: device pointer, 16-byte aligned.
+ *  - stride_t, stride_b: positive multiples of 8 elements (16 bytes), below
+ *    2^39. A stride whose dimension has size 1 is not used (T == 1: stride_t;
+ *    B == 1: stride_b) and may hold any value.
+ *  - An output view must not overlap itself: either stride_t >= H*d and
+ *    stride_b >= T*stride_t, or stride_b >= H*d and stride_t >= B*stride_b
+ *    (checked). Outputs must not overlap each other or an input (not checked).
+ * Results are bit-identical to those of the same tensors stored contiguously.
+ */
+typedef struct gqa_view {
+  void* ptr;
+  long long stride_t;
+  long long stride_b;
+} gqa_view_t;
+
+/* attn_fwd over views: q [B,T,Hq,d], k/v [B,T,Hkv,d] in, o [B,T,Hq,d] out;
+ * lse [B,Hq,T] fp32 contiguous as in attn_fwd. */
+gqa_status_t attn_fwd_strided(gqa_view_t q, gqa_view_t k, gqa_view_t v, gqa_view_t o, float* lse, int B, int T,
+                              int Hq, int Hkv, int d, int causal, void* stream);
+
+/* attn_bwd over views: q, k, v, o, dO in; dq [B,T,Hq,d], dk/dv [B,T,Hkv,d] out;
+ * lse and the workspace as in attn_bwd. */
+gqa_status_t attn_bwd_strided(gqa_view_t q, gqa_view_t k, gqa_view_t v, gqa_view_t o, const float* lse,
+                              gqa_view_t dO, gqa_view_t dq, gqa_view_t dk, gqa_view_t dv, void* workspace,
+                              size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, int causal,
+                              void* stream);
 
 /* Description of the last error returned on this host thread ("" if none). */
 const char* attn_last_error(void);

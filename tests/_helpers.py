@@ -63,3 +63,18 @@ class Guarded:
         head = self.raw[:GUARD]
         tail = self.raw[GUARD + self.n:]
         return bool((head == 0xA5).all().item()) and bool((tail == 0xA5).all().item())
+
+
+def check_against_oracle(out, ref, label):
+    o, lse = f64(out["o"]), f64(out["lse"])
+    e_o, e_l = o_err(o, ref["o"]), max_abs(lse, ref["lse"])
+    raw_o = max_abs(o, ref["o"])
+    e_dq = rel_fro(f64(out["dq"]), ref["dq"])
+    e_dk = rel_fro(f64(out["dk"]), ref["dk"])
+    e_dv = rel_fro(f64(out["dv"]), ref["dv"])
+    msg = (f"{label}: O {e_o:.2e} beyond bf16 half-ulp (raw {raw_o:.2e}, worst {worst_index(o, ref['o'])}), LSE {e_l:.2e} "
+           f"(worst {worst_index(lse, ref['lse'])}), dQ {e_dq:.2e} dK {e_dk:.2e} dV {e_dv:.2e}")
+    print(msg)
+    assert np.isfinite(o).all() and np.isfinite(lse).all(), msg
+    assert e_o <= TOL_O and e_l <= TOL_LSE, msg
+    assert e_dq <= TOL_GRAD and e_dk <= TOL_GRAD and e_dv <= TOL_GRAD, msg

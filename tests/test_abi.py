@@ -81,3 +81,55 @@ def test_last_error_is_cleared_by_next_call(lib):
     assert gqa.attn_last_error()
     lib.attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 6, 2, 96, 1, None)
     assert "d must be" in gqa.attn_last_error()
+
+
+def _view(ptr=FAKE, st=6 * 64, sb=128 * 6 * 64):
+    return gqa.GqaView(ptr.value if isinstance(ptr, ctypes.c_void_p) else ptr, st, sb)
+
+
+@pytest.mark.parametrize("st,sb,needle", [
+    (6 * 64 + 4, 128 * 6 * 64, "multiples of 8"),   # token stride not 16-byte aligned
+    (0, 128 * 6 * 64, "positive"),                  # zero token stride
+    (-384, 128 * 6 * 64, "positive"),               # negative token stride
+    (6 * 64, 1 << 39, "below 2^39"),                # batch stride out of TMA range
+])
+def test_strided_fwd_rejects_bad_strides(lib, st, sb, needle):
+    rc = lib.attn_fwd_strided(_view(st=st, sb=sb), _view(st=2 * 64, sb=128 * 2 * 64), _view(st=2 * 64, sb=128 * 2 * 64),
+                              _view(), FAKE, 2, 128, 6, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG
+    assert needle in gqa.attn_last_error() and "q strides" in gqa.attn_last_error()
+
+
+def test_strided_rejects_self_overlapping_output(lib):
+    k = _view(st=2 * 64, sb=128 * 2 * 64)
+    # token stride smaller than the H*d elements of one token: rows of o overlap
+    rc = lib.attn_fwd_strided(_view(), k, k, _view(st=4 * 64, sb=128 * 6 * 64), FAKE, 2, 128, 6, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "output o overlaps itself" in gqa.attn_last_error()
+    # batch stride smaller than one sequence while tokens are not interleaved with batches
+    rc = lib.attn_fwd_strided(_view(), k, k, _view(st=6 * 64, sb=127 * 6 * 64), FAKE, 2, 128, 6, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "overlaps itself" in gqa.attn_last_error()
+    # the same strides are fine for an input (never written)
+    ok_in = _view(st=6 * 64, sb=127 * 6 * 64)
+    rc = lib.attn_fwd_strided(ok_in, k, k, _view(st=4 * 64, sb=128 * 6 * 64), FAKE, 2, 128, 6, 2, 64, 1, None)
+    assert "output o overlaps itself" in gqa.attn_last_error()
+
+
+def test_strided_unused_strides_are_ignored(lib):
+    """With B == 1 and T == 1 the batch and token strides are never used: any value passes
+    validation, which then fails on the next check (a misaligned lse), not on the strides."""
+    junk = _view(st=3, sb=-5)
+    rc = lib.attn_fwd_strided(junk, junk, junk, junk, MISALIGNED, 1, 1, 6, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "lse is not 16-byte aligned" in gqa.attn_last_error()
+
+
+def test_strided_bwd_checks_every_view(lib):
+    need = gqa.attn_bwd_workspace_bytes(2, 128, 6)
+    q, k = _view(), _view(st=2 * 64, sb=128 * 2 * 64)
+    bad = _view(MISALIGNED)
+    rc = lib.attn_bwd_strided(q, k, k, q, FAKE, q, q, k, bad, FAKE, need, 2, 128, 6, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "dv is not 16-byte aligned" in gqa.attn_last_error()
+    rc = lib.attn_bwd_strided(q, k, k, q, FAKE, q, q, _view(st=2 * 64, sb=64), k, FAKE, need, 2, 128, 6, 2, 64, 1,
+                              None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "output dk overlaps itself" in gqa.attn_last_error()
+    rc = lib.attn_bwd_strided(q, k, k, q, FAKE, q, q, k, k, FAKE, need - 1, 2, 128, 6, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "workspace_bytes" in gqa.attn_last_error()

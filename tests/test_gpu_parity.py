@@ -7,7 +7,6 @@ stores outside it; repeated calls must give identical bytes.
 Tolerances (fixed by the method's target): O max abs error <= 1e-2, LSE max
 abs error <= 1e-3, dQ/dK/dV relative Frobenius error <= 1e-2.
 """
-import numpy as np
 import pytest
 import torch
 
@@ -15,7 +14,7 @@ import causal_gqa_flash_gb300 as gqa
 import oracle
 from causal_gqa_flash_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
 
-from _helpers import TOL_GRAD, TOL_LSE, TOL_O, Guarded, f64, max_abs, o_err, rel_fro, worst_index
+from _helpers import Guarded, check_against_oracle
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -43,21 +42,6 @@ def run_gpu(q, k, v, dout, causal):
     for name, g in (("o", go), ("lse", gl), ("dq", gdq), ("dk", gdk), ("dv", gdv)):
         assert g.intact(), f"store outside {name}"
     return dict(o=go.tensor, lse=gl.tensor, dq=gdq.tensor, dk=gdk.tensor, dv=gdv.tensor)
-
-
-def check_against_oracle(out, ref, label):
-    o, lse = f64(out["o"]), f64(out["lse"])
-    e_o, e_l = o_err(o, ref["o"]), max_abs(lse, ref["lse"])
-    raw_o = max_abs(o, ref["o"])
-    e_dq = rel_fro(f64(out["dq"]), ref["dq"])
-    e_dk = rel_fro(f64(out["dk"]), ref["dk"])
-    e_dv = rel_fro(f64(out["dv"]), ref["dv"])
-    msg = (f"{label}: O {e_o:.2e} beyond bf16 half-ulp (raw {raw_o:.2e}, worst {worst_index(o, ref['o'])}), LSE {e_l:.2e} "
-           f"(worst {worst_index(lse, ref['lse'])}), dQ {e_dq:.2e} dK {e_dk:.2e} dV {e_dv:.2e}")
-    print(msg)
-    assert np.isfinite(o).all() and np.isfinite(lse).all(), msg
-    assert e_o <= TOL_O and e_l <= TOL_LSE, msg
-    assert e_dq <= TOL_GRAD and e_dk <= TOL_GRAD and e_dv <= TOL_GRAD, msg
 
 
 CASES = [
