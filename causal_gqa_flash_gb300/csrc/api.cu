@@ -345,10 +345,10 @@ gqa_status_t bwd_preprocess_impl(const char* fn, const View& o, const float* lse
   BwdPreParams pp;
   pp.o = o.ptr;
   pp.dO = dO.ptr;
-  pp.o_st = o.st;
-  pp.o_sb = o.sb;
-  pp.do_st = dO.st;
-  pp.do_sb = dO.sb;
+  pp.o_st16 = o.st / 8;  // strides are multiples of 8 elements (16 bytes)
+  pp.o_sb16 = o.sb / 8;
+  pp.do_st16 = dO.st / 8;
+  pp.do_sb16 = dO.sb / 8;
   pp.lse = lse;
   pp.Dvec = Dvec;
   pp.lse2 = lse2;

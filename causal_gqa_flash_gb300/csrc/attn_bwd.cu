@@ -73,17 +73,17 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const BwdPreParams
   const int part = static_cast<int>(threadIdx.x) % TPR;
   const int b = bh / p.Hq, h = bh - b * p.Hq;
   constexpr int kHalf = RPB / 2;  // a thread's second row is kHalf further
+  // this thread's 16 bytes of row (b, t0, h) of O and dO; its second row is kHalf tokens on
+  const uint4* po = reinterpret_cast<const uint4*>(p.o) + (b * p.o_sb16 + t0 * p.o_st16 + h * TPR + part);
+  const uint4* pd = reinterpret_cast<const uint4*>(p.dO) + (b * p.do_sb16 + t0 * p.do_st16 + h * TPR + part);
   uint4 a[2], c[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int t = t0 + i * kHalf;
     a[i] = c[i] = make_uint4(0u, 0u, 0u, 0u);
     if (t < p.T) {
-      // element offsets of row (b, t, h) of O and dO: multiples of 8 (16 bytes)
-      const long long eo = b * p.o_sb + t * p.o_st + h * D;
-      const long long ed = b * p.do_sb + t * p.do_st + h * D;
-      a[i] = reinterpret_cast<const uint4*>(p.o)[(eo >> 3) + part];
-      c[i] = reinterpret_cast<const uint4*>(p.dO)[(ed >> 3) + part];
+      a[i] = po[i * kHalf * p.o_st16];
+      c[i] = pd[i * kHalf * p.do_st16];
     }
   }
   float lse[2] = {0.f, 0.f};

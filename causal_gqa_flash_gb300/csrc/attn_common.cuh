@@ -44,8 +44,8 @@ struct FwdParams {
 struct BwdPreParams {
   const void* o;             // [B,T,Hq,d] bf16
   const void* dO;            // [B,T,Hq,d] bf16
-  long long o_st, o_sb;      // element strides of O between tokens / batch entries (multiples of 8)
-  long long do_st, do_sb;    // the same for dO
+  long long o_st16, o_sb16;    // strides of O between tokens / batch entries, in 16-byte units
+  long long do_st16, do_sb16;  // the same for dO
   const float* lse;
   float* Dvec;   // [B,Hq,Tpad]
   float* lse2;   // [B,Hq,Tpad]
