@@ -9,6 +9,12 @@ of "A transformer in PTX" (§Flash attention, §The same bits every time) reach
 by tiles; the formulas are listed at the top of ``oracle.c``. Arrays are numpy
 float64, C-contiguous, with q/o/dO/dq in [B,T,Hq,d], k/v/dk/dv in [B,T,Hkv,d]
 and lse/D in [B,Hq,T] (natural-log LSE).
+
+``rope`` is the rotary position embedding that the trainer applies to the
+queries and keys before attention ("A transformer in PTX", §The model); the
+page names it and gives no formula, so it is the textbook rotation (pairs of
+adjacent features, frequencies base^(-2i/d), angle = token index), written
+out below in numpy.
 """
 from __future__ import annotations
 
@@ -129,3 +135,34 @@ def probs(q, k, b: int, h: int, causal: bool = True, scale: float | None = None,
     if rc != 0:
         raise ValueError(f"oracle_probs failed ({rc})")
     return P, lse
+
+
+def rope_angles(T: int, d: int, base: float = 10000.0) -> np.ndarray:
+    """Angles [T, d/2] of the rotary embedding: angle[t, i] = t * base**(-2i/d)."""
+    if d % 2:
+        raise ValueError("d must be even")
+    theta = base ** (-2.0 * np.arange(d // 2, dtype=np.float64) / d)
+    return np.arange(T, dtype=np.float64)[:, None] * theta[None, :]
+
+
+def rope(x, base: float = 10000.0, inverse: bool = False) -> np.ndarray:
+    """Rotary embedding of x [B, T, H, d] in float64.
+
+    Feature pair (2i, 2i+1) of token t is rotated by angle[t, i] (``rope_angles``):
+        y[2i]   = x[2i] cos - x[2i+1] sin
+        y[2i+1] = x[2i] sin + x[2i+1] cos
+    ``inverse`` rotates by minus the angle (the transpose), which is also the
+    gradient of the rotation: dx = rope(dy, inverse=True).
+    """
+    x = _as_f64(x)
+    B, T, H, d = x.shape
+    ang = rope_angles(T, d, base)
+    c = np.cos(ang)[None, :, None, :]
+    s = np.sin(ang)[None, :, None, :]
+    if inverse:
+        s = -s
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    y = np.empty_like(x)
+    y[..., 0::2] = x0 * c - x1 * s
+    y[..., 1::2] = x0 * s + x1 * c
+    return y

@@ -229,3 +229,60 @@ def test_bad_shapes_rejected():
     q, k, v, _ = rand_case(1, 4, 3, 2, 8, seed=1)  # 3 % 2 != 0
     with pytest.raises(ValueError):
         oracle.fwd(q, k, v)
+
+
+# ---------------------------------------------------------------- rotary embedding (oracle.rope)
+def test_rope_closed_forms():
+    """d = 2: one pair at frequency 1, so token t turns (1, 0) into (cos t, sin t); d = 4:
+    the second pair turns at base**(-1/2) = 0.01 per token (1 radian at token 100); token 0
+    is left as it is."""
+    x = np.zeros((1, 101, 1, 2))
+    x[..., 0] = 1.0
+    y = oracle.rope(x)
+    t = np.arange(101)
+    np.testing.assert_allclose(y[0, :, 0, 0], np.cos(t), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(y[0, :, 0, 1], np.sin(t), rtol=0, atol=1e-15)
+    x4 = np.zeros((1, 101, 1, 4))
+    x4[..., 2] = 1.0
+    y4 = oracle.rope(x4)
+    assert abs(y4[0, 100, 0, 2] - math.cos(1.0)) < 1e-14 and abs(y4[0, 100, 0, 3] - math.sin(1.0)) < 1e-14
+    assert np.all(y4[0, :, 0, :2] == 0.0)
+    r = rand((2, 5, 3, 8), np.random.default_rng(3))
+    assert np.array_equal(oracle.rope(r)[:, 0], r[:, 0])
+
+
+def test_rope_preserves_pair_norms_and_inverts():
+    x = rand((2, 40, 3, 16), np.random.default_rng(4))
+    y = oracle.rope(x, base=500.0)
+    n_x = x[..., 0::2] ** 2 + x[..., 1::2] ** 2
+    n_y = y[..., 0::2] ** 2 + y[..., 1::2] ** 2
+    np.testing.assert_allclose(n_y, n_x, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(oracle.rope(y, base=500.0, inverse=True), x, rtol=0, atol=1e-13)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    """<rope(q) at m, rope(k) at n> is a function of m - n: shifting both by s keeps it."""
+    rng = np.random.default_rng(5)
+    d, T = 12, 64
+    qv, kv = rng.standard_normal(d), rng.standard_normal(d)
+    q = np.broadcast_to(qv, (1, T, 1, d)).copy()
+    k = np.broadcast_to(kv, (1, T, 1, d)).copy()
+    rq, rk = oracle.rope(q), oracle.rope(k)
+    for m, n, s in ((10, 3, 17), (40, 40, 5), (2, 30, 20)):
+        a = rq[0, m, 0] @ rk[0, n, 0]
+        b = rq[0, m + s, 0] @ rk[0, n + s, 0]
+        assert abs(a - b) < 1e-12, (m, n, s)
+
+
+def test_rope_gradient_is_inverse_rotation():
+    """Finite differences of L = sum(w * rope(x)) equal rope(w, inverse=True). The rotation
+    is linear, so a central difference is exact for any step; a large one keeps the
+    cancellation error near 1e-15."""
+    rng = np.random.default_rng(6)
+    x, w = rand((1, 9, 2, 6), rng), rand((1, 9, 2, 6), rng)
+    g = oracle.rope(w, inverse=True)
+    u = rand(x.shape, rng)
+    u /= np.linalg.norm(u)
+    eps = 0.25
+    fd = (np.sum(w * oracle.rope(x + eps * u)) - np.sum(w * oracle.rope(x - eps * u))) / (2 * eps)
+    assert abs(fd - np.sum(g * u)) < 1e-12
