@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--layout", default="separate", choices=["separate", "fused"],
                     help="fused: q, k, v are views of one [B,T,Hq+2*Hkv,d] projection buffer and the gradients "
                          "go to one such buffer (attn_fwd_strided / attn_bwd_strided)")
+    ap.add_argument("--rope", action="store_true",
+                    help="with --layout fused: each step also rotates q and k (attn_rope, out of the projection "
+                         "buffer) before attention and rotates dq and dk back after it")
     ap.add_argument("--profile-run", action="store_true",
                     help="timed steps only (no clock soak, e2e or oracle leg): the command profiled under ncu")
     return ap.parse_args()
@@ -328,13 +331,30 @@ def run_ours(args, w):
     else:
         q, k, v, dout = in_views
         o, lse, dq, dk, dv = out_views
+    rope = fused and args.rope
+    if args.rope and not fused:
+        raise SystemExit("--rope needs --layout fused")
+    if rope:
+        # q and k rotated out of the projection buffer into their own buffer; dq and dk
+        # rotated back in place in the gradient buffer; the table is built once
+        table = gqa.attn_rope_table(w.T, w.d, device=dev)
+        qk_raw = qkv[:, :, :w.Hq + w.Hkv]
+        qk_rot = torch.empty((w.B, w.T, w.Hq + w.Hkv, w.d), dtype=torch.bfloat16, device=dev)
+        q, k = qk_rot[:, :, :w.Hq], qk_rot[:, :, w.Hq:]
+        dqk = dqkv[:, :, :w.Hq + w.Hkv]
     ws = torch.empty(gqa.attn_bwd_workspace_bytes(w.B, w.T, w.Hq), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     causal = w.causal
 
-    def step(ev=None):
+    def step(ev=None, rev=None):
         if fused:
+            if rope:
+                if rev is not None:
+                    rev[0].record(stream)
+                gqa.attn_rope(qk_raw, table, y=qk_rot, stream=stream)
+                if rev is not None:
+                    rev[1].record(stream)
             # the strided backward is one call: its preprocess and main kernel share one interval
             if ev is not None:
                 ev[0].record(stream)
@@ -345,6 +365,12 @@ def run_ours(args, w):
             gqa.attn_bwd_strided(q, k, v, o, lse, dout, dq, dk, dv, causal=causal, workspace=ws, stream=stream)
             if ev is not None:
                 ev[3].record(stream)
+            if rope:
+                if rev is not None:
+                    rev[2].record(stream)
+                gqa.attn_rope(dqk, table, inverse=True, stream=stream)
+                if rev is not None:
+                    rev[3].record(stream)
             return
         if ev is not None:
             ev[0].record(stream)
@@ -386,9 +412,10 @@ def run_ours(args, w):
     wall = time.perf_counter() - wall0
     # Per-kernel breakdown (events between the kernels) for the roofline, same workload.
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    rope_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for i in range(args.steps):
         flush.zero_()
-        step(events[i])
+        step(events[i], rope_ev[i])
     torch.cuda.synchronize(dev)
     # keep the GPU busy with identical untimed steps so the 100 ms clock sampler sees load
     t_soak = time.perf_counter()
@@ -408,6 +435,17 @@ def run_ours(args, w):
     if fused:  # one strided backward call: its two kernels are timed as one interval
         per_kernel = {"attn_fwd_kernel": per_kernel["attn_fwd_kernel"],
                       "bwd_pre_kernel+bwd_main_kernel": per_kernel["bwd_main_kernel"]}
+    rope_info = None
+    if rope:
+        rope_ms = sum(rope_ev[i][0].elapsed_time(rope_ev[i][1]) + rope_ev[i][2].elapsed_time(rope_ev[i][3])
+                      for i in range(args.steps)) / args.steps
+        # per step: q, k read and written, dq, dk read and written (bf16), and 32 table bytes
+        # per 16-byte chunk of a token in each of the two calls
+        rope_bytes = 4 * w.B * w.T * (w.Hq + w.Hkv) * w.d * 2 + 2 * w.B * w.T * w.d * 4
+        rope_info = {"kernel": "rope_kernel", "calls_per_step": 2, "ms_per_step": rope_ms,
+                     "bytes_per_step": rope_bytes, "bound": "hbm",
+                     "achieved_gbs": rope_bytes / (rope_ms * 1e-3) / 1e9, "peak_gbs": peaks["hbm_gbs"],
+                     "frac": rope_bytes / (rope_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
     step_ms_total = sum(step_ev[i][0].elapsed_time(step_ev[i][1]) for i in range(args.steps))
     step_ms_total = max_over_ranks(torch, dist, step_ms_total, world, dev)
     ms_per_step = step_ms_total / args.steps
@@ -444,8 +482,7 @@ def run_ours(args, w):
     def e2e_step():
         in_d.copy_(in_h, non_blocking=True)
         if fused:
-            gqa.attn_fwd_strided(q, k, v, o, causal=causal, lse=lse, stream=stream)
-            gqa.attn_bwd_strided(q, k, v, o, lse, dout, dq, dk, dv, causal=causal, workspace=ws, stream=stream)
+            step()
         else:
             gqa.attn_fwd(q, k, v, causal=causal, o=o, lse=lse, stream=stream)
             gqa.attn_bwd(q, k, v, o, lse, dout, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
@@ -478,6 +515,8 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_dict(w, {"l2": "flushed between timed steps (256 MB write, outside the events)",
+                                      "rope": "q, k rotated before and dq, dk after attention (in the step)"
+                                      if rope else "none",
                                       "layout": "fused qkv / dqkv buffers, strided views" if fused
                                       else "separate contiguous q, k, v, dq, dk, dv",
                                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
@@ -489,7 +528,8 @@ def run_ours(args, w):
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": (5 if rope else 3) * args.steps,
+            "rope": rope_info,
             "clocks": clocks,
             "wall_s_timed": wall,
         }

@@ -19,7 +19,7 @@ __all__ = [
     "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_dq_dkv", "attn_bwd_noalloc",
     "NOALLOC_SCRATCH_BYTES",
     "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_last_error", "attn_version",
-    "GqaView", "view_of", "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
+    "GqaView", "view_of", "attn_rope_table", "attn_rope", "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
     "GQA_ERR_TIMEOUT",
 ]
 
@@ -33,8 +33,9 @@ NOALLOC_SCRATCH_BYTES = 8 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_attn
 # Every function include/gqa_attn.h declares.
 EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv",
-    "attn_bwd_dq_dkv", "attn_bwd_noalloc", "attn_fwd_strided", "attn_bwd_strided", "attn_last_error",
-    "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_version",
+    "attn_bwd_dq_dkv", "attn_bwd_noalloc", "attn_fwd_strided", "attn_bwd_strided", "attn_rope_table_bytes",
+    "attn_rope_table", "attn_rope", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
+    "attn_set_wait_budget_ns", "attn_version",
 )
 
 _lib = None
@@ -82,6 +83,12 @@ def load():
     lib.attn_fwd_strided.restype = i
     lib.attn_bwd_strided.argtypes = [gv, gv, gv, gv, vp, gv, gv, gv, gv, vp, sz, i, i, i, i, i, i, vp]
     lib.attn_bwd_strided.restype = i
+    lib.attn_rope_table_bytes.argtypes = [i, i]
+    lib.attn_rope_table_bytes.restype = sz
+    lib.attn_rope_table.argtypes = [vp, i, i, ctypes.c_double, vp]
+    lib.attn_rope_table.restype = i
+    lib.attn_rope.argtypes = [gv, gv, vp, i, i, i, i, i, vp]
+    lib.attn_rope.restype = i
     lib.attn_last_error.argtypes = []
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_sync_status.argtypes = [vp]
@@ -186,6 +193,34 @@ def attn_bwd_strided(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = True, wor
                                 _ptr(workspace), _ws_bytes(workspace), B, T, Hq, Hkv, d, int(bool(causal)),
                                 _stream_handle(stream)))
     return dq, dk, dv
+
+
+def attn_rope_table(T: int, d: int, base: float = 10000.0, device=None, stream=None):
+    """fp32 [T, d/2, 2] table of (cos, sin) of the rotary angles t * base**(-2i/d)."""
+    import torch
+    lib = load()
+    n = int(lib.attn_rope_table_bytes(T, d))
+    if n == 0:
+        raise ValueError(f"bad rotary table shape (T={T}, d={d})")
+    table = torch.empty((T, d // 2, 2), dtype=torch.float32, device=device or torch.device("cuda"))
+    _check(lib.attn_rope_table(_ptr(table), T, d, float(base), _stream_handle(stream)))
+    return table
+
+
+def attn_rope(x, table, y=None, inverse: bool = False, stream=None):
+    """Rotary embedding of the bf16 view x [B, T, H, d] into y (default: in place).
+    ``inverse`` rotates back, which is also the gradient of the rotation."""
+    lib = load()
+    if y is None:
+        y = x
+    B, T, H, d = x.shape
+    if tuple(y.shape) != tuple(x.shape):
+        raise ValueError("x and y must have the same shape")
+    if table.shape[0] < T or table.shape[1] * 2 != d:
+        raise ValueError(f"table {tuple(table.shape)} does not cover T={T}, d={d}")
+    _check(lib.attn_rope(view_of(x, "x"), view_of(y, "y"), _ptr(table), B, T, H, d, int(bool(inverse)),
+                         _stream_handle(stream)))
+    return y
 
 
 def attn_bwd_workspace_bytes(B: int, T: int, Hq: int) -> int:

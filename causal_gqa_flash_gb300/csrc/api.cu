@@ -6,6 +6,7 @@
 // runtime's own words — here as a return code plus attn_last_error(), never by
 // exiting the process.
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -16,6 +17,7 @@
 
 #include "../../include/gqa_attn.h"
 #include "attn_common.cuh"
+#include "rope.cuh"
 
 namespace gqa {
 
@@ -509,6 +511,69 @@ gqa_status_t attn_bwd_strided(gqa_view_t q, gqa_view_t k, gqa_view_t v, gqa_view
     return s;
   return bwd_impl(fn, vq, vk, vv, vo, lse, vdo, vdq, vdk, vdv, workspace, workspace_bytes, B, T, Hq, Hkv, d, causal,
                   stream);
+}
+
+size_t attn_rope_table_bytes(int T, int d) {
+  if (T <= 0 || (d != 64 && d != 128)) return 0;
+  return (size_t)T * (size_t)(d / 2) * 2 * sizeof(float);
+}
+
+gqa_status_t attn_rope_table(float* table, int T, int d, double base, void* stream) {
+  const char* fn = "attn_rope_table";
+  t_last_error.clear();
+  gqa_status_t s;
+  if (T <= 0 || T > (1 << 30)) return fail(GQA_ERR_INVALID_ARG, "%s: T must be in [1, 2^30] (got %d)", fn, T);
+  if (d != 64 && d != 128) return fail(GQA_ERR_INVALID_ARG, "%s: d must be 64 or 128 (got %d)", fn, d);
+  if (!(base > 0.0) || !std::isfinite(base))
+    return fail(GQA_ERR_INVALID_ARG, "%s: base must be positive and finite (got %g)", fn, base);
+  if ((s = check_ptr(fn, "table", table))) return s;
+  DeviceState* ds = nullptr;
+  if ((s = device_state(fn, &ds))) return s;
+  RopeTableParams p;
+  memset(&p, 0, sizeof(p));
+  p.table = table;
+  p.T = T;
+  p.half_d = d / 2;
+  for (int i = 0; i < d / 2; ++i) p.theta[i] = pow(base, -2.0 * i / d);
+  cudaError_t e = launch_rope_table(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(fn, "kernel launch", e);
+  return GQA_OK;
+}
+
+gqa_status_t attn_rope(gqa_view_t x, gqa_view_t y, const float* table, int B, int T, int H, int d, int inverse,
+                       void* stream) {
+  const char* fn = "attn_rope";
+  t_last_error.clear();
+  gqa_status_t s;
+  if (B <= 0 || T <= 0 || H <= 0)
+    return fail(GQA_ERR_INVALID_ARG, "%s: B, T, H must be positive (got %d, %d, %d)", fn, B, T, H);
+  if (d != 64 && d != 128) return fail(GQA_ERR_INVALID_ARG, "%s: d must be 64 or 128 (got %d)", fn, d);
+  if ((long long)B * T * ((H + kRopeHeads - 1) / kRopeHeads) > 0x7fffffffLL / (d / 8))
+    return fail(GQA_ERR_INVALID_ARG, "%s: problem too large (B*T = %lld, H = %d)", fn, (long long)B * T, H);
+  View vx, vy;
+  if ((s = check_view(fn, "x", x, B, T, H, d, false, &vx)) || (s = check_view(fn, "y", y, B, T, H, d, true, &vy)) ||
+      (s = check_ptr(fn, "table", table)))
+    return s;
+  if (vx.ptr == vy.ptr && (vx.st != vy.st || vx.sb != vy.sb))
+    return fail(GQA_ERR_INVALID_ARG, "%s: in place (y == x) needs the same strides for x and y", fn);
+  DeviceState* ds = nullptr;
+  if ((s = device_state(fn, &ds))) return s;
+  RopeParams p;
+  memset(&p, 0, sizeof(p));
+  p.x = vx.ptr;
+  p.y = const_cast<void*>(vy.ptr);
+  p.x_st16 = vx.st / 8;
+  p.x_sb16 = vx.sb / 8;
+  p.y_st16 = vy.st / 8;
+  p.y_sb16 = vy.sb / 8;
+  p.table = table;
+  p.B = B;
+  p.T = T;
+  p.H = H;
+  p.inverse = inverse ? 1 : 0;
+  cudaError_t e = launch_rope(p, d, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(fn, "kernel launch", e);
+  return GQA_OK;
 }
 
 gqa_status_t attn_sync_status(void* stream) {

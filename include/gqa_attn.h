@@ -178,6 +178,33 @@ gqa_status_t attn_bwd_strided(gqa_view_t q, gqa_view_t k, gqa_view_t v, gqa_view
                               size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, int causal,
                               void* stream);
 
+/*
+ * Rotary position embedding ("A transformer in PTX", §The model: the trainer
+ * rotates the queries and keys with RoPE between the fused QKV matmul and
+ * attention). The page gives no formula; the rotation is the textbook one:
+ * feature pair (2i, 2i+1) of token t turns by angle t * base^(-2i/d),
+ *     y[2i] = x[2i] cos - x[2i+1] sin,   y[2i+1] = x[2i] sin + x[2i+1] cos,
+ * and its inverse (minus the angle) is also its gradient, so the gradients of
+ * the unrotated q and k are the inverse rotation of attn_bwd's dq and dk.
+ *
+ * attn_rope_table_bytes: bytes of the table for T tokens and head dim d:
+ *   T * d/2 (cos, sin) pairs of fp32 (0 for a bad T or d).
+ * attn_rope_table: fills `table` (device, 16-byte aligned, at least
+ *   attn_rope_table_bytes(T, d) bytes) with cos and sin of every angle, each
+ *   taken in double and rounded to fp32. base > 0 (10000 in the usual setting);
+ *   d is 64 or 128. One table serves every call with the same T, d and base.
+ * attn_rope: y = rotation of x (inverse != 0: by minus the angle) for every
+ *   (b, t, h) of the bf16 [B, T, H, d] views x and y (gqa_view_t); the angle of
+ *   token t is read from `table` (T tokens or more). y may be x itself (same
+ *   pointer and strides: in place); otherwise y must not overlap x (not
+ *   checked). To rotate q and k of a fused [B, T, Hq + 2*Hkv, d] projection in
+ *   one call, pass the view of its first Hq + Hkv heads.
+ */
+size_t attn_rope_table_bytes(int T, int d);
+gqa_status_t attn_rope_table(float* table, int T, int d, double base, void* stream);
+gqa_status_t attn_rope(gqa_view_t x, gqa_view_t y, const float* table, int B, int T, int H, int d, int inverse,
+                       void* stream);
+
 /* Description of the last error returned on this host thread ("" if none). */
 const char* attn_last_error(void);
 

@@ -133,3 +133,29 @@ def test_strided_bwd_checks_every_view(lib):
     assert rc == gqa.GQA_ERR_INVALID_ARG and "output dk overlaps itself" in gqa.attn_last_error()
     rc = lib.attn_bwd_strided(q, k, k, q, FAKE, q, q, k, k, FAKE, need - 1, 2, 128, 6, 2, 64, 1, None)
     assert rc == gqa.GQA_ERR_INVALID_ARG and "workspace_bytes" in gqa.attn_last_error()
+
+
+def test_rope_table_bytes_and_checks(lib):
+    assert gqa.load().attn_rope_table_bytes(8192, 128) == 8192 * 64 * 2 * 4
+    assert gqa.load().attn_rope_table_bytes(0, 64) == 0 and gqa.load().attn_rope_table_bytes(16, 96) == 0
+    for T, d, base, ptr, needle in ((16, 96, 1e4, FAKE, "d must be 64 or 128"), (0, 64, 1e4, FAKE, "T must be"),
+                                    (16, 64, 0.0, FAKE, "base must be positive"),
+                                    (16, 64, float("nan"), FAKE, "base must be positive"),
+                                    (16, 64, 1e4, None, "table is NULL"),
+                                    (16, 64, 1e4, MISALIGNED, "table is not 16-byte aligned")):
+        rc = lib.attn_rope_table(ptr, T, d, base, None)
+        assert rc == gqa.GQA_ERR_INVALID_ARG and needle in gqa.attn_last_error(), needle
+
+
+def test_rope_argument_checks(lib):
+    x = _view(st=6 * 64, sb=128 * 6 * 64)
+    rc = lib.attn_rope(x, x, FAKE, 2, 128, 6, 96, 0, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "d must be 64 or 128" in gqa.attn_last_error()
+    rc = lib.attn_rope(x, x, None, 2, 128, 6, 64, 0, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "table is NULL" in gqa.attn_last_error()
+    rc = lib.attn_rope(x, _view(st=6 * 64 + 8, sb=128 * 7 * 64), FAKE, 2, 128, 6, 64, 0, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "same strides" in gqa.attn_last_error()
+    rc = lib.attn_rope(x, _view(st=5 * 64, sb=128 * 6 * 64, ptr=0x200000), FAKE, 2, 128, 6, 64, 0, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "output y overlaps itself" in gqa.attn_last_error()
+    rc = lib.attn_rope(x, x, FAKE, 0, 128, 6, 64, 0, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "positive" in gqa.attn_last_error()
