@@ -127,12 +127,67 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
-def _dims(q, k):
+def _dims(q, k, v=None):
     if q.dim() != 4 or k.dim() != 4:
         raise ValueError("q, k, v must be [B, T, H, d]")
     B, T, Hq, d = q.shape
-    Hkv = k.shape[2]
+    Bk, Tk, Hkv, dk = k.shape
+    if (Bk, Tk, dk) != (B, T, d):
+        raise ValueError(f"k {tuple(k.shape)} does not match q {tuple(q.shape)} in B, T or d")
+    if v is not None and tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"v {tuple(v.shape)} must have the shape of k {tuple(k.shape)}")
     return B, T, Hq, Hkv, d
+
+
+def _args(*specs):
+    """Tensor arguments (name, tensor, shape, dtype[, contiguous]), checked before their
+    pointers reach the library (the C ABI takes raw pointers and cannot see sizes, types
+    or devices): shapes, types and layouts of all of them first, then their devices."""
+    import torch
+    for spec in specs:
+        name, t, shape, dtype = spec[:4]
+        if t is None:
+            raise ValueError(f"{name} is missing")
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+        if t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+        if (spec[4] if len(spec) > 4 else True) and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    for name, t, *_ in specs:
+        if not t.is_cuda or t.device.index != torch.cuda.current_device():
+            raise ValueError(f"{name} must be on the current CUDA device, got {t.device}")
+
+
+def _arg(name, t, shape, dtype, contiguous=True):
+    _args((name, t, shape, dtype, contiguous))
+    return t
+
+
+def _ws_bytes(workspace):
+    return workspace.numel() * workspace.element_size()
+
+
+def _workspace(workspace, B, T, Hq, device):
+    import torch
+    need = attn_bwd_workspace_bytes(B, T, Hq)
+    if workspace is None:
+        return torch.empty(need, dtype=torch.uint8, device=device)
+    if not workspace.is_contiguous() or not workspace.is_cuda or workspace.device != device:
+        raise ValueError(f"workspace must be a contiguous tensor on {device}")
+    if _ws_bytes(workspace) < need:
+        raise ValueError(f"workspace holds {_ws_bytes(workspace)} bytes, {need} needed")
+    return workspace
+
+
+def _bf16():
+    import torch
+    return torch.bfloat16
+
+
+def _f32():
+    import torch
+    return torch.float32
 
 
 def attn_fwd(q, k, v, causal: bool = True, o=None, lse=None, stream=None):
@@ -142,14 +197,11 @@ def attn_fwd(q, k, v, causal: bool = True, o=None, lse=None, stream=None):
     """
     import torch
     lib = load()
-    B, T, Hq, Hkv, d = _dims(q, k)
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
-    if o is None:
-        o = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    B, T, Hq, Hkv, d = _dims(q, k, v)
+    _args(("q", q, q.shape, _bf16()), ("k", k, k.shape, _bf16()), ("v", v, k.shape, _bf16()))
+    o = torch.empty_like(q) if o is None else _arg("o", o, q.shape, _bf16())
+    lse = (torch.empty((B, Hq, T), dtype=torch.float32, device=q.device) if lse is None
+           else _arg("lse", lse, (B, Hq, T), _f32()))
     _check(lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, T, Hq, Hkv, d, int(bool(causal)),
                         _stream_handle(stream)))
     return o, lse
@@ -161,10 +213,20 @@ def view_of(t, name: str = "tensor") -> GqaView:
     import torch
     if t.dim() != 4 or t.dtype != torch.bfloat16 or not t.is_cuda:
         raise ValueError(f"{name} must be a bf16 CUDA tensor [B, T, H, d]")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} must be on the current CUDA device, got {t.device}")
     B, T, H, d = t.shape
     if t.stride(3) != 1 or (H > 1 and t.stride(2) != d):
         raise ValueError(f"{name}: the heads of a token must be packed (strides {tuple(t.stride())})")
     return GqaView(t.data_ptr(), t.stride(1), t.stride(0))
+
+
+def _views(B, T, Hq, Hkv, d, **named):
+    """gqa_view_t of each named view after checking its shape ([B,T,Hq,d] for q-shaped
+    names, [B,T,Hkv,d] for k-shaped ones)."""
+    _args(*((name, t, (B, T, Hkv if name in ("k", "v", "dk", "dv") else Hq, d), _bf16(), False)
+            for name, t in named.items()))
+    return [view_of(t, name) for name, t in named.items()]
 
 
 def attn_fwd_strided(q, k, v, o, causal: bool = True, lse=None, stream=None):
@@ -172,26 +234,24 @@ def attn_fwd_strided(q, k, v, o, causal: bool = True, lse=None, stream=None):
     projection; o (a view too) is written in place. Returns (o, lse)."""
     import torch
     lib = load()
-    B, T, Hq, Hkv, d = _dims(q, k)
-    if lse is None:
-        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
-    _check(lib.attn_fwd_strided(view_of(q, "q"), view_of(k, "k"), view_of(v, "v"), view_of(o, "o"), _ptr(lse), B, T,
-                                Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
+    B, T, Hq, Hkv, d = _dims(q, k, v)
+    views = _views(B, T, Hq, Hkv, d, q=q, k=k, v=v, o=o)
+    lse = (torch.empty((B, Hq, T), dtype=torch.float32, device=q.device) if lse is None
+           else _arg("lse", lse, (B, Hq, T), _f32()))
+    _check(lib.attn_fwd_strided(*views, _ptr(lse), B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
     return o, lse
 
 
 def attn_bwd_strided(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = True, workspace=None, stream=None):
     """attn_bwd over strided views; dq, dk, dv (views too, e.g. of one fused gradient
     buffer) are written in place. Returns (dq, dk, dv)."""
-    import torch
     lib = load()
-    B, T, Hq, Hkv, d = _dims(q, k)
-    if workspace is None:
-        workspace = torch.empty(attn_bwd_workspace_bytes(B, T, Hq), dtype=torch.uint8, device=q.device)
-    _check(lib.attn_bwd_strided(view_of(q, "q"), view_of(k, "k"), view_of(v, "v"), view_of(o, "o"), _ptr(lse),
-                                view_of(dout, "dO"), view_of(dq, "dq"), view_of(dk, "dk"), view_of(dv, "dv"),
-                                _ptr(workspace), _ws_bytes(workspace), B, T, Hq, Hkv, d, int(bool(causal)),
-                                _stream_handle(stream)))
+    B, T, Hq, Hkv, d = _dims(q, k, v)
+    vq, vk, vv, vo, vdo, vdq, vdk, vdv = _views(B, T, Hq, Hkv, d, q=q, k=k, v=v, o=o, dO=dout, dq=dq, dk=dk, dv=dv)
+    _arg("lse", lse, (B, Hq, T), _f32())
+    workspace = _workspace(workspace, B, T, Hq, q.device)
+    _check(lib.attn_bwd_strided(vq, vk, vv, vo, _ptr(lse), vdo, vdq, vdk, vdv, _ptr(workspace), _ws_bytes(workspace),
+                                B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
     return dq, dk, dv
 
 
@@ -213,11 +273,12 @@ def attn_rope(x, table, y=None, inverse: bool = False, stream=None):
     lib = load()
     if y is None:
         y = x
+    if x.dim() != 4:
+        raise ValueError("x must be [B, T, H, d]")
     B, T, H, d = x.shape
-    if tuple(y.shape) != tuple(x.shape):
-        raise ValueError("x and y must have the same shape")
-    if table.shape[0] < T or table.shape[1] * 2 != d:
+    if table.dim() != 3 or table.shape[0] < T or tuple(table.shape[1:]) != (d // 2, 2):
         raise ValueError(f"table {tuple(table.shape)} does not cover T={T}, d={d}")
+    _args(("x", x, x.shape, _bf16(), False), ("y", y, x.shape, _bf16(), False), ("table", table, table.shape, _f32()))
     _check(lib.attn_rope(view_of(x, "x"), view_of(y, "y"), _ptr(table), B, T, H, d, int(bool(inverse)),
                          _stream_handle(stream)))
     return y
@@ -227,54 +288,69 @@ def attn_bwd_workspace_bytes(B: int, T: int, Hq: int) -> int:
     return int(load().attn_bwd_workspace_bytes(B, T, Hq))
 
 
-def attn_bwd(q, k, v, o, lse, dout, causal: bool = True, dq=None, dk=None, dv=None, workspace=None,
-             stream=None):
-    """dQ, dK, dV of sum(O * dO). Returns (dq, dk, dv) bf16 with the shapes of q, k, v."""
+def _bwd_inputs(q, k, v, dout, o=None, lse=None, outputs=()):
+    """Checks the backward's inputs (and o, lse, and the given (name, tensor, like) outputs)."""
+    B, T, Hq, Hkv, d = _dims(q, k, v)
+    specs = [("q", q, q.shape, _bf16()), ("k", k, k.shape, _bf16()), ("v", v, k.shape, _bf16()),
+             ("dO", dout, q.shape, _bf16())]
+    if o is not None:
+        specs.append(("o", o, q.shape, _bf16()))
+    if lse is not None:
+        specs.append(("lse", lse, (B, Hq, T), _f32()))
+    specs += [(name, t, like.shape, _bf16()) for name, t, like in outputs]
+    _args(*specs)
+    return B, T, Hq, Hkv, d
+
+
+def _grads(q, k, dq, dk, dv, need_dq=True, need_dkv=True):
     import torch
-    lib = load()
-    B, T, Hq, Hkv, d = _dims(q, k)
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dout)):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
-    if dq is None:
-        dq = torch.empty_like(q)
-    if dk is None:
-        dk = torch.empty_like(k)
-    if dv is None:
-        dv = torch.empty_like(v)
-    need = attn_bwd_workspace_bytes(B, T, Hq)
-    if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    ws_bytes = _ws_bytes(workspace)
-    _check(lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-                        _ptr(workspace), ws_bytes, B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
+    if need_dq:
+        dq = torch.empty_like(q) if dq is None else _arg("dq", dq, q.shape, _bf16())
+    if need_dkv:
+        dk = torch.empty_like(k) if dk is None else _arg("dk", dk, k.shape, _bf16())
+        dv = torch.empty_like(k) if dv is None else _arg("dv", dv, k.shape, _bf16())
     return dq, dk, dv
 
 
-def _ws_bytes(workspace):
-    return workspace.numel() * workspace.element_size()
+def attn_bwd(q, k, v, o, lse, dout, causal: bool = True, dq=None, dk=None, dv=None, workspace=None,
+             stream=None):
+    """dQ, dK, dV of sum(O * dO). Returns (dq, dk, dv) bf16 with the shapes of q, k, v."""
+    lib = load()
+    B, T, Hq, Hkv, d = _bwd_inputs(q, k, v, dout, o=o, lse=lse)
+    dq, dk, dv = _grads(q, k, dq, dk, dv)
+    workspace = _workspace(workspace, B, T, Hq, q.device)
+    _check(lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                        _ptr(workspace), _ws_bytes(workspace), B, T, Hq, Hkv, d, int(bool(causal)),
+                        _stream_handle(stream)))
+    return dq, dk, dv
 
 
 def attn_bwd_preprocess(o, lse, dout, workspace, stream=None):
     """Stage 1 of attn_bwd: workspace <- rowsum(dO * O) and LSE * log2(e)."""
     lib = load()
+    if o.dim() != 4:
+        raise ValueError("o must be [B, T, Hq, d]")
     B, T, Hq, d = o.shape
+    _args(("o", o, o.shape, _bf16()), ("dO", dout, o.shape, _bf16()), ("lse", lse, (B, Hq, T), _f32()))
+    workspace = _workspace(workspace, B, T, Hq, o.device)
     _check(lib.attn_bwd_preprocess(_ptr(o), _ptr(lse), _ptr(dout), _ptr(workspace), _ws_bytes(workspace), B, T,
                                    Hq, d, _stream_handle(stream)))
 
 
 def attn_bwd_dq(q, k, v, dout, dq, workspace, causal: bool = True, stream=None):
-    """Stage 2 of attn_bwd: dq, one CTA per query tile."""
+    """Stage 2 of attn_bwd: dq, one task per query tile."""
     lib = load()
-    B, T, Hq, Hkv, d = _dims(q, k)
+    B, T, Hq, Hkv, d = _bwd_inputs(q, k, v, dout, outputs=(("dq", dq, q),))
+    workspace = _workspace(workspace, B, T, Hq, q.device)
     _check(lib.attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(workspace), _ws_bytes(workspace),
                            B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
 
 
 def attn_bwd_dkv(q, k, v, dout, dk, dv, workspace, causal: bool = True, stream=None):
-    """Stage 3 of attn_bwd: dk and dv, one CTA per key tile looping over the kv head's query heads."""
+    """Stage 3 of attn_bwd: dk and dv, one task per key tile looping over the kv head's query heads."""
     lib = load()
-    B, T, Hq, Hkv, d = _dims(q, k)
+    B, T, Hq, Hkv, d = _bwd_inputs(q, k, v, dout, outputs=(("dk", dk, k), ("dv", dv, k)))
+    workspace = _workspace(workspace, B, T, Hq, q.device)
     _check(lib.attn_bwd_dkv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dk), _ptr(dv), _ptr(workspace),
                             _ws_bytes(workspace), B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
 
@@ -282,7 +358,8 @@ def attn_bwd_dkv(q, k, v, dout, dk, dv, workspace, causal: bool = True, stream=N
 def attn_bwd_dq_dkv(q, k, v, dout, dq, dk, dv, workspace, causal: bool = True, stream=None):
     """Stages 2+3 of attn_bwd in one launch: dq, dk and dv (heaviest tasks first)."""
     lib = load()
-    B, T, Hq, Hkv, d = _dims(q, k)
+    B, T, Hq, Hkv, d = _bwd_inputs(q, k, v, dout, outputs=(("dq", dq, q), ("dk", dk, k), ("dv", dv, k)))
+    workspace = _workspace(workspace, B, T, Hq, q.device)
     _check(lib.attn_bwd_dq_dkv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
                                _ws_bytes(workspace), B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
 
@@ -294,15 +371,9 @@ def attn_bwd_noalloc(q, k, v, o, lse, dout, causal: bool = True, dq=None, dk=Non
     Problems needing more than NOALLOC_SCRATCH_BYTES of scratch are rejected;
     calls that overlap on one GPU race on the shared array.
     """
-    import torch
     lib = load()
-    B, T, Hq, Hkv, d = _dims(q, k)
-    if dq is None:
-        dq = torch.empty_like(q)
-    if dk is None:
-        dk = torch.empty_like(k)
-    if dv is None:
-        dv = torch.empty_like(v)
+    B, T, Hq, Hkv, d = _bwd_inputs(q, k, v, dout, o=o, lse=lse)
+    dq, dk, dv = _grads(q, k, dq, dk, dv)
     _check(lib.attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                                 _ptr(dv), B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
     return dq, dk, dv

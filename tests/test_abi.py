@@ -159,3 +159,23 @@ def test_rope_argument_checks(lib):
     assert rc == gqa.GQA_ERR_INVALID_ARG and "output y overlaps itself" in gqa.attn_last_error()
     rc = lib.attn_rope(x, x, FAKE, 0, 128, 6, 64, 0, None)
     assert rc == gqa.GQA_ERR_INVALID_ARG and "positive" in gqa.attn_last_error()
+
+
+def test_binding_checks_shapes_types_and_device_before_calling(lib):
+    """The C ABI takes raw pointers and cannot see sizes: the binding refuses mismatched
+    shapes, dtypes and non-CUDA tensors before any pointer reaches the library."""
+    import torch
+    bf = torch.bfloat16
+    q, k = torch.zeros((1, 128, 6, 64), dtype=bf), torch.zeros((1, 128, 2, 64), dtype=bf)
+    with pytest.raises(ValueError, match="does not match q"):
+        gqa.attn_fwd(q, torch.zeros((1, 127, 2, 64), dtype=bf), k)
+    with pytest.raises(ValueError, match="must have the shape of k"):
+        gqa.attn_fwd(q, k, torch.zeros((1, 128, 3, 64), dtype=bf))
+    with pytest.raises(ValueError, match="q must be torch.bfloat16"):
+        gqa.attn_fwd(q.float(), k, k)
+    with pytest.raises(ValueError, match="q must be contiguous"):
+        gqa.attn_fwd(q.transpose(1, 2).contiguous().transpose(1, 2), k, k)
+    with pytest.raises(ValueError, match="current CUDA device"):
+        gqa.attn_fwd(q, k, k)
+    with pytest.raises(ValueError, match="dO must have shape"):
+        gqa.attn_bwd_dq(q, k, k, torch.zeros((1, 128, 5, 64), dtype=bf), q, None)
