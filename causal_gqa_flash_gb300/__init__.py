@@ -19,7 +19,8 @@ __all__ = [
     "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_dq_dkv", "attn_bwd_noalloc",
     "NOALLOC_SCRATCH_BYTES",
     "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_last_error", "attn_version",
-    "GqaView", "view_of", "attn_rope_table", "attn_rope", "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
+    "GqaView", "view_of", "attn_rope_table", "attn_rope", "attn_fwd_naive", "attn_bwd_naive",
+    "attn_naive_workspace_bytes", "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
     "GQA_ERR_TIMEOUT",
 ]
 
@@ -34,7 +35,8 @@ NOALLOC_SCRATCH_BYTES = 8 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_attn
 EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv",
     "attn_bwd_dq_dkv", "attn_bwd_noalloc", "attn_fwd_strided", "attn_bwd_strided", "attn_rope_table_bytes",
-    "attn_rope_table", "attn_rope", "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
+    "attn_rope_table", "attn_rope", "attn_naive_workspace_bytes", "attn_fwd_naive", "attn_bwd_naive",
+    "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
     "attn_set_wait_budget_ns", "attn_version",
 )
 
@@ -89,6 +91,12 @@ def load():
     lib.attn_rope_table.restype = i
     lib.attn_rope.argtypes = [gv, gv, vp, i, i, i, i, i, vp]
     lib.attn_rope.restype = i
+    lib.attn_naive_workspace_bytes.argtypes = [i, i, i]
+    lib.attn_naive_workspace_bytes.restype = sz
+    lib.attn_fwd_naive.argtypes = [vp] * 6 + [sz, i, i, i, i, i, i, vp]
+    lib.attn_fwd_naive.restype = i
+    lib.attn_bwd_naive.argtypes = [vp] * 10 + [sz, i, i, i, i, i, i, vp]
+    lib.attn_bwd_naive.restype = i
     lib.attn_last_error.argtypes = []
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_sync_status.argtypes = [vp]
@@ -282,6 +290,51 @@ def attn_rope(x, table, y=None, inverse: bool = False, stream=None):
     _check(lib.attn_rope(view_of(x, "x"), view_of(y, "y"), _ptr(table), B, T, H, d, int(bool(inverse)),
                          _stream_handle(stream)))
     return y
+
+
+def attn_naive_workspace_bytes(B: int, T: int, Hq: int) -> int:
+    return int(load().attn_naive_workspace_bytes(B, T, Hq))
+
+
+def _naive_workspace(workspace, B, T, Hq, device):
+    import torch
+    need = attn_naive_workspace_bytes(B, T, Hq)
+    if workspace is None:
+        return torch.empty(need, dtype=torch.uint8, device=device)
+    if not workspace.is_contiguous() or not workspace.is_cuda or workspace.device != device:
+        raise ValueError(f"workspace must be a contiguous tensor on {device}")
+    if _ws_bytes(workspace) < need:
+        raise ValueError(f"workspace holds {_ws_bytes(workspace)} bytes, {need} needed")
+    return workspace
+
+
+def attn_fwd_naive(q, k, v, causal: bool = True, o=None, lse=None, workspace=None, stream=None):
+    """attn_fwd by the plain kernels that write the whole score matrix (the check of the
+    flash kernels). Needs attn_naive_workspace_bytes(B, T, Hq) bytes of scratch."""
+    import torch
+    lib = load()
+    B, T, Hq, Hkv, d = _dims(q, k, v)
+    _args(("q", q, q.shape, _bf16()), ("k", k, k.shape, _bf16()), ("v", v, k.shape, _bf16()))
+    o = torch.empty_like(q) if o is None else _arg("o", o, q.shape, _bf16())
+    lse = (torch.empty((B, Hq, T), dtype=torch.float32, device=q.device) if lse is None
+           else _arg("lse", lse, (B, Hq, T), _f32()))
+    workspace = _naive_workspace(workspace, B, T, Hq, q.device)
+    _check(lib.attn_fwd_naive(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace), _ws_bytes(workspace),
+                              B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
+    return o, lse
+
+
+def attn_bwd_naive(q, k, v, o, lse, dout, causal: bool = True, dq=None, dk=None, dv=None, workspace=None,
+                   stream=None):
+    """attn_bwd by the plain kernels that write the whole score matrix."""
+    lib = load()
+    B, T, Hq, Hkv, d = _bwd_inputs(q, k, v, dout, o=o, lse=lse)
+    dq, dk, dv = _grads(q, k, dq, dk, dv)
+    workspace = _naive_workspace(workspace, B, T, Hq, q.device)
+    _check(lib.attn_bwd_naive(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                              _ptr(dv), _ptr(workspace), _ws_bytes(workspace), B, T, Hq, Hkv, d, int(bool(causal)),
+                              _stream_handle(stream)))
+    return dq, dk, dv
 
 
 def attn_bwd_workspace_bytes(B: int, T: int, Hq: int) -> int:

@@ -17,6 +17,7 @@
 
 #include "../../include/gqa_attn.h"
 #include "attn_common.cuh"
+#include "naive.cuh"
 #include "rope.cuh"
 
 namespace gqa {
@@ -511,6 +512,91 @@ gqa_status_t attn_bwd_strided(gqa_view_t q, gqa_view_t k, gqa_view_t v, gqa_view
     return s;
   return bwd_impl(fn, vq, vk, vv, vo, lse, vdo, vdq, vdk, vdv, workspace, workspace_bytes, B, T, Hq, Hkv, d, causal,
                   stream);
+}
+
+size_t attn_naive_workspace_bytes(int B, int T, int Hq) {
+  if (B <= 0 || T <= 0 || Hq <= 0) return 0;
+  return naive_workspace_bytes(NaiveShape{B, T, Hq, 1, 64});
+}
+
+}  // extern "C"
+
+namespace {
+
+gqa_status_t naive_checks(const char* fn, const void* workspace, size_t workspace_bytes, int B, int T, int Hq,
+                          int Hkv, int d) {
+  gqa_status_t s;
+  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
+  // one block per score row and (T/16)^2 tiles per head: keep the grids in range
+  if ((long long)B * Hq * T > 0x7fffffffLL || (long long)B * Hq > 65535)
+    return fail(GQA_ERR_INVALID_ARG, "%s: problem too large for the naive kernels", fn);
+  if ((s = check_ptr(fn, "workspace", workspace))) return s;
+  const size_t need = attn_naive_workspace_bytes(B, T, Hq);
+  if (workspace_bytes < need)
+    return fail(GQA_ERR_INVALID_ARG, "%s: workspace_bytes %zu < required %zu", fn, workspace_bytes, need);
+  return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status_t attn_fwd_naive(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                            size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, int causal, void* stream) {
+  const char* fn = "attn_fwd_naive";
+  t_last_error.clear();
+  gqa_status_t s;
+  if ((s = naive_checks(fn, workspace, workspace_bytes, B, T, Hq, Hkv, d))) return s;
+  if ((s = check_ptr(fn, "q", q)) || (s = check_ptr(fn, "k", k)) || (s = check_ptr(fn, "v", v)) ||
+      (s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)))
+    return s;
+  DeviceState* ds = nullptr;
+  if ((s = device_state(fn, &ds))) return s;
+  NaiveFwdArgs a;
+  a.s = NaiveShape{B, T, Hq, Hkv, d};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.workspace = workspace;
+  a.scale = (float)(1.0 / sqrt((double)d));
+  a.causal = causal ? 1 : 0;
+  cudaError_t e = launch_naive_fwd(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(fn, "kernel launch", e);
+  return GQA_OK;
+}
+
+gqa_status_t attn_bwd_naive(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                            int B, int T, int Hq, int Hkv, int d, int causal, void* stream) {
+  const char* fn = "attn_bwd_naive";
+  t_last_error.clear();
+  gqa_status_t s;
+  if ((s = naive_checks(fn, workspace, workspace_bytes, B, T, Hq, Hkv, d))) return s;
+  if ((s = check_ptr(fn, "q", q)) || (s = check_ptr(fn, "k", k)) || (s = check_ptr(fn, "v", v)) ||
+      (s = check_ptr(fn, "o", o)) || (s = check_ptr(fn, "lse", lse)) || (s = check_ptr(fn, "dO", dO)) ||
+      (s = check_ptr(fn, "dq", dq)) || (s = check_ptr(fn, "dk", dk)) || (s = check_ptr(fn, "dv", dv)))
+    return s;
+  DeviceState* ds = nullptr;
+  if ((s = device_state(fn, &ds))) return s;
+  NaiveBwdArgs a;
+  a.s = NaiveShape{B, T, Hq, Hkv, d};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.workspace = workspace;
+  a.scale = (float)(1.0 / sqrt((double)d));
+  a.causal = causal ? 1 : 0;
+  cudaError_t e = launch_naive_bwd(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(fn, "kernel launch", e);
+  return GQA_OK;
 }
 
 size_t attn_rope_table_bytes(int T, int d) {

@@ -205,6 +205,27 @@ gqa_status_t attn_rope_table(float* table, int T, int d, double base, void* stre
 gqa_status_t attn_rope(gqa_view_t x, gqa_view_t y, const float* table, int B, int T, int H, int d, int inverse,
                        void* stream);
 
+/*
+ * Naive attention ("A transformer in PTX", §Three ways to run it: the same
+ * operations as plain kernels on bf16 activations, the reference the fast
+ * kernels are checked against; §Flash attention: the naive kernels write the
+ * whole T x T score matrix of every head). Slow and memory-hungry by design:
+ * a check of the flash kernels at full size, not a fast path. Plain CUDA cores,
+ * fp32 products and sums; scores and dP are kept in fp32, P and dS in bf16.
+ *
+ * attn_naive_workspace_bytes: bytes of scratch for both calls,
+ *   B * Hq * T * T * (4 + 2 + 2).
+ * attn_fwd_naive / attn_bwd_naive: the same arguments and layouts as attn_fwd
+ *   and attn_bwd (contiguous tensors), with a workspace of at least
+ *   attn_naive_workspace_bytes(B, T, Hq) bytes, 16-byte aligned.
+ */
+size_t attn_naive_workspace_bytes(int B, int T, int Hq);
+gqa_status_t attn_fwd_naive(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                            size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, int causal, void* stream);
+gqa_status_t attn_bwd_naive(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                            int B, int T, int Hq, int Hkv, int d, int causal, void* stream);
+
 /* Description of the last error returned on this host thread ("" if none). */
 const char* attn_last_error(void);
 

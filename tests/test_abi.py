@@ -179,3 +179,12 @@ def test_binding_checks_shapes_types_and_device_before_calling(lib):
         gqa.attn_fwd(q, k, k)
     with pytest.raises(ValueError, match="dO must have shape"):
         gqa.attn_bwd_dq(q, k, k, torch.zeros((1, 128, 5, 64), dtype=bf), q, None)
+
+
+def test_naive_workspace_and_checks(lib):
+    assert gqa.attn_naive_workspace_bytes(2, 100, 3) == 2 * 3 * 100 * 100 * (4 + 2 + 2)
+    need = gqa.attn_naive_workspace_bytes(1, 128, 6)
+    rc = lib.attn_fwd_naive(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need - 1, 1, 128, 6, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "workspace_bytes" in gqa.attn_last_error()
+    rc = lib.attn_bwd_naive(*([FAKE] * 10), need, 1, 128, 6, 2, 96, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "d must be 64 or 128" in gqa.attn_last_error()
