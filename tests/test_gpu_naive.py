@@ -95,3 +95,24 @@ def test_flash_against_naive_full_size(name):
     assert bool(torch.isfinite(of).all()) and bool(torch.isfinite(lse).all()), msg
     assert float(e_o_bh.max()) <= TOL_O and float(e_l_bh.max()) <= TOL_LSE, msg
     assert max(errs.values()) <= TOL_GRAD and max(grp) <= 2 * TOL_GRAD, msg
+
+
+@pytest.mark.parametrize("case", [(1, 32767, 2, 1, 128, True), (1, 16385, 4, 1, 64, True)],
+                         ids=lambda c: "B{}_T{}_Hq{}_Hkv{}_d{}".format(*c[:5]))
+def test_flash_against_naive_long_context(case):
+    """Sequences far beyond what the CPU oracle can hold (a T x T f64 matrix per head):
+    256 key tiles per row at T = 32767, so the running max is rescaled across hundreds
+    of tiles; ragged ends one row past and one row short of a tile boundary."""
+    B, T, Hq, Hkv, d, causal = case
+    q, k, v, dout = (x.to(DEV) for x in make_inputs(B, T, Hq, Hkv, d, seed=T))
+    o, lse = gqa.attn_fwd(q, k, v, causal=causal)
+    dq, dk, dv = gqa.attn_bwd(q, k, v, o, lse, dout, causal=causal)
+    assert gqa.attn_sync_status() == gqa.GQA_OK, gqa.attn_last_error()
+    ref = run_naive(q, k, v, dout, causal)
+    e_o = float(((o.float() - ref["o"].float()).abs() - ulp_bf16(ref["o"].float())).max())
+    e_l = float((lse - ref["lse"]).abs().max())
+    errs = {nm: rel_fro(a, ref[nm]) for nm, a in (("dq", dq), ("dk", dk), ("dv", dv))}
+    msg = f"{case}: O {e_o:.2e} beyond one bf16 ulp, LSE {e_l:.2e}, " + ", ".join(
+        f"{nm} {e:.2e}" for nm, e in errs.items())
+    print(msg)
+    assert e_o <= TOL_O and e_l <= TOL_LSE and max(errs.values()) <= TOL_GRAD, msg
