@@ -524,6 +524,8 @@ def run_ours(args, w):
                                       "layout": "fused qkv / dqkv buffers, strided views" if fused
                                       else "separate contiguous q, k, v, dq, dk, dv",
                                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+            # the same step counted with the exact number of causal pairs, T(T+1)/2
+            "value_exact_pairs": value * ((w.T + 1) / w.T if w.causal else 1.0),
             "pct_of_peak": 100.0 * per_gpu / peaks["bf16_tflops"],
             "peak_tflops": peaks["bf16_tflops"], "peak_source": f"{peak_src} burst",
             "fwd_tflops": fwd_flops(w) / (kernel_ms["attn_fwd_kernel"] * 1e-3) / 1e12,
