@@ -188,3 +188,25 @@ def test_naive_workspace_and_checks(lib):
     assert rc == gqa.GQA_ERR_INVALID_ARG and "workspace_bytes" in gqa.attn_last_error()
     rc = lib.attn_bwd_naive(*([FAKE] * 10), need, 1, 128, 6, 2, 96, 1, None)
     assert rc == gqa.GQA_ERR_INVALID_ARG and "d must be 64 or 128" in gqa.attn_last_error()
+
+
+def test_build_compiles_every_cuda_source():
+    """build() compiles the library from an explicit list; a .cu file left out of it
+    would silently drop its kernels (and C entry points) from the GPU machine's build."""
+    from causal_gqa_flash_gb300 import _build
+    on_disk = {f for f in os.listdir(_build.CSRC) if f.endswith(".cu")}
+    assert on_disk == set(_build.SOURCES)
+
+
+def test_kernel_source_hash_ignores_comments_only(tmp_path, monkeypatch):
+    """The recorded DRAM traffic stays valid across comment edits and lapses on code edits."""
+    import bench
+    src = tmp_path / "causal_gqa_flash_gb300" / "csrc"
+    src.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (src / "k.cu").write_text("int f() { return 1; }  // one\n/* block */\n")
+    h0 = bench.kernel_source_hash(["k.cu"])
+    (src / "k.cu").write_text("// a new comment\nint f() { return 1; }  // changed\n\n")
+    assert bench.kernel_source_hash(["k.cu"]) == h0
+    (src / "k.cu").write_text("int f() { return 2; }\n")
+    assert bench.kernel_source_hash(["k.cu"]) != h0
