@@ -229,11 +229,11 @@ def view_of(t, name: str = "tensor") -> GqaView:
     return GqaView(t.data_ptr(), t.stride(1), t.stride(0))
 
 
-def _views(B, T, Hq, Hkv, d, **named):
+def _views(B, T, Hq, Hkv, d, extra=(), **named):
     """gqa_view_t of each named view after checking its shape ([B,T,Hq,d] for q-shaped
-    names, [B,T,Hkv,d] for k-shaped ones)."""
+    names, [B,T,Hkv,d] for k-shaped ones), together with the extra argument specs."""
     _args(*((name, t, (B, T, Hkv if name in ("k", "v", "dk", "dv") else Hq, d), _bf16(), False)
-            for name, t in named.items()))
+            for name, t in named.items()), *extra)
     return [view_of(t, name) for name, t in named.items()]
 
 
@@ -243,9 +243,10 @@ def attn_fwd_strided(q, k, v, o, causal: bool = True, lse=None, stream=None):
     import torch
     lib = load()
     B, T, Hq, Hkv, d = _dims(q, k, v)
-    views = _views(B, T, Hq, Hkv, d, q=q, k=k, v=v, o=o)
-    lse = (torch.empty((B, Hq, T), dtype=torch.float32, device=q.device) if lse is None
-           else _arg("lse", lse, (B, Hq, T), _f32()))
+    views = _views(B, T, Hq, Hkv, d, extra=() if lse is None else (("lse", lse, (B, Hq, T), _f32()),),
+                   q=q, k=k, v=v, o=o)
+    if lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
     _check(lib.attn_fwd_strided(*views, _ptr(lse), B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
     return o, lse
 
@@ -255,8 +256,8 @@ def attn_bwd_strided(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = True, wor
     buffer) are written in place. Returns (dq, dk, dv)."""
     lib = load()
     B, T, Hq, Hkv, d = _dims(q, k, v)
-    vq, vk, vv, vo, vdo, vdq, vdk, vdv = _views(B, T, Hq, Hkv, d, q=q, k=k, v=v, o=o, dO=dout, dq=dq, dk=dk, dv=dv)
-    _arg("lse", lse, (B, Hq, T), _f32())
+    vq, vk, vv, vo, vdo, vdq, vdk, vdv = _views(B, T, Hq, Hkv, d, extra=(("lse", lse, (B, Hq, T), _f32()),),
+                                                q=q, k=k, v=v, o=o, dO=dout, dq=dq, dk=dk, dv=dv)
     workspace = _workspace(workspace, B, T, Hq, q.device)
     _check(lib.attn_bwd_strided(vq, vk, vv, vo, _ptr(lse), vdo, vdq, vdk, vdv, _ptr(workspace), _ws_bytes(workspace),
                                 B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))

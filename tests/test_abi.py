@@ -210,3 +210,30 @@ def test_kernel_source_hash_ignores_comments_only(tmp_path, monkeypatch):
     assert bench.kernel_source_hash(["k.cu"]) == h0
     (src / "k.cu").write_text("int f() { return 2; }\n")
     assert bench.kernel_source_hash(["k.cu"]) != h0
+
+
+def test_binding_checks_views_rope_and_naive_arguments(lib):
+    """Shape and dtype mistakes in the strided, rotary and naive entry points are
+    refused by the binding, before any pointer reaches the library."""
+    import torch
+    bf = torch.bfloat16
+    q, k = torch.zeros((2, 64, 6, 64), dtype=bf), torch.zeros((2, 64, 2, 64), dtype=bf)
+    lse = torch.zeros((2, 6, 64))
+    with pytest.raises(ValueError, match="o must have shape"):
+        gqa.attn_fwd_strided(q, k, k, torch.zeros((2, 64, 5, 64), dtype=bf))
+    with pytest.raises(ValueError, match="dk must have shape"):
+        gqa.attn_bwd_strided(q, k, k, q, lse, q, q, torch.zeros((2, 64, 3, 64), dtype=bf), k)
+    with pytest.raises(ValueError, match="lse must have shape"):
+        gqa.attn_bwd_strided(q, k, k, q, torch.zeros((2, 6, 63)), q, q, k, k)
+    with pytest.raises(ValueError, match="does not cover"):
+        gqa.attn_rope(q, torch.zeros((63, 32, 2)))          # table shorter than T
+    with pytest.raises(ValueError, match="does not cover"):
+        gqa.attn_rope(q, torch.zeros((64, 64, 2)))          # table for d = 128
+    with pytest.raises(ValueError, match="y must have shape"):
+        gqa.attn_rope(q, torch.zeros((64, 32, 2)), y=k)
+    with pytest.raises(ValueError, match="table must be torch.float32"):
+        gqa.attn_rope(q, torch.zeros((64, 32, 2), dtype=torch.float64))
+    with pytest.raises(ValueError, match="must have the shape of k"):
+        gqa.attn_fwd_naive(q, k, q)
+    with pytest.raises(ValueError, match="lse must have shape"):
+        gqa.attn_bwd_naive(q, k, k, q, torch.zeros((2, 6, 65)), q)
