@@ -7,7 +7,11 @@ one batch of the workload, with inputs resident in HBM. The metric is causal
 TFLOP/s of fwd+bwd with the standard count: fwd = 4*B*Hq*T^2*d/2 and
 bwd = 2.5 * fwd (five matmuls; the dQ and dK/dV kernels actually run seven).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c4|c1..c5|all] [--impl ours|reference]
+
+The default workload is c4 (B=2 T=8192 Hq=32 Hkv=8 d=128, the largest): the
+throughput targets are stated at T >= 4096. --workload all prints one line per
+workload, c1, c2, c3 and c5 first and the c4 line last.
 
 Under torchrun (N > 1) every rank runs its own replica of the workload on its
 own GPU (the (batch, kv-head) units are independent: no collective is needed);
@@ -44,7 +48,8 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="c2", help="c1..c5 (default c2, the trainer's dev-preset shape)")
+    ap.add_argument("--workload", default="c4",
+                    help="c1..c5 or all (default c4, B=2 T=8192 Hq=32 Hkv=8 d=128, the largest single-GPU workload)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--layout", default="separate", choices=["separate", "fused"],
@@ -201,8 +206,10 @@ KERNEL_SOURCES = {
 }
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+def recorded_counters(kernel: str, workload: str):
+    """The committed ncu record of a kernel on a workload (DRAM bytes per launch and,
+    where captured, the tensor pipe's active share), or None once the kernel's source
+    has changed since the capture."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
@@ -212,7 +219,13 @@ def recorded_traffic(kernel: str, workload: str):
     ent = rec.get(kernel, {}).get(workload)
     if not ent or ent.get("source_sha256_16") != kernel_source_hash(KERNEL_SOURCES[kernel]):
         return None
-    return ent.get("dram_bytes_per_launch")
+    return ent
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+    ent = recorded_counters(kernel, workload)
+    return None if ent is None else ent.get("dram_bytes_per_launch")
 
 
 # ----------------------------------------------------------------------------- CPU oracle leg
@@ -278,39 +291,63 @@ def run_reference(args, w):
 
 
 # ----------------------------------------------------------------------------- our arm
-def run_ours(args, w):
-    import torch
-    import torch.distributed as dist
+# Matmuls (over the causal pairs of all heads) each kernel is credited with, by the
+# standard count: the forward two (S = QK^T, O = PV), the backward five (S, dP, dV,
+# dK, dQ). EXECUTED_MATMULS is what the kernels run: the backward's dQ tasks compute
+# S and dP a second time.
+CREDITED_MATMULS = {"attn_fwd_kernel": 2, "bwd_main_kernel": 5, "bwd_pre_kernel+bwd_main_kernel": 5}
+EXECUTED_MATMULS = {"attn_fwd_kernel": 2, "bwd_main_kernel": 7, "bwd_pre_kernel+bwd_main_kernel": 7}
 
-    import causal_gqa_flash_gb300 as gqa
+
+class Context:
+    """Per-process state shared by the workloads of one run."""
+
+    def __init__(self, args):
+        import torch
+        import torch.distributed as dist
+
+        import causal_gqa_flash_gb300 as gqa
+
+        self.torch, self.dist, self.gqa = torch, dist, gqa
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        if self.world > 1:
+            dist.init_process_group("nccl")
+        torch.cuda.set_device(local)
+        self.dev = torch.device("cuda", local)
+        gqa.build()
+        gqa.load()
+        self.peaks, self.peak_src = load_peaks()
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=self.dev)
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+
+def run_workload(args, ctx, w, cpu_seconds):
+    """Time the step on workload w; returns the JSON line (rank 0) or None."""
+    torch, dist, gqa = ctx.torch, ctx.dist, ctx.gqa
     from causal_gqa_flash_gb300.inputs import workload_inputs
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
-    gqa.build()
-    gqa.load()
-    peaks, peak_src = load_peaks()
+    world, rank, dev, peaks, peak_src = ctx.world, ctx.rank, ctx.dev, ctx.peaks, ctx.peak_src
+    flush = ctx.flush
 
     # Inputs and outputs each live in one contiguous buffer (views at 256-byte
     # aligned offsets), so the end-to-end leg moves them with one copy each way.
+    # Two of each on the device: the end-to-end leg alternates between them.
     q_c, k_c, v_c, do_c = workload_inputs(w)
     in_specs = [(x.shape, x.dtype) for x in (q_c, k_c, v_c, do_c)]
     out_specs = [(q_c.shape, torch.bfloat16), ((w.B, w.Hq, w.T), torch.float32), (q_c.shape, torch.bfloat16),
                  (k_c.shape, torch.bfloat16), (v_c.shape, torch.bfloat16)]
     fused = args.layout == "fused"
+    H3 = w.Hq + 2 * w.Hkv
     if fused:
         # one [B,T,Hq+2*Hkv,d] projection buffer in, one gradient buffer of that shape out
-        H3 = w.Hq + 2 * w.Hkv
         qkv_shape = (w.B, w.T, H3, w.d)
         in_specs = [(qkv_shape, torch.bfloat16), (do_c.shape, do_c.dtype)]
         out_specs = [(q_c.shape, torch.bfloat16), ((w.B, w.Hq, w.T), torch.float32), (qkv_shape, torch.bfloat16)]
-    in_d, in_views = packed_buffer(torch, in_specs, device=dev)
     in_h, host_in = packed_buffer(torch, in_specs, pin=True)
     if fused:
         host_in[0][:, :, :w.Hq].copy_(q_c)
@@ -320,39 +357,52 @@ def run_ours(args, w):
     else:
         for dst, src in zip(host_in, (q_c, k_c, v_c, do_c)):
             dst.copy_(src)
-    in_d.copy_(in_h)
-    out_d, out_views = packed_buffer(torch, out_specs, device=dev)
-    if fused:
-        qkv, dout = in_views
-        o, lse, dqkv = out_views
-        cut = (slice(0, w.Hq), slice(w.Hq, w.Hq + w.Hkv), slice(w.Hq + w.Hkv, H3))
-        q, k, v = (qkv[:, :, c] for c in cut)
-        dq, dk, dv = (dqkv[:, :, c] for c in cut)
-    else:
-        q, k, v, dout = in_views
-        o, lse, dq, dk, dv = out_views
+    del q_c, k_c, v_c, do_c
     rope = fused and args.rope
     if args.rope and not fused:
         raise SystemExit("--rope needs --layout fused")
-    if rope:
-        # q and k rotated out of the projection buffer into their own buffer; dq and dk
-        # rotated back in place in the gradient buffer; the table is built once
-        table = gqa.attn_rope_table(w.T, w.d, device=dev)
-        qk_raw = qkv[:, :, :w.Hq + w.Hkv]
-        qk_rot = torch.empty((w.B, w.T, w.Hq + w.Hkv, w.d), dtype=torch.bfloat16, device=dev)
-        q, k = qk_rot[:, :, :w.Hq], qk_rot[:, :, w.Hq:]
-        dqk = dqkv[:, :, :w.Hq + w.Hkv]
+    table = gqa.attn_rope_table(w.T, w.d, device=dev) if rope else None
+    qk_rot = torch.empty((w.B, w.T, w.Hq + w.Hkv, w.d), dtype=torch.bfloat16, device=dev) if rope else None
+    cut = (slice(0, w.Hq), slice(w.Hq, w.Hq + w.Hkv), slice(w.Hq + w.Hkv, H3))
+
+    def make_set():
+        """Device buffers of one step and their views."""
+        in_d, in_views = packed_buffer(torch, in_specs, device=dev)
+        out_d, out_views = packed_buffer(torch, out_specs, device=dev)
+        sv = {"in": in_d, "out": out_d}
+        if fused:
+            qkv, sv["dout"] = in_views
+            sv["o"], sv["lse"], dqkv = out_views
+            sv["q"], sv["k"], sv["v"] = (qkv[:, :, c] for c in cut)
+            sv["dq"], sv["dk"], sv["dv"] = (dqkv[:, :, c] for c in cut)
+            if rope:
+                # q and k rotated out of the projection buffer into their own buffer; dq and dk
+                # rotated back in place in the gradient buffer
+                sv["qk_raw"] = qkv[:, :, :w.Hq + w.Hkv]
+                sv["q"], sv["k"] = qk_rot[:, :, :w.Hq], qk_rot[:, :, w.Hq:]
+                sv["dqk"] = dqkv[:, :, :w.Hq + w.Hkv]
+        else:
+            sv["q"], sv["k"], sv["v"], sv["dout"] = in_views
+            sv["o"], sv["lse"], sv["dq"], sv["dk"], sv["dv"] = out_views
+        return sv
+
+    sets = [make_set(), make_set()]
+    for sv in sets:
+        sv["in"].copy_(in_h)
     ws = torch.empty(gqa.attn_bwd_workspace_bytes(w.B, w.T, w.Hq), dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     causal = w.causal
+    sv0 = sets[0]
 
-    def step(ev=None, rev=None):
+    def step(sv, ev=None, rev=None, public=False):
+        """One fwd + bwd on the buffers sv. ev: events between the kernels; public: the
+        calls a user makes (attn_fwd, attn_bwd) instead of the backward's two stages."""
+        q, k, v, o, lse, dout, dq, dk, dv = (sv[n] for n in ("q", "k", "v", "o", "lse", "dout", "dq", "dk", "dv"))
         if fused:
             if rope:
                 if rev is not None:
                     rev[0].record(stream)
-                gqa.attn_rope(qk_raw, table, y=qk_rot, stream=stream)
+                gqa.attn_rope(sv["qk_raw"], table, y=qk_rot, stream=stream)
                 if rev is not None:
                     rev[1].record(stream)
             # the strided backward is one call: its preprocess and main kernel share one interval
@@ -368,7 +418,7 @@ def run_ours(args, w):
             if rope:
                 if rev is not None:
                     rev[2].record(stream)
-                gqa.attn_rope(dqk, table, inverse=True, stream=stream)
+                gqa.attn_rope(sv["dqk"], table, inverse=True, stream=stream)
                 if rev is not None:
                     rev[3].record(stream)
             return
@@ -377,6 +427,9 @@ def run_ours(args, w):
         gqa.attn_fwd(q, k, v, causal=causal, o=o, lse=lse, stream=stream)
         if ev is not None:
             ev[1].record(stream)
+        if public:
+            gqa.attn_bwd(q, k, v, o, lse, dout, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+            return
         gqa.attn_bwd_preprocess(o, lse, dout, ws, stream=stream)
         if ev is not None:
             ev[2].record(stream)
@@ -385,7 +438,7 @@ def run_ours(args, w):
             ev[3].record(stream)
 
     for _ in range(max(args.warmup, 3)):
-        step()
+        step(sv0)
     torch.cuda.synchronize(dev)
     if gqa.attn_sync_status(stream) != gqa.GQA_OK:
         raise RuntimeError(gqa.attn_last_error())
@@ -397,17 +450,15 @@ def run_ours(args, w):
     # Timed region: one event pair per step (kernels back to back, so each kernel's
     # launch and prologue can overlap the previous kernel's tail).
     step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
+    ctx.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()  # L2 flush between timed steps, outside the events
         step_ev[i][0].record(stream)
-        step()
+        step(sv0)
         step_ev[i][1].record(stream)
-    if world > 1:
-        dist.barrier()
+    ctx.barrier()
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     # Per-kernel breakdown (events between the kernels) for the roofline, same workload.
@@ -415,14 +466,14 @@ def run_ours(args, w):
     rope_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for i in range(args.steps):
         flush.zero_()
-        step(events[i], rope_ev[i])
+        step(sv0, events[i], rope_ev[i])
     torch.cuda.synchronize(dev)
     # keep the GPU busy with identical untimed steps so the 100 ms clock sampler sees load
     t_soak = time.perf_counter()
     while sampler and time.perf_counter() - t_soak < max(0.0, 1.5 - wall):
         for _ in range(20):
             flush.zero_()
-            step()
+            step(sv0)
         torch.cuda.synchronize(dev)
     if sampler:
         sampler.stop()
@@ -447,10 +498,8 @@ def run_ours(args, w):
                      "achieved_gbs": rope_bytes / (rope_ms * 1e-3) / 1e9, "peak_gbs": peaks["hbm_gbs"],
                      "frac": rope_bytes / (rope_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
     step_ms = sorted(step_ev[i][0].elapsed_time(step_ev[i][1]) for i in range(args.steps))
-    ms_median = step_ms[len(step_ms) // 2] if len(step_ms) % 2 else 0.5 * (step_ms[len(step_ms) // 2 - 1]
-                                                                         + step_ms[len(step_ms) // 2])
-    step_ms_total = sum(step_ms)
-    step_ms_total = max_over_ranks(torch, dist, step_ms_total, world, dev)
+    ms_median = statistics.median(step_ms)
+    step_ms_total = max_over_ranks(torch, dist, sum(step_ms), world, dev)
     ms_per_step = step_ms_total / args.steps
     value = whole_job_tflops(world, step_flops(w), args.steps, step_ms_total)
     per_gpu = value / world
@@ -458,8 +507,6 @@ def run_ours(args, w):
     # roofline of the dominant kernel (largest share of the step)
     pairs = causal_pairs(w.T, w.causal)
     mm = 2.0 * w.B * w.Hq * pairs * w.d  # one causal matmul over all heads
-    kflops = {"attn_fwd_kernel": 2 * mm, "bwd_main_kernel": 7 * mm,  # dQ tasks 3 matmuls, dK/dV tasks 4
-              "bwd_pre_kernel+bwd_main_kernel": 7 * mm}
     pre_bytes = 2 * w.B * w.T * w.Hq * w.d * 2 + w.B * w.Hq * w.T * 4 + 2 * w.B * w.Hq * w.T * 4
     dom = max(per_kernel, key=per_kernel.get)
     avg_ms = per_kernel[dom] / args.steps
@@ -467,92 +514,150 @@ def run_ours(args, w):
         achieved = pre_bytes / (avg_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     else:
-        achieved = kflops[dom] / (avg_ms * 1e-3) / 1e12
+        achieved = CREDITED_MATMULS[dom] * mm / (avg_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_src} burst" if roof["bound"] == "tensor" else peak_src
-    roof["traffic"] = None if fused else recorded_traffic(dom, w.name)
+    rec = None if fused else recorded_counters(dom, w.name)
+    roof["traffic"] = None if rec is None else rec.get("dram_bytes_per_launch")
+    if roof["bound"] == "tensor":
+        # the same kernel time with the matmuls it runs, and against the sustained peak
+        roof["credited_matmuls"] = CREDITED_MATMULS[dom]
+        roof["executed_matmuls"] = EXECUTED_MATMULS[dom]
+        roof["executed_frac"] = EXECUTED_MATMULS[dom] * mm / (avg_ms * 1e-3) / 1e12 / roof["peak"]
+        sus = peaks.get("bf16_tflops_sustained")
+        roof["frac_of_sustained"] = roof["achieved"] / sus if sus else None
+        roof["tensor_active_pct_ncu"] = None if rec is None else rec.get("tensor_active_pct")
     kernel_ms = {n: t / args.steps for n, t in per_kernel.items()}
     bwd_ms = kernel_ms["bwd_pre_kernel+bwd_main_kernel"] if fused else (
         kernel_ms["bwd_pre_kernel"] + kernel_ms["bwd_main_kernel"])
+    fwd_tf = fwd_flops(w) / (kernel_ms["attn_fwd_kernel"] * 1e-3) / 1e12
+    bwd_tf = 2.5 * fwd_flops(w) / (bwd_ms * 1e-3) / 1e12
 
-    # end to end through the public API with host buffers (pinned), copies inside the timed region
-    out_h, _ = packed_buffer(torch, out_specs, pin=True)
-    h2d = in_h.numel()
-    d2h = out_h.numel()
-
-    def e2e_step():
-        in_d.copy_(in_h, non_blocking=True)
-        if fused:
-            step()
-        else:
-            gqa.attn_fwd(q, k, v, causal=causal, o=o, lse=lse, stream=stream)
-            gqa.attn_bwd(q, k, v, o, lse, dout, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
-        out_h.copy_(out_d, non_blocking=True)
-
-    for _ in range(0 if args.profile_run else 3):
-        e2e_step()
-    e_steps = 0 if args.profile_run else max(3, args.steps // 2)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    te_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1), world, dev)
-    e2e_value = whole_job_tflops(world, step_flops(w), e_steps, te_ms) if e_steps else None
+    e2e = e2e_leg(args, ctx, w, sets, in_h, out_specs, step)
 
     cpu = None
-    if rank == 0 and world == 1 and not (args.no_cpu_baseline or args.profile_run):
-        s = oracle_sample(w, min_seconds=10.0, max_seconds=30.0)
+    if rank == 0 and world == 1 and cpu_seconds > 0 and not (args.no_cpu_baseline or args.profile_run):
+        s = oracle_sample(w, min_seconds=cpu_seconds, max_seconds=3 * cpu_seconds)
         cpu = {"value": s["value"], "unit": "TFLOP/s", "cores": s["cores"], "kind": "oracle", "sample": s["sample"]}
 
-    if rank == 0:
-        clocks = sampler.summary() if sampler else None
-        line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_median": ms_median,
-            "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config_dict(w, {"l2": "flushed between timed steps (256 MB write, outside the events)",
-                                      "rope": "q, k rotated before and dq, dk after attention (in the step)"
-                                      if rope else "none",
-                                      "layout": "fused qkv / dqkv buffers, strided views" if fused
-                                      else "separate contiguous q, k, v, dq, dk, dv",
-                                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
-            # the same step counted with the exact number of causal pairs, T(T+1)/2
-            "value_exact_pairs": value * ((w.T + 1) / w.T if w.causal else 1.0),
-            "pct_of_peak": 100.0 * per_gpu / peaks["bf16_tflops"],
-            "peak_tflops": peaks["bf16_tflops"], "peak_source": f"{peak_src} burst",
-            "fwd_tflops": fwd_flops(w) / (kernel_ms["attn_fwd_kernel"] * 1e-3) / 1e12,
-            "bwd_tflops": 2.5 * fwd_flops(w) / (bwd_ms * 1e-3) / 1e12,
-            "kernel_ms": kernel_ms,
-            "roofline": roof,
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": (5 if rope else 3) * args.steps,
-            "rope": rope_info,
-            "clocks": clocks,
-            "wall_s_timed": wall,
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
+    del sets, ws
+    if rank != 0:
+        return None
+    clocks = sampler.summary() if sampler else None
+    peak = peaks["bf16_tflops"]
+    return {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_median": ms_median,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(w, {"l2": "flushed between timed steps (256 MB write, outside the events)",
+                                  "rope": "q, k rotated before and dq, dk after attention (in the step)"
+                                  if rope else "none",
+                                  "layout": "fused qkv / dqkv buffers, strided views" if fused
+                                  else "separate contiguous q, k, v, dq, dk, dv",
+                                  "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+        # the same step counted with the exact number of causal pairs, T(T+1)/2
+        "value_exact_pairs": value * ((w.T + 1) / w.T if w.causal else 1.0),
+        "pct_of_peak": 100.0 * per_gpu / peak,
+        "peak_tflops": peak, "peak_source": f"{peak_src} burst",
+        "fwd_tflops": fwd_tf, "fwd_pct_of_peak": 100.0 * fwd_tf / peak,
+        "bwd_tflops": bwd_tf, "bwd_pct_of_peak": 100.0 * bwd_tf / peak,
+        "kernel_ms": kernel_ms,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": (5 if rope else 3) * args.steps,
+        "rope": rope_info,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+    }
+
+
+def e2e_leg(args, ctx, w, sets, in_h, out_specs, step):
+    """The metric end to end through the public calls (attn_fwd, attn_bwd), with every
+    step's inputs copied in from pinned host memory and its outputs copied back out.
+    Two device buffer sets and two pinned output buffers alternate, and the copies run
+    on two copy streams (one each way), so step i+1's upload and step i-1's download
+    overlap step i's kernels, as a trainer feeding the GPU would overlap them."""
+    torch, dist = ctx.torch, ctx.dist
+    if args.profile_run:
+        return {"value": None, "unit": "TFLOP/s", "h2d_bytes_per_step": in_h.numel(),
+                "d2h_bytes_per_step": None}
+    dev, stream = ctx.dev, torch.cuda.current_stream(ctx.dev)
+    outs_h = [packed_buffer(torch, out_specs, pin=True)[0] for _ in range(2)]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    Ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def run(n):
+        ev_in, ev_used, ev_out = [Ev(), Ev()], [Ev(), Ev()], [Ev(), Ev()]
+        e0, e1 = Ev(), Ev()
+        e0.record(up)
+        with torch.cuda.stream(up):
+            sets[0]["in"].copy_(in_h, non_blocking=True)
+        ev_in[0].record(up)
+        for i in range(n):
+            b = i & 1
+            if i + 1 < n:
+                # next step's inputs into the other set, once step i-1 no longer reads them
+                if i >= 1:
+                    up.wait_event(ev_used[1 - b])
+                with torch.cuda.stream(up):
+                    sets[1 - b]["in"].copy_(in_h, non_blocking=True)
+                ev_in[1 - b].record(up)
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_out[b])  # outputs of step i-2 are out of this set
+            step(sets[b], public=True)
+            ev_used[b].record(stream)
+            down.wait_event(ev_used[b])
+            with torch.cuda.stream(down):
+                outs_h[b].copy_(sets[b]["out"], non_blocking=True)
+            ev_out[b].record(down)
+        e1.record(down)  # the last download comes after every other copy and kernel
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+
+    run(3)
+    n = max(3, args.steps // 2)
+    ctx.barrier()
+    torch.cuda.synchronize(dev)
+    te_ms = max_over_ranks(torch, dist, run(n), ctx.world, dev)
+    return {"value": whole_job_tflops(ctx.world, step_flops(w), n, te_ms), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": in_h.numel(), "d2h_bytes_per_step": outs_h[0].numel(),
+            "ms_per_step": te_ms / n,
+            "overlap": "double-buffered: uploads and downloads on their own streams, beside the kernels"}
+
+
+def run_ours(args, names):
+    ctx = Context(args)
+    from causal_gqa_flash_gb300.inputs import WORKLOADS
+    for i, name in enumerate(names):
+        last = i + 1 == len(names)
+        line = run_workload(args, ctx, WORKLOADS[name], cpu_seconds=10.0 if last else 5.0)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        ctx.torch.cuda.empty_cache()
+    if ctx.world > 1:
+        ctx.barrier()
+        ctx.dist.destroy_process_group()
     return 0
+
+
+ALL_ORDER = ["c1", "c2", "c3", "c5", "c4"]  # the headline workload last
 
 
 def main():
     args = parse_args()
     from causal_gqa_flash_gb300.inputs import WORKLOADS
-    w = WORKLOADS[args.workload]
+    names = ALL_ORDER if args.workload == "all" else [args.workload]
+    for n in names:
+        if n not in WORKLOADS:
+            raise SystemExit(f"unknown workload {n!r} (c1..c5 or all)")
     if args.impl == "reference":
-        return run_reference(args, w)
-    return run_ours(args, w)
+        return run_reference(args, WORKLOADS[names[-1]])
+    return run_ours(args, names)
 
 
 if __name__ == "__main__":

@@ -125,6 +125,20 @@ gqa_status_t device_state(const char* fn, DeviceState** out) {
   return GQA_OK;
 }
 
+}  // namespace
+
+namespace gqa {
+// The per-device check of every entry point, for other translation units: GQA_OK
+// when the current device is in range and of compute capability 10.3, otherwise
+// the error code with attn_last_error() set, naming `fn`.
+gqa_status_t check_current_device(const char* fn) {
+  DeviceState* ds = nullptr;
+  return device_state(fn, &ds);
+}
+}  // namespace gqa
+
+namespace {
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 gqa_status_t check_shape(const char* fn, int B, int T, int Hq, int Hkv, int d) {
@@ -205,7 +219,7 @@ gqa_status_t make_map(const char* fn, const char* name, CUtensorMap* m, const Vi
 
 size_t round_up_tile(int T) { return ((size_t)T + kTile - 1) / kTile * kTile; }
 // Task counters of the persistent dQ / dK/dV launch, after the two fp32 arrays.
-constexpr size_t kSchedBytes = 256;
+constexpr size_t kSchedBytes = kBwdSchedBytes;
 
 }  // namespace
 

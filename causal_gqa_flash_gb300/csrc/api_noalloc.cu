@@ -24,7 +24,8 @@
 #include "attn_common.cuh"
 
 namespace gqa {
-void set_last_error_message(const char* msg);  // defined in api.cu
+void set_last_error_message(const char* msg);        // defined in api.cu
+gqa_status_t check_current_device(const char* fn);   // defined in api.cu
 }
 
 namespace {
@@ -50,19 +51,29 @@ extern "C" gqa_status_t attn_bwd_noalloc(const void* q, const void* k, const voi
     return GQA_ERR_INVALID_ARG;
   }
   if (need > kNoallocScratchBytes) {
+    // D and LSE2 take 8 bytes per padded row; the task counters take the rest
     snprintf(msg, sizeof(msg),
              "attn_bwd_noalloc: problem needs %zu bytes of scratch, more than the library's fixed %zu "
              "(B*Hq*roundup(T,128) must be <= %zu); use attn_bwd with a caller workspace",
-             need, kNoallocScratchBytes, kNoallocScratchBytes / 8);
+             need, kNoallocScratchBytes, (kNoallocScratchBytes - gqa::kBwdSchedBytes) / 8);
     gqa::set_last_error_message(msg);
     return GQA_ERR_INVALID_ARG;
   }
+  // Device range and compute capability first (GQA_ERR_UNSUPPORTED_DEVICE), so the
+  // symbol lookup below only ever runs on a device this library has code for.
+  const gqa_status_t ds = gqa::check_current_device("attn_bwd_noalloc");
+  if (ds != GQA_OK) return ds;
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  if (e != cudaSuccess) {
     snprintf(msg, sizeof(msg), "attn_bwd_noalloc: cudaGetDevice failed: %s", cudaGetErrorString(e));
     gqa::set_last_error_message(msg);
     return GQA_ERR_LAUNCH;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    snprintf(msg, sizeof(msg), "attn_bwd_noalloc: device %d out of range", dev);
+    gqa::set_last_error_message(msg);
+    return GQA_ERR_UNSUPPORTED_DEVICE;
   }
   void* scratch = nullptr;
   {

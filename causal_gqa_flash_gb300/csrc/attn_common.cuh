@@ -16,6 +16,9 @@ namespace gqa {
 constexpr int kTile = 128;
 // One 128-byte swizzle atom column block: 64 bf16 of the head dim, 128 rows.
 constexpr int kHalfTileBytes = kTile * 128;
+// Bytes at the end of the backward workspace that hold the persistent launch's
+// task counters.
+constexpr size_t kBwdSchedBytes = 256;
 
 enum KernelId : unsigned int {
   kKidFwd = 1,

@@ -66,6 +66,9 @@ gqa_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, floa
  * to 128] (D_i = rowsum(dO * O) and the LSE in log2 units) followed by 256
  * bytes of task counters. The caller allocates it; nothing in it needs to be
  * initialised (the preprocess writes all of it) or preserved.
+ * Ownership follows the CPU reference of "ptx_sass.cu" (Day 46: reading PTX
+ * and SASS, decayFoldCpu): the library never allocates, the caller owns every
+ * buffer, scratch included. Returns 0 when B, T or Hq is not positive.
  */
 size_t attn_bwd_workspace_bytes(int B, int T, int Hq);
 
@@ -226,7 +229,15 @@ gqa_status_t attn_bwd_naive(const void* q, const void* k, const void* v, const v
                             const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                             int B, int T, int Hq, int Hkv, int d, int causal, void* stream);
 
-/* Description of the last error returned on this host thread ("" if none). */
+/*
+ * Description of the last error returned on this host thread ("" if none).
+ * "Talking to the GPU", §One macro for every call: every driver call is
+ * checked, and a failure is reported with the call's name and the driver's
+ * own words for the error. Here the message names the entry point, the CUDA
+ * call or argument that failed and cudaGetErrorString / cudaGetErrorName of
+ * the code, and the caller gets it back instead of the process exiting.
+ * The string stays valid until the next call of this library on the thread.
+ */
 const char* attn_last_error(void);
 
 /*
@@ -234,6 +245,10 @@ const char* attn_last_error(void);
  * current device. Returns GQA_OK, GQA_ERR_TIMEOUT (a kernel gave up waiting;
  * attn_last_error() names the kernel and wait), or GQA_ERR_LAUNCH if the
  * synchronisation itself failed.
+ * The check after the work, as in "Talking to the GPU", §One macro for every
+ * call (each call's result is tested before going on), extended to what the
+ * kernels report: a bounded wait inside a kernel cannot return an error code,
+ * so it writes one into the status word that this call reads.
  */
 gqa_status_t attn_sync_status(void* stream);
 

@@ -85,14 +85,16 @@ def test_parity_workload(name):
     check_against_oracle(out, ref, name)
 
 
-def test_bit_identical_across_runs():
-    """No float atomics: three calls give the same bytes (fwd and bwd)."""
-    w = WORKLOADS["c2"]
+@pytest.mark.parametrize("name", ["c1", "c2"])
+def test_bit_identical_across_runs(name):
+    """No float atomics: three calls give the same bytes (fwd and bwd). The larger
+    workloads repeat in test_gpu_fullsize.py."""
+    w = WORKLOADS[name]
     q, k, v, dout = (x.to(DEV) for x in workload_inputs(w))
     outs = []
     for _ in range(3):
-        o, lse = gqa.attn_fwd(q, k, v, causal=True)
-        dq, dk, dv = gqa.attn_bwd(q, k, v, o, lse, dout, causal=True)
+        o, lse = gqa.attn_fwd(q, k, v, causal=w.causal)
+        dq, dk, dv = gqa.attn_bwd(q, k, v, o, lse, dout, causal=w.causal)
         torch.cuda.synchronize()
         outs.append([t.clone() for t in (o, lse, dq, dk, dv)])
     for other in outs[1:]:

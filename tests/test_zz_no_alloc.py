@@ -4,7 +4,9 @@ It is for callers that may not allocate device memory where they run the
 backward, so its scratch is a fixed array inside the library. Called through
 the C ABI twice in a row (different shapes, so the second call meets the
 first call's leftovers in the shared array), its dQ/dK/dV must agree with
-attn_bwd given a caller workspace, within the tolerance of the parity tests.
+attn_bwd given a caller workspace: the same kernels on the same inputs, so the
+same bytes (and therefore within the tolerance of the parity tests too). A
+warmed-up call must leave the device's free memory unchanged.
 This file is collected last on purpose.
 """
 import ctypes
@@ -45,8 +47,26 @@ def test_noalloc_matches_workspace_backward(lib, shapes):
         assert gqa.attn_sync_status() == gqa.GQA_OK, gqa.attn_last_error()
         for name, a, r in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
             err = rel_fro(f64(a), f64(r))
-            print(f"B={B} T={T} Hq={Hq} Hkv={Hkv} d={d} {name}: rel-F {err:.2e}, identical={torch.equal(a, r)}")
+            print(f"B={B} T={T} Hq={Hq} Hkv={Hkv} d={d} {name}: rel-F {err:.2e}")
             assert err <= TOL_GRAD, (name, err)
+            assert torch.equal(a.view(torch.int16), r.view(torch.int16)), name
+
+
+def test_noalloc_allocates_no_device_memory(lib):
+    B, T, Hq, Hkv, d = 2, 513, 6, 2, 64
+    q, k, v, dout = (x.to(DEV) for x in make_inputs(B, T, Hq, Hkv, d, seed=21))
+    o, lse = gqa.attn_fwd(q, k, v, causal=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    args = (_p(q), _p(k), _p(v), _p(o), _p(lse), _p(dout), _p(dq), _p(dk), _p(dv), B, T, Hq, Hkv, d, 1, stream)
+    assert lib.attn_bwd_noalloc(*args) == gqa.GQA_OK, gqa.attn_last_error()  # warm-up (symbol lookup)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info(DEV)[0]
+    assert lib.attn_bwd_noalloc(*args) == gqa.GQA_OK, gqa.attn_last_error()
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info(DEV)[0]
+    assert gqa.attn_sync_status() == gqa.GQA_OK, gqa.attn_last_error()
+    assert free1 == free0, (free0, free1)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lib):
@@ -55,4 +75,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
     assert gqa.attn_bwd_workspace_bytes(B, T, Hq) > gqa.NOALLOC_SCRATCH_BYTES
     rc = lib.attn_bwd_noalloc(*([fake] * 9), B, T, Hq, 2, 64, 1, None)
     assert rc == gqa.GQA_ERR_INVALID_ARG
-    assert "more than the library's fixed" in gqa.attn_last_error()
+    msg = gqa.attn_last_error()
+    assert "more than the library's fixed" in msg
+    # the row limit it states leaves room for the 256 bytes of task counters
+    assert f"<= {(gqa.NOALLOC_SCRATCH_BYTES - 256) // 8}" in msg, msg
