@@ -20,7 +20,7 @@ __all__ = [
     "NOALLOC_SCRATCH_BYTES",
     "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_last_error", "attn_version",
     "GqaView", "view_of", "attn_rope_table", "attn_rope", "attn_fwd_naive", "attn_bwd_naive",
-    "attn_naive_workspace_bytes", "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
+    "attn_naive_workspace_bytes", "probe_rates", "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
     "GQA_ERR_TIMEOUT",
 ]
 
@@ -37,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "attn_bwd_dq_dkv", "attn_bwd_noalloc", "attn_fwd_strided", "attn_bwd_strided", "attn_rope_table_bytes",
     "attn_rope_table", "attn_rope", "attn_naive_workspace_bytes", "attn_fwd_naive", "attn_bwd_naive",
     "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
-    "attn_set_wait_budget_ns", "attn_version",
+    "attn_set_wait_budget_ns", "attn_version", "attn_probe_mma", "attn_probe_ex2",
 )
 
 _lib = None
@@ -107,6 +107,10 @@ def load():
     lib.attn_set_wait_budget_ns.restype = None
     lib.attn_version.argtypes = []
     lib.attn_version.restype = ctypes.c_char_p
+    lib.attn_probe_mma.argtypes = [i, i, i, vp, vp]
+    lib.attn_probe_mma.restype = i
+    lib.attn_probe_ex2.argtypes = [i, vp, vp, vp]
+    lib.attn_probe_ex2.restype = i
     _lib = lib
     return lib
 
@@ -444,3 +448,36 @@ def attn_selftest_timeout(budget_ns: int, stream=None):
 
 def attn_set_wait_budget_ns(budget_ns: int):
     load().attn_set_wait_budget_ns(int(budget_ns))
+
+
+def probe_rates(iters: int = 4096, device=None):
+    """Measured rates of this GPU's units, one CTA per SM (attn_probe_mma, attn_probe_ex2):
+    tcgen05 bf16 MMA FLOP/cycle/SM for N = 64, 128, 256 with A in shared or tensor
+    memory, ex2 lanes/cycle/SM, and the SM clock seen during the MMA probes (MHz,
+    median over SMs). Returns a dict; the medians over SMs are reported."""
+    import statistics
+    import torch
+    lib = load()
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = torch.zeros((sms, 2), dtype=torch.int64, device=dev)
+    res = {"sms": sms, "mma": {}}
+    clocks = []
+    for a_tmem in (0, 1):
+        for n in (64, 128, 256):
+            _check(lib.attn_probe_mma(n, a_tmem, iters, _ptr(out), _stream_handle(None)))
+            _check(attn_sync_status())
+            rec = out.cpu().tolist()
+            flop = iters * 4 * 2.0 * 128 * n * 16
+            rate = statistics.median(flop / c for c, _ in rec)
+            clocks += [c / t * 1e3 for c, t in rec]
+            res["mma"][f"{'ts' if a_tmem else 'ss'}_n{n}"] = rate
+    cyc = torch.zeros(sms, dtype=torch.int64, device=dev)
+    sink = torch.zeros(4, dtype=torch.float32, device=dev)
+    _check(lib.attn_probe_ex2(iters, _ptr(cyc), _ptr(sink), _stream_handle(None)))
+    _check(attn_sync_status())
+    res["ex2_lanes_per_clk"] = statistics.median(1024 * 8 * iters / c for c in cyc.cpu().tolist())
+    res["sm_mhz_during_mma"] = statistics.median(clocks)
+    best = max(res["mma"].values())
+    res["mma_peak_tflops_at_probe_clock"] = best * sms * res["sm_mhz_during_mma"] * 1e6 / 1e12
+    return res

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libgqa_attn.so"
-SOURCES = ["attn_fwd.cu", "attn_bwd.cu", "rope.cu", "naive.cu", "api.cu", "api_noalloc.cu"]
+SOURCES = ["attn_fwd.cu", "attn_bwd.cu", "rope.cu", "naive.cu", "probe.cu", "api.cu", "api_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
 

@@ -689,7 +689,7 @@ gqa_status_t attn_sync_status(void* stream) {
   e = cudaMemcpy(&w, ds->status, sizeof(w), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(fn, "cudaMemcpy(status word)", e);
   if (w.code == kDevOk) return GQA_OK;
-  static const char* names[] = {"?", "attn_fwd", "bwd_preprocess", "bwd_main", "?", "?", "?", "?", "?",
+  static const char* names[] = {"?", "attn_fwd", "bwd_preprocess", "bwd_main", "?", "?", "?", "?", "probe",
                                 "selftest"};
   const char* kname = w.kernel < 10 ? names[w.kernel] : "?";
   DevStatusWord zero;
@@ -697,6 +697,41 @@ gqa_status_t attn_sync_status(void* stream) {
   e = cudaMemcpy(ds->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(fn, "cudaMemcpy(clear status word)", e);
   return fail(GQA_ERR_TIMEOUT, "%s: kernel %s gave up waiting (wait %u, block %u)", fn, kname, w.where, w.block);
+}
+
+gqa_status_t attn_probe_mma(int n, int a_tmem, int iters, void* out, void* stream) {
+  const char* fn = "attn_probe_mma";
+  t_last_error.clear();
+  if (n != 64 && n != 128 && n != 256) return fail(GQA_ERR_INVALID_ARG, "%s: n must be 64, 128 or 256 (got %d)", fn, n);
+  if (iters <= 0 || iters > (1 << 20)) return fail(GQA_ERR_INVALID_ARG, "%s: iters must be in [1, 2^20]", fn);
+  gqa_status_t s;
+  if ((s = check_ptr(fn, "out", out))) return s;
+  DeviceState* ds = nullptr;
+  if ((s = device_state(fn, &ds))) return s;
+  int sms = 0;
+  cudaError_t e = sm_count(&sms);
+  if (e != cudaSuccess) return cuda_fail(fn, "cudaDeviceGetAttribute", e);
+  e = launch_mma_probe(n, a_tmem ? 1 : 0, iters, out, ds->status, g_budget_ns.load(), sms,
+                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(fn, "kernel launch", e);
+  return GQA_OK;
+}
+
+gqa_status_t attn_probe_ex2(int iters, void* out, void* sink, void* stream) {
+  const char* fn = "attn_probe_ex2";
+  t_last_error.clear();
+  if (iters <= 0 || iters > (1 << 20)) return fail(GQA_ERR_INVALID_ARG, "%s: iters must be in [1, 2^20]", fn);
+  gqa_status_t s;
+  if ((s = check_ptr(fn, "out", out)) || (s = check_ptr(fn, "sink", sink))) return s;
+  DeviceState* ds = nullptr;
+  if ((s = device_state(fn, &ds))) return s;
+  int sms = 0;
+  cudaError_t e = sm_count(&sms);
+  if (e != cudaSuccess) return cuda_fail(fn, "cudaDeviceGetAttribute", e);
+  e = launch_ex2_probe(iters, static_cast<unsigned long long*>(out), static_cast<float*>(sink), sms,
+                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(fn, "kernel launch", e);
+  return GQA_OK;
 }
 
 gqa_status_t attn_selftest_timeout(unsigned long long budget_ns, void* stream) {

@@ -147,6 +147,12 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const BwdPreParams
 // (its last S/dP MMAs are done, the fixed operands may be replaced), acc_full
 // (its last gradient MMAs are done), acc_free (the epilogue has read its
 // accumulators, the next task's first gradient MMA may overwrite them).
+// The dK/dV stages at d = 128 (two stages of 72 KB: no room for a third) have a
+// barrier pair for dO and one for Q: the gradient MMAs run as a dV chain then a dK
+// chain, and dO's slot is refilled as soon as the dV chain is done, so the next
+// tile's dP MMA no longer waits for the whole stage to be reloaded (a clock trace
+// put that load on the tile loop's critical path; the kernel is 6.7% faster at
+// T = 8192 with identical results).
 //
 // TMEM columns (S and dP are 128 fp32 columns; P and dS 64 columns of bf16 pairs):
 //   dQ:        S [0,128) dP [128,256) dS [256,320) dQ [320,320+D)
@@ -188,6 +194,8 @@ struct MainCfg {
   // at d = 64 a single N = 128 chain over block-diagonal operands (half of it
   // multiplying zeros) measured 8-10% slower overall.
   static constexpr int kKvStages = (D == 64) ? 3 : 2;   // Q/dO stages
+  // d = 128: each stage's dO and Q have their own barriers (see MainBars)
+  static constexpr bool kSplitStage = (D == 128);
   static constexpr int kKvFixBytes = 2 * kTileBytes;
   static constexpr int kKvOffK = kAuxBytes;             // buffer 0; buffer f adds f * kKvFixBytes
   static constexpr int kKvOffV = kKvOffK + kTileBytes;
@@ -305,7 +313,11 @@ __device__ __forceinline__ void score_chunk(const uint32_t (&s)[32], const uint3
 struct MainBars {
   uint64_t task_full[2], task_empty[2];   // producer <-> every other warp: next task index
   uint64_t fixed_full[2], fixed_free[2];   // per fixed buffer: operands loaded / no longer read
-  uint64_t kv_full[3], kv_empty[3];        // dK/dV stage ring
+  // dK/dV stage ring. d = 64: q_full/q_empty cover the whole stage (Q, dO and their
+  // row terms). d = 128: q_* cover Q and -LSE2, do_* cover dO and -D, so the dO slot
+  // is refilled once the dV MMAs are done while the dK MMAs still read Q.
+  uint64_t q_full[3], q_empty[3];
+  uint64_t do_full[3], do_empty[3];
   uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];  // dQ K and V rings
   uint64_t sdp_full;  // MMA -> compute: S(G) and dP(G) are in TMEM
   uint64_t sdp_free;  // compute -> MMA: every thread has S(G), dP(G) in registers
@@ -468,21 +480,49 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
       };
       for (int it = 0; it < t.n_it && ok; ++it, ++kv_used) {
         const int st = kv_used % NKV, u = kv_used / NKV;
-        if (u > 0) ok = lane0_wait(&bars.kv_empty[st], (u - 1) & 1, ctx, 1, lane);
-        if (!ok) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bars.kv_full[st], 2 * Cfg::kTileBytes);
-          for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-            tma_load_4d(smem + Cfg::st_q(st) + hf * kHalfTileBytes, &p.tmap_q, &bars.kv_full[st], hf * 64, hq,
-                        qt * kTile, t.b);
-            tma_load_4d(smem + Cfg::st_do(st) + hf * kHalfTileBytes, &p.tmap_do, &bars.kv_full[st], hf * 64, hq,
-                        qt * kTile, t.b);
+        if constexpr (Cfg::kSplitStage) {
+          // dO and its row term first (the dP MMA needs them first, and their slot is
+          // freed by the dV MMAs), then Q and its row term (freed by the dK MMAs)
+          if (u > 0) ok = lane0_wait(&bars.do_empty[st], (u - 1) & 1, ctx, 1, lane);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars.do_full[st], Cfg::kTileBytes);
+            for (int hf = 0; hf < Cfg::kHalves; ++hf)
+              tma_load_4d(smem + Cfg::st_do(st) + hf * kHalfTileBytes, &p.tmap_do, &bars.do_full[st], hf * 64, hq,
+                          qt * kTile, t.b);
           }
-        }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          write_aux_row(smem + Cfg::st_qx(st), lane + 32 * k, vnl[k] * inv_sl2);
-          write_aux_row(smem + Cfg::st_dx(st), lane + 32 * k, -vd[k]);
+          for (int k = 0; k < 4; ++k) write_aux_row(smem + Cfg::st_dx(st), lane + 32 * k, -vd[k]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.do_full[st]);
+          if (u > 0) ok = lane0_wait(&bars.q_empty[st], (u - 1) & 1, ctx, 5, lane);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars.q_full[st], Cfg::kTileBytes);
+            for (int hf = 0; hf < Cfg::kHalves; ++hf)
+              tma_load_4d(smem + Cfg::st_q(st) + hf * kHalfTileBytes, &p.tmap_q, &bars.q_full[st], hf * 64, hq,
+                          qt * kTile, t.b);
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) write_aux_row(smem + Cfg::st_qx(st), lane + 32 * k, vnl[k] * inv_sl2);
+        } else {
+          if (u > 0) ok = lane0_wait(&bars.q_empty[st], (u - 1) & 1, ctx, 1, lane);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars.q_full[st], 2 * Cfg::kTileBytes);
+            for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+              tma_load_4d(smem + Cfg::st_q(st) + hf * kHalfTileBytes, &p.tmap_q, &bars.q_full[st], hf * 64, hq,
+                          qt * kTile, t.b);
+              tma_load_4d(smem + Cfg::st_do(st) + hf * kHalfTileBytes, &p.tmap_do, &bars.q_full[st], hf * 64, hq,
+                          qt * kTile, t.b);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            write_aux_row(smem + Cfg::st_qx(st), lane + 32 * k, vnl[k] * inv_sl2);
+            write_aux_row(smem + Cfg::st_dx(st), lane + 32 * k, -vd[k]);
+          }
         }
         if (++qt_n == p.nT) {
           qt_n = t.i0;
@@ -493,7 +533,7 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
         qt = qt_n;
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.kv_full[st]);
+        if (lane == 0) mbar_arrive(&bars.q_full[st]);
       }
     } else {
       uint8_t* fix = smem + f * Cfg::kDqFixBytes;
@@ -546,7 +586,8 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
   }
   for (int s2 = 0; s2 < NKV && ok; ++s2) {
     const int uses = kv_used / NKV + (s2 < kv_used % NKV ? 1 : 0);
-    if (uses > 0) ok = mbar_wait(&bars.kv_empty[s2], (uses - 1) & 1, ctx, 4);
+    if (uses > 0) ok = mbar_wait(&bars.q_empty[s2], (uses - 1) & 1, ctx, 4);
+    if (Cfg::kSplitStage && ok && uses > 0) ok = mbar_wait(&bars.do_empty[s2], (uses - 1) & 1, ctx, 4);
   }
   for (int s2 = 0; s2 < NK && ok; ++s2) {
     const int uses = q_used / NK + (s2 < q_used % NK ? 1 : 0);
@@ -564,7 +605,8 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
     }
     for (int s2 = 0; s2 < NKV; ++s2) {
       const int uses = kv_used / NKV + (s2 < kv_used % NKV ? 1 : 0);
-      if (uses > 0) mbar_wait_drain(&bars.kv_full[s2], (uses - 1) & 1, p.budget_ns);
+      if (uses > 0) mbar_wait_drain(&bars.q_full[s2], (uses - 1) & 1, p.budget_ns);
+      if (Cfg::kSplitStage && uses > 0) mbar_wait_drain(&bars.do_full[s2], (uses - 1) & 1, p.budget_ns);
     }
     for (int s2 = 0; s2 < NK; ++s2) {
       const int uses = q_used / NK + (s2 < q_used % NK ? 1 : 0);
@@ -652,6 +694,19 @@ struct MmaCtx {
       mma_ss(dst, qXA_P + fo, ones, idesc_s, 1u);
     }
   }
+  // dK/dV gradient MMAs as two chains, dV first, with a commit on `do_free` between
+  // them so that the dO slot is refilled while the dK chain still reads Q.
+  __device__ __forceinline__ void grad_mmas_split(int bslot, bool first, uint64_t* do_free) const {
+    const uint32_t tP = tmem + Cfg::kKvColP, tDS = tmem + Cfg::kKvColDS;
+    const uint64_t g1 = kvG1 + bslot * kStG1, g2 = kvG2 + bslot * kStG2;
+#pragma unroll
+    for (int kk = 0; kk < kTile / 16; ++kk)
+      mma_ts(tmem + Cfg::kKvColDV, tP + kk * 8, g1 + kk * 128, idesc_g, (!first || kk > 0) ? 1u : 0u);
+    mma_commit(do_free);
+#pragma unroll
+    for (int kk = 0; kk < kTile / 16; ++kk)
+      mma_ts(tmem + Cfg::kKvColDK, tDS + kk * 8, g2 + kk * 128, idesc_g, (!first || kk > 0) ? 1u : 0u);
+  }
   // Gradient MMAs of one tile; `first` starts the task's accumulators.
   template <bool DKV>
   __device__ __forceinline__ void grad_mmas(int bslot, bool first) const {
@@ -709,7 +764,9 @@ __device__ __forceinline__ bool sdp_task(const MmaCtx<D>& m, MainBars& bars, con
     // Q/dO stage) operand is waited for first; in dQ tasks V only before dP, so
     // a late V tile (its ring is refilled only when dP(G-1) completes) does not
     // hold up S.
-    ok = warp_wait(DKV ? &bars.kv_full[rb.slot] : &bars.k_full[rb.slot], rb.phase, ctx, 11);
+    // dK/dV: the dP MMA needs dO (d = 128: its own barrier) and, at d = 64, the S MMA Q
+    ok = warp_wait(DKV ? (Cfg::kSplitStage ? &bars.do_full[rb.slot] : &bars.q_full[rb.slot]) : &bars.k_full[rb.slot],
+                   rb.phase, ctx, 11);
     if (ok && G > 0) ok = warp_wait(&bars.sdp_free, (G - 1) & 1, ctx, 14);
     if (!ok) break;
     tc_fence_after();
@@ -804,9 +861,12 @@ __device__ __forceinline__ bool grad_task(const MmaCtx<D>& m, MainBars& bars, co
       if (!ok) break;
       tc_fence_after();
       if (elect_one()) {
-        m.template grad_mmas<DKV>(rg.slot, it == 1);
+        if (DKV && Cfg::kSplitStage)
+          m.grad_mmas_split(rg.slot, it == 1, &bars.do_empty[rg.slot]);
+        else
+          m.template grad_mmas<DKV>(rg.slot, it == 1);
         mma_commit(&bars.pds_free);
-        mma_commit(DKV ? &bars.kv_empty[rg.slot] : &bars.k_empty[rg.slot]);
+        mma_commit(DKV ? &bars.q_empty[rg.slot] : &bars.k_empty[rg.slot]);
         if (it == n_it) mma_commit(&bars.acc_full);
       }
       __syncwarp();
@@ -815,7 +875,7 @@ __device__ __forceinline__ bool grad_task(const MmaCtx<D>& m, MainBars& bars, co
     }
     if (ok && s_here && it < n_it) {
       // S(it) overwrites the columns the gradient MMAs above read: same thread, in order
-      ok = warp_wait(&bars.kv_full[rs.slot], rs.phase, ctx, 18);
+      ok = warp_wait(&bars.q_full[rs.slot], rs.phase, ctx, 18);
       if (!ok) break;
       tc_fence_after();
       if (elect_one()) {
@@ -1051,8 +1111,10 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
       mbar_init(&bars.fixed_free[s], 2);  // one commit from each MMA issuer
     }
     for (int s = 0; s < 3; ++s) {
-      mbar_init(&bars.kv_full[s], 2);  // TMA bytes + the producer warp's aux operands
-      mbar_init(&bars.kv_empty[s], 1);
+      mbar_init(&bars.q_full[s], 2);  // TMA bytes + the producer warp's aux operands
+      mbar_init(&bars.q_empty[s], 1);
+      mbar_init(&bars.do_full[s], 2);
+      mbar_init(&bars.do_empty[s], 1);
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
     }

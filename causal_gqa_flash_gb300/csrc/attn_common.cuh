@@ -24,6 +24,7 @@ enum KernelId : unsigned int {
   kKidFwd = 1,
   kKidBwdPre = 2,
   kKidBwdMain = 3,
+  kKidProbe = 8,
   kKidSelfTest = 9,
 };
 
@@ -126,5 +127,8 @@ cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, int d, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_selftest_timeout(DevStatusWord* status, unsigned long long budget_ns, cudaStream_t stream);
+cudaError_t launch_mma_probe(int n, int a_tmem, int iters, void* out, DevStatusWord* status,
+                             unsigned long long budget_ns, int grid, cudaStream_t stream);
+cudaError_t launch_ex2_probe(int iters, unsigned long long* cycles, float* sink, int grid, cudaStream_t stream);
 
 }  // namespace gqa

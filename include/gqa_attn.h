@@ -261,6 +261,27 @@ gqa_status_t attn_sync_status(void* stream);
 gqa_status_t attn_selftest_timeout(unsigned long long budget_ns, void* stream);
 
 /*
+ * Rate probes ("Talking to the GPU", §The real tensor core peak: measure the
+ * unit's real rate with enough independent work per SM, over one wave, timed on
+ * the device). Each runs one CTA on every SM of the current device; `out` is a
+ * caller-owned device buffer with one record per SM (cudaDevAttrMultiProcessorCount
+ * records); nothing is allocated. Read the records after attn_sync_status().
+ *
+ * attn_probe_mma: one thread per SM issues `iters` x 4 tcgen05 MMAs (bf16 x bf16 ->
+ *   fp32, M = 128, N = n in {64, 128, 256}, K = 16 each; A from shared memory, or
+ *   from tensor memory when a_tmem != 0) into one accumulator and waits once for
+ *   the last. Record per SM: {u64 SM cycles, u64 global-timer ns} of the chain, so
+ *   FLOP/cycle/SM = iters * 4 * 2*128*n*16 / cycles and the clock = cycles / ns.
+ *   iters in [1, 2^20]; out 16 bytes per SM, 8-byte aligned (16 here: checked).
+ * attn_probe_ex2: 1024 threads per SM each run 8 independent chains of
+ *   ex2.approx.f32 for `iters` rounds. Record per SM: u64 SM cycles; ex2
+ *   lanes/cycle/SM = 1024 * 8 * iters / cycles. sink: 4 bytes of device memory
+ *   (written only to keep the chains alive).
+ */
+gqa_status_t attn_probe_mma(int n, int a_tmem, int iters, void* out, void* stream);
+gqa_status_t attn_probe_ex2(int iters, void* out, void* sink, void* stream);
+
+/*
  * Time budget of every pipeline wait, in nanoseconds (default 2e9). Applies
  * to launches made after the call, on every device. 0 restores the default.
  */

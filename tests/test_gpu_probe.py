@@ -1,0 +1,22 @@
+"""The rate probes run on every SM and report plausible rates: the tcgen05 MMA
+chain between 1/8 of and the nominal dense bf16 rate per SM (8192 FLOP per cycle at
+M = 128 with N >= 128), wider N never slower per FLOP than N = 64, the ex2 unit
+between 4 and 128 lanes per cycle per SM, and an SM clock of a few hundred MHz to
+a few GHz while the probes ran."""
+import pytest
+
+import causal_gqa_flash_gb300 as gqa
+
+pytestmark = pytest.mark.gpu
+
+
+def test_probe_rates():
+    gqa.build()
+    r = gqa.probe_rates(iters=1024)
+    print(r)
+    for key, rate in r["mma"].items():
+        assert 1024 < rate <= 8192 * 1.02, (key, rate)
+    assert r["mma"]["ss_n128"] >= 0.98 * r["mma"]["ss_n64"]
+    assert 4 <= r["ex2_lanes_per_clk"] <= 128
+    assert 300 < r["sm_mhz_during_mma"] < 3000
+    assert gqa.attn_sync_status() == gqa.GQA_OK

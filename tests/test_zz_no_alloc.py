@@ -1,12 +1,14 @@
 """The backward entry point that allocates nothing (attn_bwd_noalloc).
 
 It is for callers that may not allocate device memory where they run the
-backward, so its scratch is a fixed array inside the library. Called through
-the C ABI twice in a row (different shapes, so the second call meets the
-first call's leftovers in the shared array), its dQ/dK/dV must agree with
-attn_bwd given a caller workspace: the same kernels on the same inputs, so the
-same bytes (and therefore within the tolerance of the parity tests too). A
-warmed-up call must leave the device's free memory unchanged.
+backward, so its scratch is a fixed array inside the library. It runs the
+preprocess and the dQ and dK/dV task launch (attn_bwd_preprocess and
+attn_bwd_dq_dkv), whose scratch is small. Called through the C ABI twice in a
+row (different shapes, so the second call meets the first call's leftovers in
+the shared array), its dQ/dK/dV must equal those of the same two stages given
+a caller workspace (the same kernels on the same inputs: the same bytes), and
+agree with attn_bwd within the tolerance of the parity tests. A warmed-up call
+must leave the device's free memory unchanged.
 This file is collected last on purpose.
 """
 import ctypes
@@ -38,18 +40,22 @@ def test_noalloc_matches_workspace_backward(lib, shapes):
     for B, T, Hq, Hkv, d, seed in shapes:
         q, k, v, dout = (x.to(DEV) for x in make_inputs(B, T, Hq, Hkv, d, seed=seed))
         o, lse = gqa.attn_fwd(q, k, v, causal=True)
-        ref = gqa.attn_bwd(q, k, v, o, lse, dout, causal=True)  # caller-provided workspace
+        full = gqa.attn_bwd(q, k, v, o, lse, dout, causal=True)  # caller-provided workspace
+        ws = torch.empty(gqa.attn_bwd_workspace_bytes(B, T, Hq), dtype=torch.uint8, device=DEV)
+        ref = tuple(torch.empty_like(x) for x in (q, k, v))
+        gqa.attn_bwd_preprocess(o, lse, dout, ws)
+        gqa.attn_bwd_dq_dkv(q, k, v, dout, *ref, ws, causal=True)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
         rc = lib.attn_bwd_noalloc(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(dout), _p(dq), _p(dk), _p(dv), B, T, Hq,
                                   Hkv, d, 1, stream)
         assert rc == gqa.GQA_OK, gqa.attn_last_error()
         assert gqa.attn_sync_status() == gqa.GQA_OK, gqa.attn_last_error()
-        for name, a, r in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
-            err = rel_fro(f64(a), f64(r))
-            print(f"B={B} T={T} Hq={Hq} Hkv={Hkv} d={d} {name}: rel-F {err:.2e}")
+        for i, (name, a) in enumerate((("dq", dq), ("dk", dk), ("dv", dv))):
+            err = rel_fro(f64(a), f64(full[i]))
+            print(f"B={B} T={T} Hq={Hq} Hkv={Hkv} d={d} {name}: rel-F {err:.2e} against attn_bwd")
             assert err <= TOL_GRAD, (name, err)
-            assert torch.equal(a.view(torch.int16), r.view(torch.int16)), name
+            assert torch.equal(a.view(torch.int16), ref[i].view(torch.int16)), name
 
 
 def test_noalloc_allocates_no_device_memory(lib):
