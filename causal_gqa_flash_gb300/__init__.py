@@ -107,7 +107,7 @@ def load():
     lib.attn_set_wait_budget_ns.restype = None
     lib.attn_version.argtypes = []
     lib.attn_version.restype = ctypes.c_char_p
-    lib.attn_probe_mma.argtypes = [i, i, i, vp, vp]
+    lib.attn_probe_mma.argtypes = [i, i, i, i, vp, vp]
     lib.attn_probe_mma.restype = i
     lib.attn_probe_ex2.argtypes = [i, vp, vp, vp]
     lib.attn_probe_ex2.restype = i
@@ -453,8 +453,9 @@ def attn_set_wait_budget_ns(budget_ns: int):
 def probe_rates(iters: int = 4096, device=None):
     """Measured rates of this GPU's units, one CTA per SM (attn_probe_mma, attn_probe_ex2):
     tcgen05 bf16 MMA FLOP/cycle/SM for N = 64, 128, 256 with A in shared or tensor
-    memory, ex2 lanes/cycle/SM, and the SM clock seen during the MMA probes (MHz,
-    median over SMs). Returns a dict; the medians over SMs are reported."""
+    memory, into one accumulator or alternately into two, ex2 lanes/cycle/SM, and the
+    SM clock seen during the MMA probes (MHz, median over SMs). Returns a dict; the
+    medians over SMs are reported."""
     import statistics
     import torch
     lib = load()
@@ -463,15 +464,18 @@ def probe_rates(iters: int = 4096, device=None):
     out = torch.zeros((sms, 2), dtype=torch.int64, device=dev)
     res = {"sms": sms, "mma": {}}
     clocks = []
-    for a_tmem in (0, 1):
-        for n in (64, 128, 256):
-            _check(lib.attn_probe_mma(n, a_tmem, iters, _ptr(out), _stream_handle(None)))
-            _check(attn_sync_status())
-            rec = out.cpu().tolist()
-            flop = iters * 4 * 2.0 * 128 * n * 16
-            rate = statistics.median(flop / c for c, _ in rec)
-            clocks += [c / t * 1e3 for c, t in rec]
-            res["mma"][f"{'ts' if a_tmem else 'ss'}_n{n}"] = rate
+    for chains in (1, 2):
+        for a_tmem in (0, 1):
+            for n in (64, 128, 256):
+                if chains == 2 and a_tmem and n == 256:
+                    continue
+                _check(lib.attn_probe_mma(n, a_tmem, chains, iters, _ptr(out), _stream_handle(None)))
+                _check(attn_sync_status())
+                rec = out.cpu().tolist()
+                flop = iters * 4 * 2.0 * 128 * n * 16
+                rate = statistics.median(flop / c for c, _ in rec)
+                clocks += [c / t * 1e3 for c, t in rec]
+                res["mma"][f"{'ts' if a_tmem else 'ss'}_n{n}_{'one' if chains == 1 else 'two'}_acc"] = rate
     cyc = torch.zeros(sms, dtype=torch.int64, device=dev)
     sink = torch.zeros(4, dtype=torch.float32, device=dev)
     _check(lib.attn_probe_ex2(iters, _ptr(cyc), _ptr(sink), _stream_handle(None)))

@@ -699,10 +699,13 @@ gqa_status_t attn_sync_status(void* stream) {
   return fail(GQA_ERR_TIMEOUT, "%s: kernel %s gave up waiting (wait %u, block %u)", fn, kname, w.where, w.block);
 }
 
-gqa_status_t attn_probe_mma(int n, int a_tmem, int iters, void* out, void* stream) {
+gqa_status_t attn_probe_mma(int n, int a_tmem, int chains, int iters, void* out, void* stream) {
   const char* fn = "attn_probe_mma";
   t_last_error.clear();
   if (n != 64 && n != 128 && n != 256) return fail(GQA_ERR_INVALID_ARG, "%s: n must be 64, 128 or 256 (got %d)", fn, n);
+  if (chains != 1 && chains != 2) return fail(GQA_ERR_INVALID_ARG, "%s: chains must be 1 or 2 (got %d)", fn, chains);
+  if (chains == 2 && a_tmem && n == 256)
+    return fail(GQA_ERR_INVALID_ARG, "%s: two accumulators of N = 256 leave no TMEM columns for A", fn);
   if (iters <= 0 || iters > (1 << 20)) return fail(GQA_ERR_INVALID_ARG, "%s: iters must be in [1, 2^20]", fn);
   gqa_status_t s;
   if ((s = check_ptr(fn, "out", out))) return s;
@@ -711,7 +714,7 @@ gqa_status_t attn_probe_mma(int n, int a_tmem, int iters, void* out, void* strea
   int sms = 0;
   cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return cuda_fail(fn, "cudaDeviceGetAttribute", e);
-  e = launch_mma_probe(n, a_tmem ? 1 : 0, iters, out, ds->status, g_budget_ns.load(), sms,
+  e = launch_mma_probe(n, a_tmem ? 1 : 0, chains, iters, out, ds->status, g_budget_ns.load(), sms,
                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(fn, "kernel launch", e);
   return GQA_OK;

@@ -127,7 +127,7 @@ cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, int d, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream);
 cudaError_t launch_selftest_timeout(DevStatusWord* status, unsigned long long budget_ns, cudaStream_t stream);
-cudaError_t launch_mma_probe(int n, int a_tmem, int iters, void* out, DevStatusWord* status,
+cudaError_t launch_mma_probe(int n, int a_tmem, int chains, int iters, void* out, DevStatusWord* status,
                              unsigned long long budget_ns, int grid, cudaStream_t stream);
 cudaError_t launch_ex2_probe(int iters, unsigned long long* cycles, float* sink, int grid, cudaStream_t stream);
 

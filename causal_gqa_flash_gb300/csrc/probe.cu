@@ -21,8 +21,13 @@ struct MmaProbeOut {
   unsigned long long ns;      // the same interval in global-timer nanoseconds
 };
 
-// n: MMA N (64, 128 or 256); a_tmem: A operand from TMEM (TS) instead of shared memory (SS).
-__global__ void __launch_bounds__(kProbeThreads, 1) mma_probe_kernel(int n, int a_tmem, int iters, MmaProbeOut* out,
+// n: MMA N (64, 128 or 256); a_tmem: A operand from TMEM (TS) instead of shared memory (SS);
+// chains: 1 = every MMA accumulates into one accumulator (each waits for the previous
+// one's result), 2 = alternate between two accumulators (independent neighbours).
+// TMEM: accumulators at columns 0 and (n <= 128 ? 128 : 256); A at 256 (TS: n <= 128
+// when chains == 2).
+__global__ void __launch_bounds__(kProbeThreads, 1) mma_probe_kernel(int n, int a_tmem, int chains, int iters,
+                                                                     MmaProbeOut* out,
                                                                      DevStatusWord* status,
                                                                      unsigned long long budget_ns) {
   extern __shared__ uint8_t smem_raw[];
@@ -62,6 +67,7 @@ __global__ void __launch_bounds__(kProbeThreads, 1) mma_probe_kernel(int n, int 
     const uint64_t a_desc = sdesc_sw128(smem_u32(smem), 16, 1024);
     const uint64_t b_desc = sdesc_sw128(smem_u32(smem + 16 * 1024), 16, 1024);
     const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(n), 0, 0);
+    const uint32_t d1 = chains == 2 ? (n <= 128 ? 128u : 256u) : 0u;  // second accumulator
     uint64_t c0 = 0, t0 = 0;
     if (elect_one()) {
       c0 = clock64();
@@ -70,10 +76,12 @@ __global__ void __launch_bounds__(kProbeThreads, 1) mma_probe_kernel(int n, int 
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t off = static_cast<uint32_t>(kk * 32) >> 4;
+          const uint32_t d = (kk & 1) ? d1 : 0u;
+          const uint32_t acc = (it > 0 || kk > 1 || (chains == 1 && kk > 0)) ? 1u : 0u;
           if (a_tmem)
-            mma_ts(tmem, tmem + 256, b_desc + off, idesc, (it | kk) ? 1u : 0u);
+            mma_ts(tmem + d, tmem + 256, b_desc + off, idesc, acc);
           else
-            mma_ss(tmem, a_desc + off, b_desc + off, idesc, (it | kk) ? 1u : 0u);
+            mma_ss(tmem + d, a_desc + off, b_desc + off, idesc, acc);
         }
       }
       mma_commit(&bar_done);
@@ -122,13 +130,13 @@ __global__ void __launch_bounds__(1024, 1) ex2_probe_kernel(int iters, unsigned 
 // runs exactly one CTA (grid = the SM count).
 constexpr int kProbeSmem = 120 * 1024;
 
-cudaError_t launch_mma_probe(int n, int a_tmem, int iters, void* out, DevStatusWord* status,
+cudaError_t launch_mma_probe(int n, int a_tmem, int chains, int iters, void* out, DevStatusWord* status,
                              unsigned long long budget_ns, int grid, cudaStream_t stream) {
   constexpr int smem = kProbeSmem;
   cudaError_t e = cudaFuncSetAttribute(mma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  mma_probe_kernel<<<grid, kProbeThreads, smem, stream>>>(n, a_tmem, iters, static_cast<MmaProbeOut*>(out), status,
-                                                          budget_ns);
+  mma_probe_kernel<<<grid, kProbeThreads, smem, stream>>>(n, a_tmem, chains, iters, static_cast<MmaProbeOut*>(out),
+                                                          status, budget_ns);
   return cudaGetLastError();
 }
 

@@ -269,16 +269,18 @@ gqa_status_t attn_selftest_timeout(unsigned long long budget_ns, void* stream);
  *
  * attn_probe_mma: one thread per SM issues `iters` x 4 tcgen05 MMAs (bf16 x bf16 ->
  *   fp32, M = 128, N = n in {64, 128, 256}, K = 16 each; A from shared memory, or
- *   from tensor memory when a_tmem != 0) into one accumulator and waits once for
- *   the last. Record per SM: {u64 SM cycles, u64 global-timer ns} of the chain, so
- *   FLOP/cycle/SM = iters * 4 * 2*128*n*16 / cycles and the clock = cycles / ns.
- *   iters in [1, 2^20]; out 16 bytes per SM, 8-byte aligned (16 here: checked).
+ *   from tensor memory when a_tmem != 0) and waits once for the last. chains = 1:
+ *   all into one accumulator (each MMA needs the previous one's result); chains =
+ *   2: alternately into two (not with a_tmem at n = 256: no TMEM room). Record per
+ *   SM: {u64 SM cycles, u64 global-timer ns} of the chain, so FLOP/cycle/SM =
+ *   iters * 4 * 2*128*n*16 / cycles and the clock = cycles / ns.
+ *   iters in [1, 2^20]; out 16 bytes per SM, 16-byte aligned.
  * attn_probe_ex2: 1024 threads per SM each run 8 independent chains of
  *   ex2.approx.f32 for `iters` rounds. Record per SM: u64 SM cycles; ex2
  *   lanes/cycle/SM = 1024 * 8 * iters / cycles. sink: 4 bytes of device memory
  *   (written only to keep the chains alive).
  */
-gqa_status_t attn_probe_mma(int n, int a_tmem, int iters, void* out, void* stream);
+gqa_status_t attn_probe_mma(int n, int a_tmem, int chains, int iters, void* out, void* stream);
 gqa_status_t attn_probe_ex2(int iters, void* out, void* sink, void* stream);
 
 /*

@@ -16,7 +16,7 @@ def test_probe_rates():
     print(r)
     for key, rate in r["mma"].items():
         assert 1024 < rate <= 8192 * 1.02, (key, rate)
-    assert r["mma"]["ss_n128"] >= 0.98 * r["mma"]["ss_n64"]
+    assert r["mma"]["ss_n128_one_acc"] >= 0.98 * r["mma"]["ss_n64_one_acc"]
     assert 4 <= r["ex2_lanes_per_clk"] <= 128
     assert 300 < r["sm_mhz_during_mma"] < 3000
     assert gqa.attn_sync_status() == gqa.GQA_OK
