@@ -178,14 +178,12 @@ struct MainCfg {
   // Fixed operands of a task (dQ: Q, dO, QX, DX; dK/dV: K, V) are double-buffered
   // at d = 64, so the next task's are loaded while this task runs.
   static constexpr int kNF = (D == 64) ? 2 : 1;
-  // dQ task: fixed buffers [Q][dO][QX][DX], K ring, V ring
+  // dQ task: fixed buffers [Q][dO], K ring, V ring (its row terms stay in registers)
   static constexpr int kDqKStages = 3;
   static constexpr int kDqVStages = (D == 64) ? 2 : 1;
-  static constexpr int kDqFixBytes = 2 * kTileBytes + 2 * kAuxBytes;
+  static constexpr int kDqFixBytes = 2 * kTileBytes;
   static constexpr int kDqOffQ = kAuxBytes;  // buffer 0; buffer f adds f * kDqFixBytes
   static constexpr int kDqOffDO = kDqOffQ + kTileBytes;
-  static constexpr int kDqOffQX = kDqOffDO + kTileBytes;
-  static constexpr int kDqOffDX = kDqOffQX + kAuxBytes;
   static constexpr int kDqOffK = kAuxBytes + kNF * kDqFixBytes;
   static constexpr int kDqOffV = kDqOffK + kDqKStages * kTileBytes;
   static constexpr int kDqBytes = kDqOffV + kDqVStages * kTileBytes;
@@ -278,19 +276,27 @@ __device__ __forceinline__ void store_acc_bf16(const uint32_t (&r)[NC], __nv_bfl
   }
 }
 
-// This thread's 32 score columns of one tile. The accumulators already hold
-// S - LSE2/c and dP - D, so P = 2^(c * s') and dS = P * dp'. Columns outside
-// [lo, hi) of the warpgroup's frame are masked (MASKED only). Writes the bf16
-// pairs of P (dK/dV only) and dS.
+// This thread's 32 score columns of one tile. dK/dV tasks: the accumulators
+// already hold S - LSE2/c and dP - D (the row terms differ per column there and
+// were folded in by an extra K-step), so P = 2^(c * s') and dS = P * dp'. dQ
+// tasks: the thread's row is fixed for the whole task, so its row terms come in
+// as nl = -LSE2 and nd = -D and P = 2^(c * s + nl), dS = P * (dp + nd): no fold
+// MMA. Columns outside [lo, hi) of the warpgroup's frame are masked (MASKED
+// only). Writes the bf16 pairs of P (dK/dV only) and dS.
 template <bool DKV, bool MASKED>
 __device__ __forceinline__ void score_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32], float sl2, int lo,
-                                            int hi, uint32_t (&pk)[16], uint32_t (&dk)[16]) {
+                                            int hi, uint32_t (&pk)[16], uint32_t (&dk)[16], float nl = 0.f,
+                                            float nd = 0.f) {
   // column pairs through packed fp32 multiplies (same rounding as scalar ones)
   const uint64_t c2 = f2_make(sl2, sl2);
+  const uint64_t nl2 = f2_make(nl, nl), nd2 = f2_make(nd, nd);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     float x0, x1;
-    f2_split(f2_mul(f2_make(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2), x0, x1);
+    if (DKV)
+      f2_split(f2_mul(f2_make(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2), x0, x1);
+    else
+      f2_split(f2_fma(f2_make(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, nl2), x0, x1);
     float p0 = ex2_approx(x0);
     float p1 = ex2_approx(x1);
     if (MASKED) {
@@ -299,7 +305,11 @@ __device__ __forceinline__ void score_chunk(const uint32_t (&s)[32], const uint3
     }
     if (DKV) pk[i] = pack_bf16x2(p0, p1);
     float d0, d1;
-    f2_split(f2_mul(f2_make(p0, p1), f2_make(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1]))), d0, d1);
+    if (DKV)
+      f2_split(f2_mul(f2_make(p0, p1), f2_make(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1]))), d0, d1);
+    else
+      f2_split(f2_mul(f2_make(p0, p1), f2_add(f2_make(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])), nd2)),
+               d0, d1);
     dk[i] = pack_bf16x2(d0, d1);
   }
 }
@@ -417,16 +427,14 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
     // it from the ring.
     TaskInfo t{};
     if (id >= 0) t = decode_task(p, id);
-    // Row terms (-LSE2, D; 4 rows per lane) of the task's first query tile: of its
-    // own tile in a dQ task, of the first stage in a dK/dV task. Their loads are
-    // issued here so the latency overlaps the waits below instead of holding up
-    // the task's first operand loads.
+    // dK/dV task: row terms (-LSE2, D; 4 rows per lane) of its first stage's query
+    // tile. Their loads are issued here so the latency overlaps the waits below
+    // instead of holding up the task's first operand loads. (A dQ task's compute
+    // threads read their own row's terms.)
     float vnl[4], vd[4];
     const size_t vec_bh0 = (static_cast<size_t>(t.b) * p.Hq) * p.Tpad;
-    if (id >= 0) {
-      const int hq0 = t.dkv ? t.kvh * p.G : t.h;
-      const int qt0 = t.dkv ? t.i0 : t.tile;
-      const size_t vec = vec_bh0 + static_cast<size_t>(hq0) * p.Tpad + static_cast<size_t>(qt0) * kTile + lane;
+    if (id >= 0 && t.dkv) {
+      const size_t vec = vec_bh0 + static_cast<size_t>(t.kvh * p.G) * p.Tpad + static_cast<size_t>(t.i0) * kTile + lane;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         vnl[k] = __ldg(p.lse2 + vec + 32 * k);
@@ -542,6 +550,8 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
           tma_load_4d(fix + Cfg::kDqOffQ + hf * kHalfTileBytes, &p.tmap_q, fbar, hf * 64, t.h, t.tile * kTile, t.b);
           tma_load_4d(fix + Cfg::kDqOffDO + hf * kHalfTileBytes, &p.tmap_do, fbar, hf * 64, t.h, t.tile * kTile, t.b);
         }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(fbar);
       for (int j = 0; j < t.n_it && ok; ++j, ++q_used) {
         const int ks = q_used % NK, ku = q_used / NK;
         if (ku > 0) ok = lane0_wait(&bars.k_empty[ks], (ku - 1) & 1, ctx, 1, lane);
@@ -560,17 +570,6 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
           for (int hf = 0; hf < Cfg::kHalves; ++hf)
             tma_load_4d(smem + Cfg::kDqOffV + vs * Cfg::kTileBytes + hf * kHalfTileBytes, &p.tmap_v,
                         &bars.v_full[vs], hf * 64, t.kvh, j * kTile, t.b);
-        }
-        if (j == 0) {
-          // the row terms, once the first K and V tiles are on their way
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            write_aux_row(fix + Cfg::kDqOffQX, lane + 32 * k, vnl[k] * inv_sl2);
-            write_aux_row(fix + Cfg::kDqOffDX, lane + 32 * k, -vd[k]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(fbar);
         }
       }
     }
@@ -634,7 +633,7 @@ struct MmaCtx {
   // dK/dV descriptors (fixed buffer 0, stage 0)
   uint64_t kvA_S, kvA_P, kvB_S, kvB_P, kvG1, kvG2, kvXB_S, kvXB_P;
   // dQ descriptors (fixed buffer 0, ring slot 0)
-  uint64_t qA_S, qA_P, qB_S, qB_P, qG1, qXA_S, qXA_P;
+  uint64_t qA_S, qA_P, qB_S, qB_P, qG1;
   uint64_t ones;
 
   __device__ __forceinline__ void init(uint8_t* smem, uint32_t tm) {
@@ -654,10 +653,9 @@ struct MmaCtx {
     qB_S = sdesc_sw128(b + Cfg::kDqOffK, 16, 1024);             // K slot 0 (K-major)
     qB_P = sdesc_sw128(b + Cfg::kDqOffV, 16, 1024);             // V slot 0 (K-major)
     qG1 = sdesc_sw128(b + Cfg::kDqOffK, kHalfTileBytes, 1024);  // K slot 0 (MN-major) for dQ
-    qXA_S = sdesc_noswz(b + Cfg::kDqOffQX, 128, 256);           // QX x ONES^T -> -LSE2/c
-    qXA_P = sdesc_noswz(b + Cfg::kDqOffDX, 128, 256);           // DX x ONES^T -> -D
   }
-  // S = A_S B_S^T + aux into columns [0,128); f: fixed buffer, bslot: ring slot of B.
+  // S = A_S B_S^T (+ the row-term step for dK/dV) into columns [0,128); f: fixed
+  // buffer, bslot: ring slot of B.
   template <bool DKV>
   __device__ __forceinline__ void s_mmas(int f, int bslot) const {
     const uint32_t dst = tmem + Cfg::kColS;
@@ -673,7 +671,6 @@ struct MmaCtx {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(dst, qA_S + fo + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
-      mma_ss(dst, qXA_S + fo, ones, idesc_s, 1u);
     }
   }
   template <bool DKV>
@@ -691,7 +688,6 @@ struct MmaCtx {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(dst, qA_P + fo + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
-      mma_ss(dst, qXA_P + fo, ones, idesc_s, 1u);
     }
   }
   // dK/dV gradient MMAs as two chains, dV first, with a commit on `do_free` between
@@ -939,6 +935,13 @@ __device__ __forceinline__ bool compute_tiles(const BwdParams& p, MainBars& bars
   const uint32_t tP = tmem + lane_base + colP + wg * 16;
   const uint32_t tDS = tmem + lane_base + colDS + wg * 16;
   const float sl2 = p.scale_log2;
+  // dQ tasks: this thread's query row's -LSE2 and -D, applied in the score math
+  float nl = 0.f, nd = 0.f;
+  if (!DKV) {
+    const size_t idx = (static_cast<size_t>(t.b) * p.Hq + t.h) * p.Tpad + static_cast<size_t>(t.tile) * kTile + row;
+    nl = __ldg(p.lse2 + idx);
+    nd = -__ldg(p.Dvec + idx);
+  }
   // One tile: S, dP -> registers -> sdp_free; P, dS -> TMEM -> pds_full.
   auto tile = [&](int g, bool masked, int lo, int hi) -> bool {
     if (!warp_wait(&bars.sdp_full, g & 1, ctx, 20)) return false;
@@ -951,9 +954,9 @@ __device__ __forceinline__ bool compute_tiles(const BwdParams& p, MainBars& bars
     mbar_arrive(&bars.sdp_free);
     uint32_t pk[16], dk[16];
     if (masked)
-      score_chunk<DKV, true>(s, dp, sl2, lo, hi, pk, dk);
+      score_chunk<DKV, true>(s, dp, sl2, lo, hi, pk, dk, nl, nd);
     else
-      score_chunk<DKV, false>(s, dp, sl2, lo, hi, pk, dk);
+      score_chunk<DKV, false>(s, dp, sl2, lo, hi, pk, dk, nl, nd);
     // The P/dS region must be free: read by the gradient MMAs of g-1 (separate
     // region), or S(g) read by every warpgroup (region inside S; the gradient
     // MMAs of g-1 are complete there, since S(g) was issued after them by the
@@ -1107,7 +1110,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
       mbar_init(&bars.task_empty[s], kTaskConsumers);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars.fixed_full[s], 2);  // TMA bytes + the producer warp's own operands
+      mbar_init(&bars.fixed_full[s], 2);  // TMA bytes + the producer warp's arrival once all are issued
       mbar_init(&bars.fixed_free[s], 2);  // one commit from each MMA issuer
     }
     for (int s = 0; s < 3; ++s) {
