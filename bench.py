@@ -55,9 +55,11 @@ def parse_args():
     ap.add_argument("--layout", default="separate", choices=["separate", "fused"],
                     help="fused: q, k, v are views of one [B,T,Hq+2*Hkv,d] projection buffer and the gradients "
                          "go to one such buffer (attn_fwd_strided / attn_bwd_strided)")
-    ap.add_argument("--rope", action="store_true",
-                    help="with --layout fused: each step also rotates q and k (attn_rope, out of the projection "
-                         "buffer) before attention and rotates dq and dk back after it")
+    ap.add_argument("--rope", nargs="?", const="fused", default="none", choices=["none", "fused", "separate"],
+                    help="with --layout fused: each step also applies the rotary embedding to q and k. fused (the "
+                         "default of a bare --rope): attn_fwd_rope / attn_bwd_rope, the rotation inside the "
+                         "attention kernels (keys in one pass); separate: attn_rope before attention and its "
+                         "inverse on dq and dk after it")
     ap.add_argument("--profile-run", action="store_true",
                     help="timed steps only (no clock soak, e2e or oracle leg): the command profiled under ncu")
     return ap.parse_args()
@@ -358,10 +360,11 @@ def run_workload(args, ctx, w, cpu_seconds):
         for dst, src in zip(host_in, (q_c, k_c, v_c, do_c)):
             dst.copy_(src)
     del q_c, k_c, v_c, do_c
-    rope = fused and args.rope
-    if args.rope and not fused:
+    rope = args.rope if fused else "none"
+    if args.rope != "none" and not fused:
         raise SystemExit("--rope needs --layout fused")
-    table = gqa.attn_rope_table(w.T, w.d, device=dev) if rope else None
+    rope = None if rope == "none" else rope
+    table = gqa.attn_rope_table(w.T, w.d, device=dev) if rope == "separate" else None
     qk_rot = torch.empty((w.B, w.T, w.Hq + w.Hkv, w.d), dtype=torch.bfloat16, device=dev) if rope else None
     cut = (slice(0, w.Hq), slice(w.Hq, w.Hq + w.Hkv), slice(w.Hq + w.Hkv, H3))
 
@@ -375,12 +378,16 @@ def run_workload(args, ctx, w, cpu_seconds):
             sv["o"], sv["lse"], dqkv = out_views
             sv["q"], sv["k"], sv["v"] = (qkv[:, :, c] for c in cut)
             sv["dq"], sv["dk"], sv["dv"] = (dqkv[:, :, c] for c in cut)
-            if rope:
+            if rope == "separate":
                 # q and k rotated out of the projection buffer into their own buffer; dq and dk
                 # rotated back in place in the gradient buffer
                 sv["qk_raw"] = qkv[:, :, :w.Hq + w.Hkv]
                 sv["q"], sv["k"] = qk_rot[:, :, :w.Hq], qk_rot[:, :, w.Hq:]
                 sv["dqk"] = dqkv[:, :, :w.Hq + w.Hkv]
+            elif rope == "fused":
+                # the forward rotates q and k of the projection buffer into their own buffer,
+                # the backward takes those and writes dq, dk of the unrotated q, k
+                sv["q_rot"], sv["k_rot"] = qk_rot[:, :, :w.Hq], qk_rot[:, :, w.Hq:]
         else:
             sv["q"], sv["k"], sv["v"], sv["dout"] = in_views
             sv["o"], sv["lse"], sv["dq"], sv["dk"], sv["dv"] = out_views
@@ -398,6 +405,19 @@ def run_workload(args, ctx, w, cpu_seconds):
         """One fwd + bwd on the buffers sv. ev: events between the kernels; public: the
         calls a user makes (attn_fwd, attn_bwd) instead of the backward's two stages."""
         q, k, v, o, lse, dout, dq, dk, dv = (sv[n] for n in ("q", "k", "v", "o", "lse", "dout", "dq", "dk", "dv"))
+        if fused and rope == "fused":
+            if ev is not None:
+                ev[0].record(stream)
+            gqa.attn_fwd_rope(q, k, v, causal=causal, o=o, lse=lse, q_rot=sv["q_rot"], k_rot=sv["k_rot"],
+                              stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+                ev[2].record(stream)
+            gqa.attn_bwd_rope(sv["q_rot"], sv["k_rot"], v, o, lse, dout, causal=causal, dq=dq, dk=dk, dv=dv,
+                              workspace=ws, stream=stream)
+            if ev is not None:
+                ev[3].record(stream)
+            return
         if fused:
             if rope:
                 if rev is not None:
@@ -487,13 +507,21 @@ def run_workload(args, ctx, w, cpu_seconds):
         per_kernel = {"attn_fwd_kernel": per_kernel["attn_fwd_kernel"],
                       "bwd_pre_kernel+bwd_main_kernel": per_kernel["bwd_main_kernel"]}
     rope_info = None
-    if rope:
+    if rope == "fused":
+        # extra HBM bytes of the fused rotation per step: k read and k_rot written, q_rot
+        # written by the forward (the angles are computed in registers)
+        extra = (2 * w.Hkv + w.Hq) * w.B * w.T * w.d * 2
+        rope_info = {"mode": "fused", "calls_per_step": 2,
+                     "kernels": "rope_kernel on k (in the forward interval); q rotated inside attn_fwd_kernel, "
+                                "dq and dk inverse-rotated inside bwd_main_kernel",
+                     "extra_bytes_per_step": extra}
+    elif rope:
         rope_ms = sum(rope_ev[i][0].elapsed_time(rope_ev[i][1]) + rope_ev[i][2].elapsed_time(rope_ev[i][3])
                       for i in range(args.steps)) / args.steps
         # per step: q, k read and written, dq, dk read and written (bf16), and 32 table bytes
         # per 16-byte chunk of a token in each of the two calls
         rope_bytes = 4 * w.B * w.T * (w.Hq + w.Hkv) * w.d * 2 + 2 * w.B * w.T * w.d * 4
-        rope_info = {"kernel": "rope_kernel", "calls_per_step": 2, "ms_per_step": rope_ms,
+        rope_info = {"mode": "separate", "kernel": "rope_kernel", "calls_per_step": 2, "ms_per_step": rope_ms,
                      "bytes_per_step": rope_bytes, "bound": "hbm",
                      "achieved_gbs": rope_bytes / (rope_ms * 1e-3) / 1e9, "peak_gbs": peaks["hbm_gbs"],
                      "frac": rope_bytes / (rope_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
@@ -553,8 +581,9 @@ def run_workload(args, ctx, w, cpu_seconds):
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_dict(w, {"l2": "flushed between timed steps (256 MB write, outside the events)",
-                                  "rope": "q, k rotated before and dq, dk after attention (in the step)"
-                                  if rope else "none",
+                                  "rope": {"fused": "rotary embedding inside the attention kernels (in the step)",
+                                           "separate": "q, k rotated before and dq, dk after attention (in the step)",
+                                           None: "none"}[rope],
                                   "layout": "fused qkv / dqkv buffers, strided views" if fused
                                   else "separate contiguous q, k, v, dq, dk, dv",
                                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
@@ -568,7 +597,7 @@ def run_workload(args, ctx, w, cpu_seconds):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": (5 if rope else 3) * args.steps,
+        "gpu_launches": {"fused": 4, "separate": 5, None: 3}[rope] * args.steps,
         "rope": rope_info,
         "clocks": clocks,
         "wall_s_timed": wall,

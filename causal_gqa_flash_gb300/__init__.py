@@ -19,7 +19,7 @@ __all__ = [
     "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_dq_dkv", "attn_bwd_noalloc",
     "NOALLOC_SCRATCH_BYTES",
     "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_last_error", "attn_version",
-    "GqaView", "view_of", "attn_rope_table", "attn_rope", "attn_fwd_naive", "attn_bwd_naive",
+    "GqaView", "view_of", "attn_rope_table", "attn_rope", "attn_fwd_rope", "attn_bwd_rope", "attn_fwd_naive", "attn_bwd_naive",
     "attn_naive_workspace_bytes", "probe_rates", "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
     "GQA_ERR_TIMEOUT",
 ]
@@ -35,7 +35,7 @@ NOALLOC_SCRATCH_BYTES = 8 << 20  # GQA_NOALLOC_SCRATCH_BYTES in include/gqa_attn
 EXPORTED_SYMBOLS = (
     "attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv",
     "attn_bwd_dq_dkv", "attn_bwd_noalloc", "attn_fwd_strided", "attn_bwd_strided", "attn_rope_table_bytes",
-    "attn_rope_table", "attn_rope", "attn_naive_workspace_bytes", "attn_fwd_naive", "attn_bwd_naive",
+    "attn_rope_table", "attn_rope", "attn_fwd_rope", "attn_bwd_rope", "attn_naive_workspace_bytes", "attn_fwd_naive", "attn_bwd_naive",
     "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
     "attn_set_wait_budget_ns", "attn_version", "attn_probe_mma", "attn_probe_ex2",
 )
@@ -91,6 +91,11 @@ def load():
     lib.attn_rope_table.restype = i
     lib.attn_rope.argtypes = [gv, gv, vp, i, i, i, i, i, vp]
     lib.attn_rope.restype = i
+    dbl = ctypes.c_double
+    lib.attn_fwd_rope.argtypes = [gv, gv, gv, gv, vp, gv, gv, dbl, i, i, i, i, i, i, vp]
+    lib.attn_fwd_rope.restype = i
+    lib.attn_bwd_rope.argtypes = [gv, gv, gv, gv, vp, gv, gv, gv, gv, dbl, vp, sz, i, i, i, i, i, i, vp]
+    lib.attn_bwd_rope.restype = i
     lib.attn_naive_workspace_bytes.argtypes = [i, i, i]
     lib.attn_naive_workspace_bytes.restype = sz
     lib.attn_fwd_naive.argtypes = [vp] * 6 + [sz, i, i, i, i, i, i, vp]
@@ -236,7 +241,7 @@ def view_of(t, name: str = "tensor") -> GqaView:
 def _views(B, T, Hq, Hkv, d, extra=(), **named):
     """gqa_view_t of each named view after checking its shape ([B,T,Hq,d] for q-shaped
     names, [B,T,Hkv,d] for k-shaped ones), together with the extra argument specs."""
-    _args(*((name, t, (B, T, Hkv if name in ("k", "v", "dk", "dv") else Hq, d), _bf16(), False)
+    _args(*((name, t, (B, T, Hkv if name in ("k", "v", "dk", "dv", "k_rot") else Hq, d), _bf16(), False)
             for name, t in named.items()), *extra)
     return [view_of(t, name) for name, t in named.items()]
 
@@ -295,6 +300,45 @@ def attn_rope(x, table, y=None, inverse: bool = False, stream=None):
     _check(lib.attn_rope(view_of(x, "x"), view_of(y, "y"), _ptr(table), B, T, H, d, int(bool(inverse)),
                          _stream_handle(stream)))
     return y
+
+
+def attn_fwd_rope(q, k, v, base: float = 10000.0, causal: bool = True, o=None, lse=None, q_rot=None, k_rot=None,
+                  stream=None):
+    """Attention of the rotated q and k with the rotation fused in: q and k are the
+    unrotated projections (views allowed), rotated by angle t * base**(-2i/d) of pair i
+    of token t. Returns (o, lse, q_rot, k_rot); q_rot and k_rot (new tensors unless
+    given; q_rot=q / k_rot=k rotates in place) feed attn_bwd_rope."""
+    import torch
+    lib = load()
+    B, T, Hq, Hkv, d = _dims(q, k, v)
+    o = torch.empty(q.shape, dtype=q.dtype, device=q.device) if o is None else o
+    q_rot = torch.empty(q.shape, dtype=q.dtype, device=q.device) if q_rot is None else q_rot
+    k_rot = torch.empty(k.shape, dtype=k.dtype, device=k.device) if k_rot is None else k_rot
+    extra = () if lse is None else (("lse", lse, (B, Hq, T), _f32()),)
+    vq, vk, vv, vo, vqr, vkr = _views(B, T, Hq, Hkv, d, extra=extra, q=q, k=k, v=v, o=o, q_rot=q_rot, k_rot=k_rot)
+    if lse is None:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    _check(lib.attn_fwd_rope(vq, vk, vv, vo, _ptr(lse), vqr, vkr, float(base), B, T, Hq, Hkv, d, int(bool(causal)),
+                             _stream_handle(stream)))
+    return o, lse, q_rot, k_rot
+
+
+def attn_bwd_rope(q_rot, k_rot, v, o, lse, dout, base: float = 10000.0, causal: bool = True, dq=None, dk=None,
+                  dv=None, workspace=None, stream=None):
+    """Gradients of the UNROTATED q and k (and of v) from attn_fwd_rope's outputs (same
+    base); the inverse rotation runs in the backward kernel's epilogue. Returns (dq, dk, dv)."""
+    import torch
+    lib = load()
+    B, T, Hq, Hkv, d = _dims(q_rot, k_rot, v)
+    dq = torch.empty(q_rot.shape, dtype=q_rot.dtype, device=q_rot.device) if dq is None else dq
+    dk = torch.empty(k_rot.shape, dtype=k_rot.dtype, device=k_rot.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=v.dtype, device=v.device) if dv is None else dv
+    vq, vk, vv, vo, vdo, vdq, vdk, vdv = _views(B, T, Hq, Hkv, d, extra=(("lse", lse, (B, Hq, T), _f32()),),
+                                                q=q_rot, k=k_rot, v=v, o=o, dO=dout, dq=dq, dk=dk, dv=dv)
+    workspace = _workspace(workspace, B, T, Hq, q_rot.device)
+    _check(lib.attn_bwd_rope(vq, vk, vv, vo, _ptr(lse), vdo, vdq, vdk, vdv, float(base), _ptr(workspace),
+                             _ws_bytes(workspace), B, T, Hq, Hkv, d, int(bool(causal)), _stream_handle(stream)))
+    return dq, dk, dv
 
 
 def attn_naive_workspace_bytes(B: int, T: int, Hq: int) -> int:

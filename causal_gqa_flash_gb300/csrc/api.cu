@@ -218,6 +218,21 @@ gqa_status_t make_map(const char* fn, const char* name, CUtensorMap* m, const Vi
 }
 
 size_t round_up_tile(int T) { return ((size_t)T + kTile - 1) / kTile * kTile; }
+
+// Fixed-point rotary frequencies (RopeFreq) of head dim d: pair i turns by
+// base^(-2i/d) / (2 pi) per token, the same angles as attn_rope_table's.
+gqa_status_t rope_freq(const char* fn, double base, int d, RopeFreq* rf) {
+  if (!(base > 0.0) || !std::isfinite(base))
+    return fail(GQA_ERR_INVALID_ARG, "%s: base must be positive and finite (got %g)", fn, base);
+  memset(rf, 0, sizeof(*rf));
+  for (int i = 0; i < d / 2; ++i) {
+    const double turns = pow(base, -2.0 * i / d) / 6.283185307179586;  // per token, below 1/(2 pi)
+    const uint64_t f = static_cast<uint64_t>(ldexp(turns, 64));
+    rf->lo[i] = static_cast<uint32_t>(f);
+    rf->hi[i] = static_cast<uint32_t>(f >> 32);
+  }
+  return GQA_OK;
+}
 // Task counters of the persistent dQ / dK/dV launch, after the two fp32 arrays.
 constexpr size_t kSchedBytes = kBwdSchedBytes;
 
@@ -242,9 +257,11 @@ size_t attn_bwd_workspace_bytes(int B, int T, int Hq) {
 
 namespace {
 
-// Shape, pointers and views already checked.
+// Shape, pointers and views already checked. Rotary (rf != null): q is the
+// unrotated query, rotated in the kernel and written to q_rot; k is already rotated.
 gqa_status_t fwd_impl(const char* fn, const View& q, const View& k, const View& v, const View& o, float* lse, int B,
-                      int T, int Hq, int Hkv, int d, int causal, cudaStream_t stream) {
+                      int T, int Hq, int Hkv, int d, int causal, cudaStream_t stream, const View* q_rot = nullptr,
+                      const RopeFreq* rf = nullptr) {
   gqa_status_t s;
   DeviceState* ds = nullptr;
   if ((s = device_state(fn, &ds))) return s;
@@ -254,6 +271,12 @@ gqa_status_t fwd_impl(const char* fn, const View& q, const View& k, const View& 
       (s = make_map(fn, "v", &p.tmap_v, v, B, T, Hkv, d)))
     return s;
   if ((s = make_map(fn, "o", &p.tmap_o, o, B, T, Hq, d, 64, 32))) return s;  // epilogue stores (32-row boxes)
+  if (rf) {
+    // the rotated Q tile leaves in the same 128-row boxes it arrived in
+    if ((s = make_map(fn, "q_rot", &p.tmap_qrot, *q_rot, B, T, Hq, d))) return s;
+    p.rope = 1;
+    p.rope_f = *rf;
+  }
   p.lse = lse;
   p.B = B;
   p.T = T;
@@ -383,7 +406,8 @@ gqa_status_t bwd_preprocess_impl(const char* fn, const View& o, const float* lse
 // pointers of the views it uses already checked.
 gqa_status_t bwd_main_impl(const char* fn, int which, const View& q, const View& k, const View& v, const View& dO,
                            const View& dq, const View& dk, const View& dv, const void* workspace,
-                           size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, int causal, cudaStream_t st) {
+                           size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, int causal, cudaStream_t st,
+                           const RopeFreq* rf = nullptr) {
   gqa_status_t s;
   float *Dvec, *lse2;
   unsigned* sched;
@@ -402,6 +426,10 @@ gqa_status_t bwd_main_impl(const char* fn, int which, const View& q, const View&
   p.dk_sb = dk.sb;
   p.dv_st = dv.st;
   p.dv_sb = dv.sb;
+  if (rf) {
+    p.rope = 1;
+    p.rope_f = *rf;
+  }
   if (d == 64) {
     // d = 64 epilogues store through TMA, one 32-row box per compute warp: dQ 16
     // columns of a warpgroup, dK / dV 32 columns.
@@ -456,7 +484,8 @@ gqa_status_t bwd_stage(const char* fn, int which, const void* q, const void* k, 
 // The whole backward on checked views: everything is validated before the first launch.
 gqa_status_t bwd_impl(const char* fn, const View& q, const View& k, const View& v, const View& o, const float* lse,
                       const View& dO, const View& dq, const View& dk, const View& dv, void* workspace,
-                      size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, int causal, void* stream) {
+                      size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, int causal, void* stream,
+                      const RopeFreq* rf = nullptr) {
   gqa_status_t s;
   float *Dvec, *lse2;
   unsigned* sched;
@@ -464,7 +493,8 @@ gqa_status_t bwd_impl(const char* fn, const View& q, const View& k, const View& 
   if ((s = check_workspace(fn, workspace, workspace_bytes, B, T, Hq, &Dvec, &lse2, &Tpad, &sched))) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if ((s = bwd_preprocess_impl(fn, o, lse, dO, workspace, workspace_bytes, B, T, Hq, d, st))) return s;
-  return bwd_main_impl(fn, 3, q, k, v, dO, dq, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv, d, causal, st);
+  return bwd_main_impl(fn, 3, q, k, v, dO, dq, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv, d, causal, st,
+                       rf);
 }
 
 }  // namespace
@@ -526,6 +556,75 @@ gqa_status_t attn_bwd_strided(gqa_view_t q, gqa_view_t k, gqa_view_t v, gqa_view
     return s;
   return bwd_impl(fn, vq, vk, vv, vo, lse, vdo, vdq, vdk, vdv, workspace, workspace_bytes, B, T, Hq, Hkv, d, causal,
                   stream);
+}
+
+gqa_status_t attn_fwd_rope(gqa_view_t q, gqa_view_t k, gqa_view_t v, gqa_view_t o, float* lse, gqa_view_t q_rot,
+                           gqa_view_t k_rot, double base, int B, int T, int Hq, int Hkv, int d, int causal,
+                           void* stream) {
+  const char* fn = "attn_fwd_rope";
+  t_last_error.clear();
+  gqa_status_t s;
+  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
+  View vq, vk, vv, vo, vqr, vkr;
+  if ((s = check_view(fn, "q", q, B, T, Hq, d, false, &vq)) || (s = check_view(fn, "k", k, B, T, Hkv, d, false, &vk)) ||
+      (s = check_view(fn, "v", v, B, T, Hkv, d, false, &vv)) || (s = check_view(fn, "o", o, B, T, Hq, d, true, &vo)) ||
+      (s = check_ptr(fn, "lse", lse)) || (s = check_view(fn, "q_rot", q_rot, B, T, Hq, d, true, &vqr)) ||
+      (s = check_view(fn, "k_rot", k_rot, B, T, Hkv, d, true, &vkr)))
+    return s;
+  RopeFreq rf;
+  if ((s = rope_freq(fn, base, d, &rf))) return s;
+  if (vqr.ptr == vq.ptr && (vqr.st != vq.st || vqr.sb != vq.sb))
+    return fail(GQA_ERR_INVALID_ARG, "%s: in place (q_rot == q) needs the same strides for q and q_rot", fn);
+  if (vkr.ptr == vk.ptr && (vkr.st != vk.st || vkr.sb != vk.sb))
+    return fail(GQA_ERR_INVALID_ARG, "%s: in place (k_rot == k) needs the same strides for k and k_rot", fn);
+  if ((long long)B * T * ((Hkv + kRopeHeads - 1) / kRopeHeads) > 0x7fffffffLL / (d / 8))
+    return fail(GQA_ERR_INVALID_ARG, "%s: problem too large for the key rotation (B*T = %lld)", fn, (long long)B * T);
+  DeviceState* ds = nullptr;
+  if ((s = device_state(fn, &ds))) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Keys: one rotation pass (each key tile is read by every query tile of its
+  // group, so rotating it once beats rotating it at every load). Queries: rotated
+  // in the attention kernel as each tile arrives, and stored from there.
+  RopeParams rp;
+  memset(&rp, 0, sizeof(rp));
+  rp.x = vk.ptr;
+  rp.y = const_cast<void*>(vkr.ptr);
+  rp.x_st16 = vk.st / 8;
+  rp.x_sb16 = vk.sb / 8;
+  rp.y_st16 = vkr.st / 8;
+  rp.y_sb16 = vkr.sb / 8;
+  rp.table = nullptr;  // angles from rf, as in the attention kernels
+  rp.freq = rf;
+  rp.B = B;
+  rp.T = T;
+  rp.H = Hkv;
+  rp.inverse = 0;
+  cudaError_t e = launch_rope(rp, d, st);
+  if (e != cudaSuccess) return cuda_fail(fn, "key rotation launch", e);
+  return fwd_impl(fn, vq, vkr, vv, vo, lse, B, T, Hq, Hkv, d, causal, st, &vqr, &rf);
+}
+
+gqa_status_t attn_bwd_rope(gqa_view_t q_rot, gqa_view_t k_rot, gqa_view_t v, gqa_view_t o, const float* lse,
+                           gqa_view_t dO, gqa_view_t dq, gqa_view_t dk, gqa_view_t dv, double base,
+                           void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, int causal,
+                           void* stream) {
+  const char* fn = "attn_bwd_rope";
+  t_last_error.clear();
+  gqa_status_t s;
+  if ((s = check_shape(fn, B, T, Hq, Hkv, d))) return s;
+  View vq, vk, vv, vo, vdo, vdq, vdk, vdv;
+  if ((s = check_view(fn, "q_rot", q_rot, B, T, Hq, d, false, &vq)) ||
+      (s = check_view(fn, "k_rot", k_rot, B, T, Hkv, d, false, &vk)) ||
+      (s = check_view(fn, "v", v, B, T, Hkv, d, false, &vv)) || (s = check_view(fn, "o", o, B, T, Hq, d, false, &vo)) ||
+      (s = check_ptr(fn, "lse", lse)) || (s = check_view(fn, "dO", dO, B, T, Hq, d, false, &vdo)) ||
+      (s = check_view(fn, "dq", dq, B, T, Hq, d, true, &vdq)) ||
+      (s = check_view(fn, "dk", dk, B, T, Hkv, d, true, &vdk)) ||
+      (s = check_view(fn, "dv", dv, B, T, Hkv, d, true, &vdv)))
+    return s;
+  RopeFreq rf;
+  if ((s = rope_freq(fn, base, d, &rf))) return s;
+  return bwd_impl(fn, vq, vk, vv, vo, lse, vdo, vdq, vdk, vdv, workspace, workspace_bytes, B, T, Hq, Hkv, d, causal,
+                  stream, &rf);
 }
 
 size_t attn_naive_workspace_bytes(int B, int T, int Hq) {

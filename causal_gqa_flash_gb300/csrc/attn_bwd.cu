@@ -1036,7 +1036,27 @@ __device__ __forceinline__ void tma_store_rows(const uint32_t (&r)[NC], float sc
   }
 }
 
-template <int D, bool DKV>
+// Rotary embedding fused into the epilogue: the kernel differentiates with respect
+// to the rotated q and k, and the gradient of a rotation is the inverse rotation,
+// so NC accumulator columns of one row (feature pairs pair0, pair0 + 1, ...) turn
+// by minus the angles of its token `tok`, in fp32, before the one rounding to
+// bf16. The angles come from rope_cos_sin, in registers: a table lookup here sat
+// on the compute warps' path between two tasks.
+template <int NC>
+__device__ __forceinline__ void unrotate_acc(uint32_t (&r)[NC], int tok, int pair0, const RopeFreq& f) {
+  const uint32_t t = static_cast<uint32_t>(tok);
+#pragma unroll
+  for (int i = 0; i < NC / 2; ++i) {
+    float cs, sn;
+    rope_cos_sin(t, f.lo[pair0 + i], f.hi[pair0 + i], cs, sn);
+    float x0 = __uint_as_float(r[2 * i]), x1 = __uint_as_float(r[2 * i + 1]);
+    rope_rotate_f32(x0, x1, cs, -sn);
+    r[2 * i] = __float_as_uint(x0);
+    r[2 * i + 1] = __float_as_uint(x1);
+  }
+}
+
+template <int D, bool DKV, bool ROPE>
 __device__ __forceinline__ bool compute_epilogue(const BwdParams& p, MainBars& bars, uint32_t tmem, uint8_t* smem,
                                                  const WaitCtx& ctx, const TaskInfo& t, int n, int warp, int lane) {
   using Cfg = MainCfg<D>;
@@ -1044,16 +1064,21 @@ __device__ __forceinline__ bool compute_epilogue(const BwdParams& p, MainBars& b
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+  // columns of this thread's row: dK/dV NC = D/2 (part wg & 1), dQ NC = D/4 (wg)
+  constexpr int NC = DKV ? D / 2 : D / 4;
+  const int c0 = (DKV ? (wg & 1) : wg) * NC;
+  const bool unrot = ROPE && (!DKV || wg >= 2);  // dQ and dK, not dV
   if (!warp_wait(&bars.acc_full, n & 1, ctx, 21)) return false;
   tc_fence_after();
   if (DKV) {
-    constexpr int NC = D / 2;  // warpgroups 0, 1: dV halves; 2, 3: dK halves
+    // warpgroups 0, 1: dV halves; 2, 3: dK halves
     const int part = wg & 1;
     uint32_t r[NC];
     load_acc<NC>(tmem + lane_base + (wg < 2 ? Cfg::kKvColDV : Cfg::kKvColDK) + part * NC, r);
     tmem_wait_ld();
     tc_fence_before();
     mbar_arrive(&bars.acc_free);
+    if (unrot) unrotate_acc<NC>(r, t.tile * kTile + row, c0 / 2, p.rope_f);
     if constexpr (Cfg::kTmaStore) {
       tma_store_rows<NC>(r, wg < 2 ? 1.f : p.scale, smem + Cfg::kOffOut + (warp - 2) * Cfg::kOutWarpBytes,
                          wg < 2 ? &p.tmap_dv : &p.tmap_dk, part * NC, t.kvh, t.tile * kTile + quarter * 32, t.b,
@@ -1067,12 +1092,12 @@ __device__ __forceinline__ bool compute_epilogue(const BwdParams& p, MainBars& b
       store_acc_bf16<NC>(r, reinterpret_cast<__nv_bfloat16*>(wg < 2 ? p.dv : p.dk) + off, wg < 2 ? 1.f : p.scale);
     }
   } else {
-    constexpr int NC = D / 4;
     uint32_t r[NC];
     load_acc<NC>(tmem + lane_base + Cfg::kDqColAcc + wg * NC, r);
     tmem_wait_ld();
     tc_fence_before();
     mbar_arrive(&bars.acc_free);
+    if (unrot) unrotate_acc<NC>(r, t.tile * kTile + row, c0 / 2, p.rope_f);
     if constexpr (Cfg::kTmaStore) {
       tma_store_rows<NC>(r, p.scale, smem + Cfg::kOffOut + (warp - 2) * Cfg::kOutWarpBytes, &p.tmap_dq, wg * NC,
                          t.h, t.tile * kTile + quarter * 32, t.b, p.T, lane);
@@ -1087,7 +1112,9 @@ __device__ __forceinline__ bool compute_epilogue(const BwdParams& p, MainBars& b
   return true;
 }
 
-template <int D>
+// ROPE: dq and dk leave inverse-rotated (p.rope_f); a separate instance so that
+// the plain kernel's code is untouched by it.
+template <int D, bool ROPE>
 __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -1163,8 +1190,8 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
     bool ok = true;
     auto epilogue = [&](int tn) {
       const TaskInfo t = task_ring[tn & 3];
-      return t.dkv ? compute_epilogue<D, true>(p, bars, tmem, smem, ctx, t, tn, warp, lane)
-                   : compute_epilogue<D, false>(p, bars, tmem, smem, ctx, t, tn, warp, lane);
+      return t.dkv ? compute_epilogue<D, true, ROPE>(p, bars, tmem, smem, ctx, t, tn, warp, lane)
+                   : compute_epilogue<D, false, ROPE>(p, bars, tmem, smem, ctx, t, tn, warp, lane);
     };
     auto tiles = [&](const TaskInfo& t, int i0, int i1) {
       return t.dkv ? compute_tiles<D, true>(p, bars, tmem, ctx, t, G, i0, i1, warp, lane)
@@ -1225,6 +1252,13 @@ cudaError_t ensure_smem_attr(K kernel, int smem, int slot) {
 }
 
 
+template <int D, bool ROPE>
+cudaError_t launch_main(const BwdParams& p, unsigned grid, int attr_slot, cudaStream_t stream) {
+  cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, ROPE>, MainCfg<D>::kSmemBytes, attr_slot);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(bwd_main_kernel<D, ROPE>, grid, kMainThreads, MainCfg<D>::kSmemBytes, stream, p);
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_pre(const BwdPreParams& p, int d, cudaStream_t stream) {
@@ -1244,15 +1278,12 @@ cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream) {
   cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(n_tasks < sms ? n_tasks : sms);
-  if (d == 64) {
-    if ((e = ensure_smem_attr(bwd_main_kernel<64>, MainCfg<64>::kSmemBytes, 0)) != cudaSuccess) return e;
-    e = launch_pdl(bwd_main_kernel<64>, grid, kMainThreads, MainCfg<64>::kSmemBytes, stream, p);
-    if (e != cudaSuccess) return e;
-  } else {
-    if ((e = ensure_smem_attr(bwd_main_kernel<128>, MainCfg<128>::kSmemBytes, 1)) != cudaSuccess) return e;
-    e = launch_pdl(bwd_main_kernel<128>, grid, kMainThreads, MainCfg<128>::kSmemBytes, stream, p);
-    if (e != cudaSuccess) return e;
-  }
+  const bool rope = p.rope != 0;
+  if (d == 64)
+    e = rope ? launch_main<64, true>(p, grid, 2, stream) : launch_main<64, false>(p, grid, 0, stream);
+  else
+    e = rope ? launch_main<128, true>(p, grid, 3, stream) : launch_main<128, false>(p, grid, 1, stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

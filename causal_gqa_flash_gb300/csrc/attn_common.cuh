@@ -28,6 +28,15 @@ enum KernelId : unsigned int {
   kKidSelfTest = 9,
 };
 
+// Rotary frequencies as fixed-point turns: feature pair i of token t turns by
+// t * f_i turns, f_i = base^(-2i/d) / (2 pi), held to 64 bits (hi and lo words).
+// The fraction t * f_i mod 1 then comes out of two 32-bit integer multiplies,
+// exact to 2^-32 of a turn for any t, so the angle needs no floating-point range
+// reduction and no table in memory.
+struct RopeFreq {
+  uint32_t lo[64], hi[64];
+};
+
 // Forward: work items of one 128-query tile of one (query head, batch).
 // Tensors [B,T,H,d] bf16 are reached through TMA maps or through element strides
 // (token, batch) with the heads of one token packed (head stride d).
@@ -36,6 +45,9 @@ struct FwdParams {
   CUtensorMap tmap_k;  // [B,T,Hkv,d]
   CUtensorMap tmap_v;  // [B,T,Hkv,d]
   CUtensorMap tmap_o;  // [B,T,Hq,d], box 64 x 1 x 32 x 1 (epilogue stores)
+  CUtensorMap tmap_qrot;  // rotary only: [B,T,Hq,d] rotated Q out, boxes as tmap_q
+  int rope;              // 1: q is rotated in the kernel (rope_f) and stored to tmap_qrot
+  RopeFreq rope_f;
   float* lse;          // [B,Hq,T] fp32, natural log
   int B, T, Hq, Hkv, G, nT;
   int causal;
@@ -72,6 +84,8 @@ struct BwdParams {
   void* dq;            // [B,T,Hq,d]
   void* dk;            // [B,T,Hkv,d]
   void* dv;            // [B,T,Hkv,d]
+  int rope;            // 1: dq, dk leave inverse-rotated by rope_f's angles
+  RopeFreq rope_f;
   long long dq_st, dq_sb, dk_st, dk_sb, dv_st, dv_sb;  // element strides (token, batch) of the outputs
   int B, T, Hq, Hkv, G, nT, Tpad;
   int causal;
@@ -82,6 +96,30 @@ struct BwdParams {
   DevStatusWord* status;
   unsigned long long budget_ns;
 };
+
+// Rotary embedding of one bf16 pair (x0, x1) = (low, high half of w) by the angle
+// with cosine c and sine s: (x0 c - x1 s, x0 s + x1 c), products and sums in fp32,
+// each result rounded once to bf16. The standalone rotation and the forward's
+// fused one both call this, so they produce the same bits.
+__device__ __forceinline__ uint32_t rope_rotate_bf16x2(uint32_t w, float c, float s) {
+  const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xffff0000u);
+  return pack_bf16x2(fmaf(x0, c, -x1 * s), fmaf(x0, s, x1 * c));
+}
+
+// cos and sin of token t's angle for the pair with frequency (lo, hi) (see RopeFreq):
+// the turn fraction as a signed 32-bit fixed-point number in [-1/2, 1/2), scaled to
+// radians in [-pi, pi), where the hardware sine and cosine are accurate to ~2^-21.
+__device__ __forceinline__ void rope_cos_sin(uint32_t t, uint32_t lo, uint32_t hi, float& c, float& s) {
+  const int32_t turns = static_cast<int32_t>(__umulhi(t, lo) + t * hi);
+  __sincosf(static_cast<float>(turns) * 1.4629180792671596e-09f, &s, &c);  // 2 pi / 2^32
+}
+
+// The same rotation of an fp32 pair in place (the backward passes -s: the inverse).
+__device__ __forceinline__ void rope_rotate_f32(float& x0, float& x1, float c, float s) {
+  const float y0 = fmaf(x0, c, -x1 * s), y1 = fmaf(x0, s, x1 * c);
+  x0 = y0;
+  x1 = y1;
+}
 
 // Number of SMs of the current device (cached per device).
 inline cudaError_t sm_count(int* n) {

@@ -145,6 +145,35 @@ __device__ __forceinline__ FwdItem decode_item(const FwdParams& p, int id) {
   return it;
 }
 
+// Rotary embedding fused into the Q load: this thread's query row of the Q tile in
+// shared memory (128-byte swizzle: 16-byte chunk c of row r at c ^ (r & 7), one
+// 128-row box per 64 columns) turned by the angles of its token `tok`, computed in
+// registers (rope_cos_sin: nothing is read from memory on this path). Rows past T
+// hold TMA's zero fill and are left as they are (the rotated tile's store skips them).
+template <int D>
+__device__ __forceinline__ void rotate_q_row(uint8_t* q_tile, int row, int tok, int T, const RopeFreq& f) {
+  if (tok >= T) return;
+  const uint32_t t = static_cast<uint32_t>(tok);
+#pragma unroll
+  for (int hf = 0; hf < D / 64; ++hf) {
+    uint8_t* base = q_tile + hf * kHalfTileBytes + row * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4* ptr = reinterpret_cast<uint4*>(base + ((c ^ (row & 7)) * 16));
+      uint4 v = *ptr;
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = hf * 32 + c * 4 + j;  // feature pair (2i, 2i+1)
+        float cs, sn;
+        rope_cos_sin(t, f.lo[i], f.hi[i], cs, sn);
+        w[j] = rope_rotate_bf16x2(w[j], cs, sn);
+      }
+      *ptr = v;
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using Cfg = FwdCfg<D>;
@@ -158,7 +187,9 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
   // last PV is done), bar_ofree (the softmax holds O in registers). Per tile,
   // counted over the CTA's items: bar_s (S in TMEM), bar_sfree (every softmax
   // thread holds S; d = 64), bar_p (P in TMEM), bar_pfree (PV done; d = 64).
-  __shared__ uint64_t bar_q, bar_qfree, bar_kf[KS], bar_ke[KS], bar_vf[VS], bar_ve[VS], bar_s, bar_sfree, bar_p,
+  // With the rotary embedding, bar_qrot (every softmax thread has rotated its
+  // row of Q) takes bar_q's place for the MMA warp.
+  __shared__ uint64_t bar_q, bar_qrot, bar_qfree, bar_kf[KS], bar_ke[KS], bar_vf[VS], bar_ve[VS], bar_s, bar_sfree, bar_p,
       bar_pfree, bar_o, bar_ofree, bar_drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -173,6 +204,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_qrot, 128);
     mbar_init(&bar_qfree, 1);
     for (int s = 0; s < KS; ++s) { mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1); }
     for (int s = 0; s < VS; ++s) { mbar_init(&bar_vf[s], 1); mbar_init(&bar_ve[s], 1); }
@@ -195,6 +227,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const WaitCtx ctx{&abort_sh, p.status, p.budget_ns, kKidFwd};
+  const bool rope = p.rope != 0;
   pdl_wait_previous();  // inputs may be written by the previous kernel; outputs may still be read by it
 
   if (warp == 0) {
@@ -263,6 +296,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
     const uint64_t dK = sdesc_sw128(smem_u32(smem + Cfg::kOffK), 16, 1024);
     const uint64_t dV = sdesc_sw128(smem_u32(smem + Cfg::kOffV), kHalfTileBytes, 1024);
     constexpr uint32_t kTileD = Cfg::kTileBytes >> 4;  // descriptor units
+    if (rope && lane == 0) tma_prefetch_desc(&p.tmap_qrot);
     bool issued = false;
     auto commit = [&](uint64_t* bar) {
       if (elect_one()) mma_commit(bar);
@@ -275,6 +309,11 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
       if (!warp_wait(&bar_kf[ks], (g / KS) & 1, ctx, 11)) return false;
       tc_fence_after();
       const uint64_t kb = dK + ks * kTileD;
+      if (rope && Cfg::kPersistent && last_of_item) {
+        // the next item's Q load overwrites the tile: its rotated copy must have left
+        if (lane == 0) tma_store_wait_read();
+        __syncwarp();
+      }
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -313,9 +352,20 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
     for (int r = 0; r < Cfg::kMaxRounds && ok; ++r) {
       const int id = item_of(r, blockIdx.x, gridDim.x);
       if (id >= n_items) break;
-      const int n_kv = decode_item(p, id).n_kv;
-      ok = warp_wait(&bar_q, r & 1, ctx, 10);
+      const FwdItem itm = decode_item(p, id);
+      const int n_kv = itm.n_kv;
+      ok = warp_wait(rope ? &bar_qrot : &bar_q, r & 1, ctx, 10);
       if (!ok) break;
+      if (rope) {
+        // the rotated Q tile goes out once, for the backward
+        if (lane == 0) {
+          for (int hf = 0; hf < Cfg::kHalves; ++hf)
+            tma_store_4d(&p.tmap_qrot, smem + Cfg::kOffQ + hf * kHalfTileBytes, hf * 64, itm.h, itm.qt * kTile,
+                         itm.b);
+          tma_store_commit();
+        }
+        __syncwarp();
+      }
       if (kSepP) {
         // S(j+1) as soon as the softmax holds S(j); PV(j) once P(j) is written.
         ok = issue_s(g0, n_kv == 1);
@@ -331,6 +381,11 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
         }
         if (ok) ok = issue_pv(g0 + n_kv - 1, n_kv == 1, r);
       }
+      if (ok && rope) {
+        // d = 128 stages O in the Q buffer once bar_o completes
+        if (lane == 0) tma_store_wait_read();
+        __syncwarp();
+      }
       if (ok) commit(&bar_o);
       g0 += n_kv;
     }
@@ -338,6 +393,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
       commit(&bar_drain);
       mbar_wait_drain(&bar_drain, 0, p.budget_ns);
     }
+    if (rope && lane == 0) tma_store_wait_all();
   } else {
     // ------------------------------------------------------------ softmax warpgroup
     const int quarter = warp & 3;
@@ -348,10 +404,24 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
     const uint32_t tO = tmem + lane_base + kColO;
     const float sl2 = p.scale_log2;
     bool ok = true;
+    // Rotary embedding: rotate this thread's row of round rr's Q tile once it has
+    // landed (no-op past the CTA's last item).
+    auto rotate_round = [&](int rr) -> bool {
+      if (rr >= Cfg::kMaxRounds) return true;
+      const int id2 = item_of(rr, blockIdx.x, gridDim.x);
+      if (id2 >= n_items) return true;
+      const int tok = (p.nT - 1 - id2 / (p.B * p.Hq)) * kTile + row;
+      if (!warp_wait(&bar_q, rr & 1, ctx, 23)) return false;
+      rotate_q_row<D>(smem + Cfg::kOffQ, row, tok, p.T, p.rope_f);
+      fence_proxy_async_smem();
+      mbar_arrive(&bar_qrot);
+      return true;
+    };
     int g = 0;  // tiles seen so far, over all items
     for (int r = 0; r < Cfg::kMaxRounds && ok; ++r) {
       const int id = item_of(r, blockIdx.x, gridDim.x);
       if (id >= n_items) break;
+      if (rope && r == 0 && !(ok = rotate_round(0))) break;
       const int qt = p.nT - 1 - id / (p.B * p.Hq);
       const int n_kv = p.causal ? qt + 1 : p.nT;
       float m_used = -INFINITY;  // running max in log2 units (possibly stale by <= 8)
@@ -455,6 +525,9 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
         tc_fence_before();
         mbar_arrive(&bar_p);
       }
+      // the next item's Q is rotated before this item's epilogue, so its first S can
+      // be computed while the epilogue runs
+      if (ok && rope) ok = rotate_round(r + 1);
       if (ok) ok = warp_wait(&bar_o, r & 1, ctx, 21);
       if (!ok) break;
       // ---- epilogue: O / l as bf16, and the row's log-sum-exp

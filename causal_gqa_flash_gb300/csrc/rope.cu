@@ -14,6 +14,8 @@
 //    loads are all issued before its stores (no chunk is touched by two threads,
 //    so this holds in place too), which keeps kRopeHeads loads in flight per
 //    thread. Products and sums in fp32, each result rounded once to bf16.
+//    Without a table (FREQ) the cosines and sines come from rope_cos_sin, the
+//    angles the attention kernels' fused rotation uses.
 #include "attn_common.cuh"
 #include "rope.cuh"
 
@@ -32,12 +34,7 @@ __global__ void rope_table_kernel(const RopeTableParams p) {
   }
 }
 
-__device__ __forceinline__ uint32_t rotate_pair(uint32_t w, float c, float s) {
-  const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xffff0000u);
-  return pack_bf16x2(fmaf(x0, c, -x1 * s), fmaf(x0, s, x1 * c));
-}
-
-template <int D>
+template <int D, bool FREQ>
 __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p) {
   constexpr int kChunks = D / 8;  // 16-byte chunks (4 pairs) of one head's row
   pdl_launch_dependents();
@@ -53,11 +50,20 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p) 
   const int nh = min(kRopeHeads, p.H - h0);
   const int b = static_cast<int>(bt / p.T), t = static_cast<int>(bt - static_cast<long long>(b) * p.T);
   // (cos, sin) of the chunk's four pairs
-  const float4* tab = reinterpret_cast<const float4*>(p.table) + (static_cast<long long>(t) * (D / 2) + chunk * 4) / 2;
-  const float4 e01 = tab[0], e23 = tab[1];
   const float sg = p.inverse ? -1.f : 1.f;
-  const float c[4] = {e01.x, e01.z, e23.x, e23.z};
-  const float s[4] = {sg * e01.y, sg * e01.w, sg * e23.y, sg * e23.w};
+  float c[4], s[4];
+  if (FREQ) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      rope_cos_sin(static_cast<uint32_t>(t), p.freq.lo[chunk * 4 + j], p.freq.hi[chunk * 4 + j], c[j], s[j]);
+      s[j] *= sg;
+    }
+  } else {
+    const float4* tab = reinterpret_cast<const float4*>(p.table) + (static_cast<long long>(t) * (D / 2) + chunk * 4) / 2;
+    const float4 e01 = tab[0], e23 = tab[1];
+    c[0] = e01.x, c[1] = e01.z, c[2] = e23.x, c[3] = e23.z;
+    s[0] = sg * e01.y, s[1] = sg * e01.w, s[2] = sg * e23.y, s[3] = sg * e23.w;
+  }
   const uint4* src = reinterpret_cast<const uint4*>(p.x) + (b * p.x_sb16 + t * p.x_st16 + h0 * kChunks + chunk);
   uint4* dst = reinterpret_cast<uint4*>(p.y) + (b * p.y_sb16 + t * p.y_st16 + h0 * kChunks + chunk);
   uint4 v[kRopeHeads];
@@ -67,8 +73,8 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p) 
 #pragma unroll
   for (int j = 0; j < kRopeHeads; ++j)
     if (j < nh)
-      dst[j * kChunks] = make_uint4(rotate_pair(v[j].x, c[0], s[0]), rotate_pair(v[j].y, c[1], s[1]),
-                                    rotate_pair(v[j].z, c[2], s[2]), rotate_pair(v[j].w, c[3], s[3]));
+      dst[j * kChunks] = make_uint4(rope_rotate_bf16x2(v[j].x, c[0], s[0]), rope_rotate_bf16x2(v[j].y, c[1], s[1]),
+                                    rope_rotate_bf16x2(v[j].z, c[2], s[2]), rope_rotate_bf16x2(v[j].w, c[3], s[3]));
 }
 
 }  // namespace
@@ -84,8 +90,13 @@ cudaError_t launch_rope(const RopeParams& p, int d, cudaStream_t stream) {
   const long long threads =
       static_cast<long long>(p.B) * p.T * ((p.H + kRopeHeads - 1) / kRopeHeads) * (d / 8);
   const unsigned grid = static_cast<unsigned>((threads + kRopeThreads - 1) / kRopeThreads);
-  cudaError_t e = d == 64 ? launch_pdl(rope_kernel<64>, grid, kRopeThreads, 0, stream, p)
-                          : launch_pdl(rope_kernel<128>, grid, kRopeThreads, 0, stream, p);
+  cudaError_t e;
+  if (p.table)
+    e = d == 64 ? launch_pdl(rope_kernel<64, false>, grid, kRopeThreads, 0, stream, p)
+                : launch_pdl(rope_kernel<128, false>, grid, kRopeThreads, 0, stream, p);
+  else
+    e = d == 64 ? launch_pdl(rope_kernel<64, true>, grid, kRopeThreads, 0, stream, p)
+                : launch_pdl(rope_kernel<128, true>, grid, kRopeThreads, 0, stream, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

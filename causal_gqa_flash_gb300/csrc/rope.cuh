@@ -3,6 +3,8 @@
 
 #include <cuda_runtime.h>
 
+#include "attn_common.cuh"
+
 namespace gqa {
 
 constexpr int kRopeThreads = 128;
@@ -21,9 +23,10 @@ struct RopeParams {
   void* y;
   long long x_st16, x_sb16;   // token / batch strides of x in 16-byte units
   long long y_st16, y_sb16;
-  const float* table;         // [T, d/2] of (cos, sin)
+  const float* table;         // [T, d/2] of (cos, sin), or null: angles from freq
   int B, T, H;
   int inverse;                // rotate by minus the angle
+  RopeFreq freq;              // with table == null
 };
 
 cudaError_t launch_rope_table(const RopeTableParams& p, cudaStream_t stream);

@@ -209,6 +209,44 @@ gqa_status_t attn_rope(gqa_view_t x, gqa_view_t y, const float* table, int B, in
                        void* stream);
 
 /*
+ * Attention with the rotary embedding fused in ("A transformer in PTX", §The
+ * model: q and k are rotated between the fused QKV matmul and attention). The
+ * rotation of attn_rope with base `base` (> 0, finite; 10000 in the usual
+ * setting); the attention is attn_fwd / attn_bwd of the rotated q and k.
+ * No table: each kernel computes its angles in registers. The turn count of
+ * token t, t * base^(-2i/d) / (2 pi) mod 1, is taken exactly to 2^-32 of a turn
+ * with integer multiplies, and the hardware sine and cosine of the reduced angle
+ * (in [-pi, pi)) are within ~1e-6 of the exact values (attn_rope's fp32 table:
+ * ~6e-8); a rotated element may therefore differ from attn_rope's by one bf16
+ * rounding step.
+ *
+ * attn_fwd_rope: q [B,T,Hq,d] and k [B,T,Hkv,d] are the UNROTATED projections.
+ *   The keys are rotated once into k_rot (one pass: every key tile is read by
+ *   all query tiles of its group). The forward kernel rotates each query tile in
+ *   shared memory as it arrives and writes the rotated tile to q_rot, so the
+ *   queries make one trip through HBM. o, lse as in attn_fwd; q_rot and k_rot
+ *   are what attn_bwd_rope takes, and o and lse are bit-identical to attn_fwd of
+ *   q_rot and k_rot. q_rot may be q itself (same pointer and strides: rotated in
+ *   place, as the page's trainer does on its QKV buffer), and k_rot may be k;
+ *   otherwise they must not overlap any other argument (not checked).
+ * attn_bwd_rope: q_rot, k_rot from attn_fwd_rope (same base); v, o, lse, dO, the
+ *   workspace and dv as in attn_bwd (dv bit-identical to attn_bwd of q_rot and
+ *   k_rot). dq and dk are the gradients of the UNROTATED q and k: the kernel's
+ *   fp32 gradients of q_rot and k_rot are turned back by the inverse rotation in
+ *   its epilogue, before the one rounding to bf16.
+ * All tensors are views (gqa_view_t); errors as in attn_fwd_strided and
+ * attn_bwd_strided, plus GQA_ERR_INVALID_ARG for a bad base; nothing is
+ * launched when an argument is refused.
+ */
+gqa_status_t attn_fwd_rope(gqa_view_t q, gqa_view_t k, gqa_view_t v, gqa_view_t o, float* lse, gqa_view_t q_rot,
+                           gqa_view_t k_rot, double base, int B, int T, int Hq, int Hkv, int d, int causal,
+                           void* stream);
+gqa_status_t attn_bwd_rope(gqa_view_t q_rot, gqa_view_t k_rot, gqa_view_t v, gqa_view_t o, const float* lse,
+                           gqa_view_t dO, gqa_view_t dq, gqa_view_t dk, gqa_view_t dv, double base,
+                           void* workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int d, int causal,
+                           void* stream);
+
+/*
  * Naive attention ("A transformer in PTX", §Three ways to run it: the same
  * operations as plain kernels on bf16 activations, the reference the fast
  * kernels are checked against; §Flash attention: the naive kernels write the

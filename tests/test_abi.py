@@ -237,3 +237,45 @@ def test_binding_checks_views_rope_and_naive_arguments(lib):
         gqa.attn_fwd_naive(q, k, q)
     with pytest.raises(ValueError, match="lse must have shape"):
         gqa.attn_bwd_naive(q, k, k, q, torch.zeros((2, 6, 65)), q)
+
+
+def test_fused_rope_argument_checks(lib):
+    """attn_fwd_rope / attn_bwd_rope refuse bad views, a bad base and an in-place
+    rotation whose strides differ, before any launch."""
+    q, k = _view(), _view(st=2 * 64, sb=128 * 2 * 64)
+    for base in (0.0, -1.0, float("nan"), float("inf")):
+        rc = lib.attn_fwd_rope(q, k, k, q, FAKE, q, k, base, 2, 128, 6, 2, 64, 1, None)
+        assert rc == gqa.GQA_ERR_INVALID_ARG and "base must be positive" in gqa.attn_last_error()
+    rc = lib.attn_fwd_rope(q, k, k, q, FAKE, _view(st=6 * 64 + 64, sb=128 * 7 * 64), k, 1e4, 2, 128, 6, 2, 64, 1,
+                           None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "q_rot == q" in gqa.attn_last_error()
+    rc = lib.attn_fwd_rope(q, k, k, q, FAKE, _view(ptr=0x400000), _view(st=3 * 64, sb=128 * 3 * 64), 1e4, 2, 128,
+                           6, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "k_rot == k" in gqa.attn_last_error()
+    rc = lib.attn_fwd_rope(q, k, k, q, FAKE, _view(MISALIGNED), k, 1e4, 2, 128, 6, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "q_rot is not 16-byte aligned" in gqa.attn_last_error()
+    rc = lib.attn_fwd_rope(q, k, k, q, FAKE, q, k, 1e4, 2, 128, 6, 4, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "multiple" in gqa.attn_last_error()
+    need = gqa.attn_bwd_workspace_bytes(2, 128, 6)
+    rc = lib.attn_bwd_rope(q, k, k, q, FAKE, q, q, k, k, 0.0, FAKE, need, 2, 128, 6, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "base must be positive" in gqa.attn_last_error()
+    rc = lib.attn_bwd_rope(q, k, k, q, FAKE, q, q, _view(st=2 * 64, sb=64), k, 1e4, FAKE, need, 2, 128, 6, 2, 64, 1,
+                           None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "output dk overlaps itself" in gqa.attn_last_error()
+    rc = lib.attn_bwd_rope(q, k, k, q, FAKE, q, q, k, k, 1e4, FAKE, need - 1, 2, 128, 6, 2, 64, 1, None)
+    assert rc == gqa.GQA_ERR_INVALID_ARG and "workspace_bytes" in gqa.attn_last_error()
+
+
+def test_binding_checks_fused_rope_arguments(lib):
+    import torch
+    bf = torch.bfloat16
+    q, k = torch.zeros((2, 64, 6, 64), dtype=bf), torch.zeros((2, 64, 2, 64), dtype=bf)
+    lse = torch.zeros((2, 6, 64))
+    with pytest.raises(ValueError, match="k_rot must have shape"):
+        gqa.attn_fwd_rope(q, k, k, k_rot=q)
+    with pytest.raises(ValueError, match="q_rot must have shape"):
+        gqa.attn_fwd_rope(q, k, k, q_rot=k)
+    with pytest.raises(ValueError, match="lse must have shape"):
+        gqa.attn_bwd_rope(q, k, k, q, torch.zeros((2, 6, 63)), q)
+    with pytest.raises(ValueError, match="dk must have shape"):
+        gqa.attn_bwd_rope(q, k, k, q, lse, q, dk=q)
