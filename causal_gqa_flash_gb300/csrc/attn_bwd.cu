@@ -220,12 +220,19 @@ struct MainCfg {
   static constexpr uint32_t kColDP = 128;
   static constexpr uint32_t kDqColDS = 256;
   static constexpr uint32_t kDqColAcc = 320;
+  // d = 128 dQ tasks: Q is copied to the 64 free columns at the end of TMEM once per
+  // task and S runs as a TS MMA (SS MMAs with N = 128 reach ~60% of the tensor
+  // rate, TS ~86%). Measured 0.8% faster at d = 128; at d = 64, Q and dO in TMEM
+  // and both S and dP as TS gave the same bits but no gain, so d = 64 keeps SS.
+  static constexpr bool kDqTsS = (D == 128);
+  static constexpr uint32_t kDqColQA = 448;
   static constexpr bool kKvSepPdS = (D == 64);  // dK/dV: P/dS region of its own
   static constexpr uint32_t kKvColP = kKvSepPdS ? 256 : 0;
   static constexpr uint32_t kKvColDS = kKvSepPdS ? 320 : 64;
   static constexpr uint32_t kKvColDV = kKvSepPdS ? 384 : 256;
   static constexpr uint32_t kKvColDK = kKvColDV + D;
   static_assert(kDqColAcc + D <= 512 && kKvColDK + D <= 512, "TMEM columns");
+  static_assert(!kDqTsS || (kDqColAcc + D <= kDqColQA && kDqColQA + D / 2 <= 512), "TMEM columns of Q");
 };
 
 // Unswizzled K-major layout of a 128 x 16 bf16 operand: byte offset of (row, 8-column half).
@@ -668,9 +675,15 @@ struct MmaCtx {
     } else {
       const uint64_t fo = f * (Cfg::kDqFixBytes >> 4);
       const uint64_t b0 = qB_S + bslot * kTileD;
+      if constexpr (Cfg::kDqTsS) {
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss(dst, qA_S + fo + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ts(dst, tmem + Cfg::kDqColQA + kk * 8, b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(dst, qA_S + fo + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+      }
     }
   }
   template <bool DKV>
@@ -689,6 +702,15 @@ struct MmaCtx {
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(dst, qA_P + fo + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
     }
+  }
+  // d = 128 dQ task: its Q into TMEM (one fixed buffer), ahead of its S MMAs. The
+  // columns were last read by the previous dQ task's S MMAs (done: this task's
+  // fixed operands were loaded only after its fixed_free) or written by a dK/dV
+  // task's dK accumulator (read out: a change of task kind waits for acc_free).
+  __device__ __forceinline__ void copy_q_to_tmem(int f) const {
+    const uint64_t fo = f * (Cfg::kDqFixBytes >> 4);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) tmem_cp_128x256b(tmem + Cfg::kDqColQA + kk * 8, qA_S + fo + kmaj_step(kk));
   }
   // dK/dV gradient MMAs as two chains, dV first, with a commit on `do_free` between
   // them so that the dO slot is refilled while the dK chain still reads Q.
@@ -818,6 +840,10 @@ __device__ __forceinline__ void sdp_issuer_role(const BwdParams& p, uint8_t* sme
     ok = warp_wait(&bars.fixed_full[f], (n / Cfg::kNF) & 1, ctx, 10);
     if (!ok) break;
     tc_fence_after();
+    if (Cfg::kDqTsS && !t.dkv) {
+      if (elect_one()) m.copy_q_to_tmem(f);
+      __syncwarp();
+    }
     if (t.dkv) {
       ok = sdp_task<D, true>(m, bars, ctx, t.n_it, f, G, kv_used, issued);
       kv_used += t.n_it;

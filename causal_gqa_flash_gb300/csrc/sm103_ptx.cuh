@@ -250,6 +250,14 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Copy a 128-row x 256-bit matrix (one K = 16 step of a bf16 operand) from shared
+// memory, described by a matrix descriptor (any of its swizzles), to TMEM lanes
+// 0-127, columns [taddr, taddr + 8): row r to lane r, in the layout a TS MMA reads
+// its A operand in. Executed in order with MMAs issued later by the same thread.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
 // Arrive (once) on an mbarrier when all previously issued tcgen05 async ops of
 // this thread have completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
