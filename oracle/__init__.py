@@ -166,3 +166,75 @@ def rope(x, base: float = 10000.0, inverse: bool = False) -> np.ndarray:
     y[..., 0::2] = x0 * c - x1 * s
     y[..., 1::2] = x0 * s + x1 * c
     return y
+
+
+# ----------------------------------------------------------------------------
+# The attention half of one decoder layer ("A transformer in PTX", §The model):
+# RMSNorm of the residual stream, one fused matmul for q, k and v, RoPE on q and
+# k, causal grouped-query attention, and the output projection added straight
+# into the residual stream. Used by the whole-layer check of the GPU attention
+# (the matmuls and the norm on the GPU side come from torch there). The page
+# gives no epsilon for RMSNorm; 1e-5 is used, and the gain multiplies after the
+# normalisation.
+# ----------------------------------------------------------------------------
+
+def rmsnorm(x, g, eps: float = 1e-5):
+    """y = x / sqrt(mean(x^2 over the last axis) + eps) * g, and the per-row 1/sqrt(...)."""
+    x, g = _as_f64(x), _as_f64(g)
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1) + eps)
+    return x * r[..., None] * g, r
+
+
+def rmsnorm_bwd(x, g, r, dy):
+    """Gradients of rmsnorm with respect to x and g, given dL/dy and the forward's r:
+    dx_j = g_j r dy_j - x_j r^3 / C * sum_i dy_i g_i x_i,  dg = sum over rows of dy * x * r."""
+    x, g, dy = _as_f64(x), _as_f64(g), _as_f64(dy)
+    C = x.shape[-1]
+    dot = np.sum(dy * g * x, axis=-1)
+    dx = g * r[..., None] * dy - x * (r ** 3 * dot / C)[..., None]
+    dg = np.sum((dy * x * r[..., None]).reshape(-1, C), axis=0)
+    return dx, dg
+
+
+def layer_attn(x, g, w_qkv, w_o, Hq: int, Hkv: int, d: int, dx2, base: float = 10000.0, eps: float = 1e-5):
+    """Forward and backward of the attention half of a layer, in f64.
+
+    x [B,T,C] residual stream, g [C] norm gain, w_qkv [(Hq+2*Hkv)*d, C] (rows: q heads,
+    then k heads, then v heads), w_o [C, Hq*d], dx2 [B,T,C] the upstream gradient of the
+    output x2 = x + attention(rope(q), rope(k), v) w_o^T. The loss is sum(x2 * dx2).
+    Returns x2 and the gradients dx, dg, dw_qkv, dw_o, plus the intermediates q, k, v
+    (unrotated) and o."""
+    x, g, w_qkv, w_o, dx2 = (_as_f64(a) for a in (x, g, w_qkv, w_o, dx2))
+    B, T, C = x.shape
+    H3 = Hq + 2 * Hkv
+    xn, r = rmsnorm(x, g, eps)
+    qkv = (xn.reshape(-1, C) @ w_qkv.T).reshape(B, T, H3, d)
+    q, k, v = qkv[:, :, :Hq], qkv[:, :, Hq:Hq + Hkv], qkv[:, :, Hq + Hkv:]
+    qr, kr = rope(q, base), rope(k, base)
+    # the attention output's upstream gradient is known before the attention runs
+    do = (dx2.reshape(-1, C) @ w_o).reshape(B, T, Hq, d)
+    att = bwd(np.ascontiguousarray(qr), np.ascontiguousarray(kr), np.ascontiguousarray(v), do, causal=True)
+    y = att["o"].reshape(B * T, Hq * d)
+    x2 = x + (y @ w_o.T).reshape(B, T, C)
+    dw_o = dx2.reshape(-1, C).T @ y
+    dq = rope(att["dq"], base, inverse=True)
+    dk = rope(att["dk"], base, inverse=True)
+    dqkv = np.concatenate([dq, dk, att["dv"]], axis=2).reshape(B * T, H3 * d)
+    dw_qkv = dqkv.T @ xn.reshape(-1, C)
+    dxn = (dqkv @ w_qkv).reshape(B, T, C)
+    dx_norm, dg = rmsnorm_bwd(x, g, r, dxn)
+    return dict(x2=x2, dx=dx2 + dx_norm, dg=dg, dw_qkv=dw_qkv, dw_o=dw_o, q=q, k=k, v=v, o=att["o"])
+
+
+def layer_attn_loss(x, g, w_qkv, w_o, Hq: int, Hkv: int, d: int, dx2, base: float = 10000.0, eps: float = 1e-5):
+    """The scalar sum(x2 * dx2) of layer_attn's forward alone (for finite differences)."""
+    x, g, w_qkv, w_o, dx2 = (_as_f64(a) for a in (x, g, w_qkv, w_o, dx2))
+    B, T, C = x.shape
+    H3 = Hq + 2 * Hkv
+    xn, _ = rmsnorm(x, g, eps)
+    qkv = (xn.reshape(-1, C) @ w_qkv.T).reshape(B, T, H3, d)
+    q, k, v = qkv[:, :, :Hq], qkv[:, :, Hq:Hq + Hkv], qkv[:, :, Hq + Hkv:]
+    o, _ = fwd(np.ascontiguousarray(rope(q, base)), np.ascontiguousarray(rope(k, base)), np.ascontiguousarray(v),
+               causal=True)
+    x2 = x + (o.reshape(B * T, Hq * d) @ w_o.T).reshape(B, T, C)
+    return float(np.sum(x2 * dx2))
