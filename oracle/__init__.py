@@ -15,6 +15,11 @@ queries and keys before attention ("A transformer in PTX", §The model); the
 page names it and gives no formula, so it is the textbook rotation (pairs of
 adjacent features, frequencies base^(-2i/d), angle = token index), written
 out below in numpy.
+
+``rmsnorm``, ``rmsnorm_bwd`` and ``layer_attn`` compose these into the attention
+half of a decoder layer (§The model: RMSNorm, fused QKV matmul, RoPE, attention,
+output projection into the residual stream), forward and backward in f64, for the
+whole-layer check of the GPU attention.
 """
 from __future__ import annotations
 
