@@ -14,7 +14,8 @@
 // The dQ and dK/dV passes are two kinds of task of one launch (ordered so the
 // heaviest tasks start first), each task owning its outputs:
 //   dQ task (per 128-query tile of one query head), key tiles in ascending order:
-//     S = Q K^T, dP = dO V^T                  (SS MMAs into TMEM)
+//     S = Q K^T, dP = dO V^T                  (MMAs into TMEM; at d = 128 S is a
+//                                              TS MMA with Q copied to TMEM)
 //     P = 2^(S*scale*log2e - LSE2), dS = P (dP - D)   (per row, bf16 into TMEM)
 //     dQ += dS K                              (TS MMA, K as MN-major operand)
 //   dK/dV task (per 128-key tile of one kv head), query heads of the group in
@@ -22,7 +23,10 @@
 //     S^T = K Q^T, dP^T = V dO^T              (SS MMAs)
 //     P^T, dS^T per key row                   (bf16 into TMEM)
 //     dV += P^T dO, dK += dS^T Q              (TS MMAs, dO/Q as MN-major operands)
-// dQ and dK carry the score scale once, in the epilogue.
+// dQ and dK carry the score scale once, in the epilogue; with the rotary
+// embedding (a separate template instance) the epilogue also turns them back by
+// the inverse rotation, since the kernel differentiates with respect to the
+// rotated q and k.
 #include "attn_common.cuh"
 
 namespace gqa {

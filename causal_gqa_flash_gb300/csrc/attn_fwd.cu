@@ -33,7 +33,10 @@
 //  * the running max is rescaled lazily: O and l are only rescaled when a
 //    row's max grows by more than 2^8, otherwise p = 2^(s - m_stale) <= 256;
 //  * causal tiles past the diagonal are never visited; only the diagonal tile
-//    is masked; ragged T relies on TMA zero fill plus the causal mask.
+//    is masked; ragged T relies on TMA zero fill plus the causal mask;
+//  * with the rotary embedding (a separate template instance) the softmax warps
+//    rotate their rows of each Q tile in shared memory right after its load, and
+//    the MMA warp stores the rotated tile for the backward before the first S.
 #include "attn_common.cuh"
 
 namespace gqa {
