@@ -360,23 +360,40 @@ __device__ __forceinline__ TaskInfo decode_task(const BwdParams& p, int id) {
   t.ni = 1;
   if (id < p.n_dkv_tasks) {
     t.dkv = 1;
-    const int nbk = p.B * p.Hkv;
-    t.tile = id / nbk;
-    const int bk = id % nbk;
-    t.b = bk / p.Hkv;
-    t.kvh = bk % p.Hkv;
+    // key tile ascending = causal cost descending, within a group or over all groups
+    int bk;
+    if (p.dkv_group_major) {
+      bk = fdiv(id, p.fd_nt);
+      t.tile = id - bk * p.nT;
+    } else {
+      t.tile = fdiv(id, p.fd_bk);
+      bk = id - t.tile * (p.B * p.Hkv);
+    }
+    t.b = fdiv(bk, p.fd_hkv);
+    t.kvh = bk - t.b * p.Hkv;
     t.i0 = p.causal ? t.tile : 0;
     t.ni = p.nT - t.i0;
     t.n_it = p.G * t.ni;
   } else {
     t.dkv = 0;
     const int q = id - p.n_dkv_tasks;
-    const int nbh = p.B * p.Hq;
-    t.tile = p.nT - 1 - q / nbh;
-    const int bh = q % nbh;
-    t.b = bh / p.Hq;
-    t.h = bh % p.Hq;
-    t.kvh = t.h / p.G;
+    if (p.dq_group_major) {
+      // group (b, kv head), then query tile descending, then the group's query heads
+      const int grp = fdiv(q, p.fd_ntg);
+      const int rem = q - grp * (p.nT * p.G);
+      const int qt = fdiv(rem, p.fd_g);
+      t.tile = p.nT - 1 - qt;
+      t.b = fdiv(grp, p.fd_hkv);
+      t.kvh = grp - t.b * p.Hkv;
+      t.h = t.kvh * p.G + (rem - qt * p.G);
+    } else {
+      const int qt = fdiv(q, p.fd_bh);
+      t.tile = p.nT - 1 - qt;
+      const int bh = q - qt * (p.B * p.Hq);
+      t.b = fdiv(bh, p.fd_hq);
+      t.h = bh - t.b * p.Hq;
+      t.kvh = fdiv(t.h, p.fd_g);
+    }
     t.n_it = p.causal ? t.tile + 1 : p.nT;
   }
   return t;

@@ -28,6 +28,29 @@ enum KernelId : unsigned int {
   kKidSelfTest = 9,
 };
 
+// Division of a non-negative int below 2^31 by a divisor fixed for the launch, as a
+// multiply-high, an add and a shift instead of the tens of instructions of a
+// division by a runtime value (Granlund and Montgomery, "Division by invariant
+// integers using multiplication", 1994): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, n / d = (umulhi(n, m) + n) >> l, and the sum
+// stays below 2^32 because umulhi(n, m) < n < 2^31. The work-item decodes sit on
+// the path between one task and the next, where these divisions showed.
+struct FastDiv {
+  uint32_t d, m, s;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((uint64_t{1} << l) < d) ++l;
+  const uint64_t m = ((uint64_t{1} << 32) * ((uint64_t{1} << l) - d)) / d + 1;
+  return FastDiv{d, static_cast<uint32_t>(m), l};
+}
+
+__device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
+  const uint32_t u = static_cast<uint32_t>(n);
+  return static_cast<int>((__umulhi(u, f.m) + u) >> f.s);
+}
+
 // Rotary frequencies as fixed-point turns: feature pair i of token t turns by
 // t * f_i turns, f_i = base^(-2i/d) / (2 pi), held to 64 bits (hi and lo words).
 // The fraction t * f_i mod 1 then comes out of two 32-bit integer multiplies,
@@ -50,6 +73,7 @@ struct FwdParams {
   RopeFreq rope_f;
   float* lse;          // [B,Hq,T] fp32, natural log
   int B, T, Hq, Hkv, G, nT;
+  FastDiv fd_bh, fd_hq, fd_g;  // divisors B*Hq, Hq, G of the work-item decode
   int causal;
   float scale_log2;    // (1/sqrt(d)) * log2(e)
   DevStatusWord* status;
@@ -91,6 +115,10 @@ struct BwdParams {
   int causal;
   int n_dkv_tasks;     // tasks [0, n_dkv_tasks) compute dK/dV (0 = none)
   int n_dq_tasks;      // the next n_dq_tasks tasks compute dQ (0 = none)
+  int dkv_group_major;  // dK/dV task order: 1 = per (batch, kv head) group, 0 = key tile outermost
+  int dq_group_major;   // dQ task order: 1 = per (batch, kv head) group, 0 = query tile outermost
+  // divisors of the task decode: nT, B*Hkv, Hkv, B*Hq, Hq, G, nT*G
+  FastDiv fd_nt, fd_bk, fd_hkv, fd_bh, fd_hq, fd_g, fd_ntg;
   float scale;         // 1/sqrt(d)
   float scale_log2;    // scale * log2(e)
   DevStatusWord* status;

@@ -137,13 +137,13 @@ struct FwdItem {
 
 __device__ __forceinline__ FwdItem decode_item(const FwdParams& p, int id) {
   // heaviest query tiles first (causal cost grows with the tile index)
-  const int nbh = p.B * p.Hq;
   FwdItem it;
-  it.qt = p.nT - 1 - id / nbh;
-  const int bh = id % nbh;
-  it.b = bh / p.Hq;
-  it.h = bh % p.Hq;
-  it.kvh = it.h / p.G;
+  const int r = fdiv(id, p.fd_bh);
+  it.qt = p.nT - 1 - r;
+  const int bh = id - r * (p.B * p.Hq);
+  it.b = fdiv(bh, p.fd_hq);
+  it.h = bh - it.b * p.Hq;
+  it.kvh = fdiv(it.h, p.fd_g);
   it.n_kv = p.causal ? it.qt + 1 : p.nT;
   return it;
 }
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
       if (rr >= Cfg::kMaxRounds) return true;
       const int id2 = item_of(rr, blockIdx.x, gridDim.x);
       if (id2 >= n_items) return true;
-      const int tok = (p.nT - 1 - id2 / (p.B * p.Hq)) * kTile + row;
+      const int tok = (p.nT - 1 - fdiv(id2, p.fd_bh)) * kTile + row;
       if (!warp_wait(&bar_q, rr & 1, ctx, 23)) return false;
       rotate_q_row<D>(smem + Cfg::kOffQ, row, tok, p.T, p.rope_f);
       fence_proxy_async_smem();
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
       const int id = item_of(r, blockIdx.x, gridDim.x);
       if (id >= n_items) break;
       if (rope && r == 0 && !(ok = rotate_round(0))) break;
-      const int qt = p.nT - 1 - id / (p.B * p.Hq);
+      const int qt = p.nT - 1 - fdiv(id, p.fd_bh);
       const int n_kv = p.causal ? qt + 1 : p.nT;
       float m_used = -INFINITY;  // running max in log2 units (possibly stale by <= 8)
       float l = 0.f;
