@@ -18,7 +18,7 @@ __all__ = [
     "attn_bwd_workspace_bytes",
     "attn_bwd_preprocess", "attn_bwd_dq", "attn_bwd_dkv", "attn_bwd_dq_dkv", "attn_bwd_noalloc",
     "NOALLOC_SCRATCH_BYTES",
-    "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_last_error", "attn_version",
+    "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_set_task_order", "attn_last_error", "attn_version",
     "GqaView", "view_of", "attn_rope_table", "attn_rope", "attn_fwd_rope", "attn_bwd_rope", "attn_fwd_naive", "attn_bwd_naive",
     "attn_naive_workspace_bytes", "probe_rates", "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
     "GQA_ERR_TIMEOUT",
@@ -37,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "attn_bwd_dq_dkv", "attn_bwd_noalloc", "attn_fwd_strided", "attn_bwd_strided", "attn_rope_table_bytes",
     "attn_rope_table", "attn_rope", "attn_fwd_rope", "attn_bwd_rope", "attn_naive_workspace_bytes", "attn_fwd_naive", "attn_bwd_naive",
     "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
-    "attn_set_wait_budget_ns", "attn_version", "attn_probe_mma", "attn_probe_ex2",
+    "attn_set_wait_budget_ns", "attn_set_task_order", "attn_version", "attn_probe_mma", "attn_probe_ex2",
 )
 
 _lib = None
@@ -110,6 +110,8 @@ def load():
     lib.attn_selftest_timeout.restype = i
     lib.attn_set_wait_budget_ns.argtypes = [ull]
     lib.attn_set_wait_budget_ns.restype = None
+    lib.attn_set_task_order.argtypes = [i]
+    lib.attn_set_task_order.restype = i
     lib.attn_version.argtypes = []
     lib.attn_version.restype = ctypes.c_char_p
     lib.attn_probe_mma.argtypes = [i, i, i, i, vp, vp]
@@ -488,6 +490,12 @@ def attn_sync_status(stream=None) -> int:
 
 def attn_selftest_timeout(budget_ns: int, stream=None):
     _check(load().attn_selftest_timeout(int(budget_ns), _stream_handle(stream)))
+
+
+def attn_set_task_order(order: int):
+    """Backward task order: 0 by size (default), 1 tile-major, 2 group-major. The
+    results are the same bits in any order; this only moves the time."""
+    _check(load().attn_set_task_order(int(order)))
 
 
 def attn_set_wait_budget_ns(budget_ns: int):

@@ -62,6 +62,7 @@ void set_last_error_message(const char* msg) { t_last_error = msg ? msg : ""; }
 namespace {
 
 std::atomic<unsigned long long> g_budget_ns{2000000000ull};
+std::atomic<int> g_task_order{0};  // attn_set_task_order
 constexpr unsigned long long kDefaultBudgetNs = 2000000000ull;
 
 constexpr int kMaxDevices = 64;
@@ -251,6 +252,15 @@ const char* attn_last_error(void) { return t_last_error.c_str(); }
 
 void attn_set_wait_budget_ns(unsigned long long budget_ns) {
   g_budget_ns.store(budget_ns ? budget_ns : kDefaultBudgetNs);
+}
+
+gqa_status_t attn_set_task_order(int order) {
+  t_last_error.clear();
+  if (order < 0 || order > 2)
+    return fail(GQA_ERR_INVALID_ARG, "attn_set_task_order: order must be 0 (by size), 1 (tile-major) or 2 "
+                                     "(group-major) (got %d)", order);
+  g_task_order.store(order);
+  return GQA_OK;
 }
 
 size_t attn_bwd_workspace_bytes(int B, int T, int Hq) {
@@ -468,8 +478,9 @@ gqa_status_t bwd_main_impl(const char* fn, int which, const View& q, const View&
   // tile-major balances the end of the launch better. The switch sits at 45%.
   const long long limit = ds->l2_bytes * 9 / 20;
   const long long qdo_bytes = 2LL * B * T * Hq * d * 2, kv_bytes = 2LL * B * T * Hkv * d * 2;
-  p.dkv_group_major = qdo_bytes > limit ? 1 : 0;
-  p.dq_group_major = kv_bytes > limit ? 1 : 0;
+  const int order = g_task_order.load();
+  p.dkv_group_major = order == 2 || (order == 0 && qdo_bytes > limit) ? 1 : 0;
+  p.dq_group_major = order == 2 || (order == 0 && kv_bytes > limit) ? 1 : 0;
   cudaError_t e = launch_bwd_main(p, d, st);
   if (e != cudaSuccess) return cuda_fail(fn, "backward kernel launch", e);
   return GQA_OK;

@@ -327,6 +327,21 @@ gqa_status_t attn_probe_ex2(int iters, void* out, void* sink, void* stream);
  */
 void attn_set_wait_budget_ns(unsigned long long budget_ns);
 
+/*
+ * Order in which the backward's persistent launch hands out its tasks (a
+ * performance choice only: every output element has one owner and a fixed
+ * summation order, so the results are the same bits in any order).
+ *   0 (default): per task kind, group-major when the tiles its tasks stream
+ *      (Q and dO for dK/dV tasks, K and V for dQ tasks) exceed 45% of the
+ *      device's L2, otherwise tile-major;
+ *   1: tile-major (heaviest tiles first over all (batch, kv head) groups);
+ *   2: group-major (one (batch, kv head) group after another, heaviest first
+ *      within it).
+ * Applies to launches made after the call. Returns GQA_ERR_INVALID_ARG for any
+ * other value (the setting is then unchanged).
+ */
+gqa_status_t attn_set_task_order(int order);
+
 /* Library version as "major.minor.patch". */
 const char* attn_version(void);
 

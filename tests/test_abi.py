@@ -279,3 +279,11 @@ def test_binding_checks_fused_rope_arguments(lib):
         gqa.attn_bwd_rope(q, k, k, q, torch.zeros((2, 6, 63)), q)
     with pytest.raises(ValueError, match="dk must have shape"):
         gqa.attn_bwd_rope(q, k, k, q, lse, q, dk=q)
+
+
+def test_task_order_argument_checks(lib):
+    assert lib.attn_set_task_order(3) == gqa.GQA_ERR_INVALID_ARG
+    assert "order must be 0" in gqa.attn_last_error()
+    assert lib.attn_set_task_order(-1) == gqa.GQA_ERR_INVALID_ARG
+    for order in (1, 2, 0):
+        assert lib.attn_set_task_order(order) == gqa.GQA_OK

@@ -146,3 +146,26 @@ def test_repeated_steps_no_timeout(name):
         else:
             for a, b in zip(ref, cur):
                 assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f"step {i}"
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,d,causal", [
+    (2, 1000, 6, 2, 64, True),
+    (1, 2048, 8, 2, 128, True),
+    (3, 700, 9, 3, 64, False),
+])
+def test_task_orders_give_identical_bits(B, T, Hq, Hkv, d, causal):
+    """The backward's task order (tile-major, group-major, or chosen by size) only moves
+    the time: every output element has one owner and a fixed summation order."""
+    q, k, v, dout = (x.to(DEV) for x in make_inputs(B, T, Hq, Hkv, d, seed=4242 + T))
+    o, lse = gqa.attn_fwd(q, k, v, causal=causal)
+    outs = []
+    try:
+        for order in (1, 2, 0):
+            gqa.attn_set_task_order(order)
+            outs.append([t.clone() for t in gqa.attn_bwd(q, k, v, o, lse, dout, causal=causal)])
+    finally:
+        gqa.attn_set_task_order(0)
+    assert gqa.attn_sync_status() == gqa.GQA_OK, gqa.attn_last_error()
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
