@@ -451,8 +451,8 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
       id = x < n_tasks ? x : -1;
     }
     id = __shfl_sync(0xffffffffu, id, 0);
-    // Decoded once here (integer divisions by runtime sizes); the other warps read
-    // it from the ring.
+    // Decoded once here (FastDiv divisions by the launch's sizes); the other warps
+    // read it from the ring.
     TaskInfo t{};
     if (id >= 0) t = decode_task(p, id);
     // dK/dV task: row terms (-LSE2, D; 4 rows per lane) of its first stage's query
