@@ -81,7 +81,8 @@ struct FwdCfg {
 
 // Whole S row of this thread's lane (128 columns) in one TMEM load, and the 64
 // columns of bf16 P pairs in one store: at d = 64 one instruction each in place of
-// four measured 5-7% faster, with fewer live registers.
+// four measured 5-7% faster, with fewer live registers; at d = 128 the same time
+// (168 -> 157 registers).
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];"
@@ -465,12 +466,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
         {
           // one batched load of the whole row, one wait
           uint32_t rr[kTile];
-          if constexpr (D == 64) {
-            tmem_ld128(tS, rr);
-          } else {
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[cc * 32]));
-          }
+          tmem_ld128(tS, rr);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < kTile; ++i) s[i] = __uint_as_float(rr[i]);
@@ -534,12 +530,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
           if (!ok) break;
           tc_fence_after();
         }
-        if constexpr (D == 64) {
-          tmem_st64(tP, pk);
-        } else {
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) tmem_st16(tP + cc * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[cc * 16]));
-        }
+        tmem_st64(tP, pk);
         // Rescale O (complete: PV_{j-1} has finished) when any row of this warp needs it.
         if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
