@@ -488,9 +488,13 @@ def run_workload(args, ctx, w, cpu_seconds):
         flush.zero_()
         step(sv0, events[i], rope_ev[i])
     torch.cuda.synchronize(dev)
-    # keep the GPU busy with identical untimed steps so the 100 ms clock sampler sees load
-    t_soak = time.perf_counter()
-    while sampler and time.perf_counter() - t_soak < max(0.0, 1.5 - wall):
+    # The end-to-end leg next, while the GPU is in the state the device-timed steps saw
+    # (after a long soak a power-capped part runs slower, which would charge the copies
+    # with a clock drop they did not cause); the clock sampler keeps running through it.
+    e2e = e2e_leg(args, ctx, w, sets, in_h, out_specs, step)
+    # keep the GPU busy with identical untimed steps so the 100 ms clock sampler sees
+    # at least 1.5 s of load
+    while sampler and time.perf_counter() - wall0 < 1.5:
         for _ in range(20):
             flush.zero_()
             step(sv0)
@@ -562,8 +566,6 @@ def run_workload(args, ctx, w, cpu_seconds):
         kernel_ms["bwd_pre_kernel"] + kernel_ms["bwd_main_kernel"])
     fwd_tf = fwd_flops(w) / (kernel_ms["attn_fwd_kernel"] * 1e-3) / 1e12
     bwd_tf = 2.5 * fwd_flops(w) / (bwd_ms * 1e-3) / 1e12
-
-    e2e = e2e_leg(args, ctx, w, sets, in_h, out_specs, step)
 
     cpu = None
     if rank == 0 and world == 1 and cpu_seconds > 0 and not (args.no_cpu_baseline or args.profile_run):
