@@ -62,6 +62,10 @@ CASES = [
     # CTAs run several items back to back
     (4, 1500, 8, 2, 64, True, 1.0),    # causal, ragged, 384 items
     (4, 1000, 12, 4, 64, False, 1.0),  # full attention, ragged, 384 items of equal cost
+    # runs of short items (one or two key tiles) back to back: a CTA's next item can
+    # start before its query tile has landed in the other buffer
+    (48, 256, 8, 2, 64, True, 1.0),    # 768 items of 1-2 tiles
+    (64, 128, 8, 2, 64, False, 1.0),   # 512 single-tile items
 ]
 
 
