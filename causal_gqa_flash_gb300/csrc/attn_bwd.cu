@@ -174,14 +174,20 @@ constexpr int kGradWarp = 18;       // second MMA issuer (gradient MMAs)
 constexpr int kTaskConsumers = 18;  // warps 1..18 each take every task from the producer
 
 // Ring depths the barrier arrays of MainBars hold.
-constexpr int kMaxKvStages = 3, kMaxDqKStages = 4, kMaxDqVStages = 3;
+constexpr int kMaxKvStages = 4, kMaxDqKStages = 4, kMaxDqVStages = 3;
 
 template <int D>
 struct MainCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = kHalves * kHalfTileBytes;
   static constexpr int kAuxBytes = 4096;  // 128 rows x 16 bf16, unswizzled K-major (one K-step)
-  static constexpr int kOffOnes = 0;      // both layouts: the ONES operand, written once
+  // d = 64: one row-term tile per dK/dV stage carries both terms (-LSE2/c in its
+  // columns 0-1, -D in 2-3), and two ONES operands pick one pair each; d = 128 keeps
+  // a tile per term (its Q and dO slots are freed at different times) and one ONES.
+  static constexpr bool kCombAux = (D == 64);
+  static constexpr int kOffOnes = 0;      // both layouts: the ONES operand(s), written once
+  static constexpr int kOffOnesP = kCombAux ? kAuxBytes : kOffOnes;
+  static constexpr int kAuxRegion = kCombAux ? 2 * kAuxBytes : kAuxBytes;
   // Fixed operands of a task (dQ: Q, dO, QX, DX; dK/dV: K, V) are double-buffered
   // at d = 64, so the next task's are loaded while this task runs.
   static constexpr int kNF = (D == 64) ? 2 : 1;
@@ -191,23 +197,26 @@ struct MainCfg {
   static constexpr int kDqKStages = (D == 64) ? 4 : 3;
   static constexpr int kDqVStages = (D == 64) ? 3 : 1;
   static constexpr int kDqFixBytes = 2 * kTileBytes;
-  static constexpr int kDqOffQ = kAuxBytes;  // buffer 0; buffer f adds f * kDqFixBytes
+  static constexpr int kDqOffQ = kAuxRegion;  // buffer 0; buffer f adds f * kDqFixBytes
   static constexpr int kDqOffDO = kDqOffQ + kTileBytes;
-  static constexpr int kDqOffK = kAuxBytes + kNF * kDqFixBytes;
+  static constexpr int kDqOffK = kAuxRegion + kNF * kDqFixBytes;
   static constexpr int kDqOffV = kDqOffK + kDqKStages * kTileBytes;
   static constexpr int kDqBytes = kDqOffV + kDqVStages * kTileBytes;
   // dK/dV task: fixed buffers [K][V], then the ring of stages [Q][dO][QX][DX].
   // The two gradient chains (dV += P^T dO, dK += dS^T Q) are separate N = D MMAs:
   // at d = 64 a single N = 128 chain over block-diagonal operands (half of it
   // multiplying zeros) measured 8-10% slower overall.
-  static constexpr int kKvStages = (D == 64) ? 3 : 2;   // Q/dO stages
+  // Q/dO stages. At d = 64 a stage is busy from its load (~1 us from the L2) until
+  // the tile's gradient MMAs finish, about two tile periods later: two stages
+  // measured 18% slower than three, and the fourth gained 2-3% more.
+  static constexpr int kKvStages = (D == 64) ? 4 : 2;
   // d = 128: each stage's dO and Q have their own barriers (see MainBars)
   static constexpr bool kSplitStage = (D == 128);
   static constexpr int kKvFixBytes = 2 * kTileBytes;
-  static constexpr int kKvOffK = kAuxBytes;             // buffer 0; buffer f adds f * kKvFixBytes
+  static constexpr int kKvOffK = kAuxRegion;            // buffer 0; buffer f adds f * kKvFixBytes
   static constexpr int kKvOffV = kKvOffK + kTileBytes;
-  static constexpr int kKvOffStages = kAuxBytes + kNF * kKvFixBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kAuxBytes;
+  static constexpr int kKvOffStages = kAuxRegion + kNF * kKvFixBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes + (kCombAux ? 1 : 2) * kAuxBytes;
   static constexpr int kKvBytes = kKvOffStages + kKvStages * kStageBytes;
   static_assert(kKvStages <= kMaxKvStages && kDqKStages <= kMaxDqKStages && kDqVStages <= kMaxDqVStages &&
                     kNF <= 2,
@@ -215,16 +224,21 @@ struct MainCfg {
   __host__ __device__ static constexpr int st_q(int s) { return kKvOffStages + s * kStageBytes; }
   __host__ __device__ static constexpr int st_do(int s) { return st_q(s) + kTileBytes; }
   __host__ __device__ static constexpr int st_qx(int s) { return st_q(s) + 2 * kTileBytes; }
-  __host__ __device__ static constexpr int st_dx(int s) { return st_qx(s) + kAuxBytes; }
+  __host__ __device__ static constexpr int st_dx(int s) { return kCombAux ? st_qx(s) : st_qx(s) + kAuxBytes; }
   // d = 64 epilogue: each compute warp stages its 32 rows of bf16 output (dK/dV:
   // 32 columns, dQ: 16) in a region of its own and stores them with one TMA box.
-  // At d = 128 there is no room for the 64 KB this would take; rows are stored
-  // directly from registers.
+  // The regions lie in the task's own fixed buffer, which no MMA reads once the
+  // task's accumulators are complete; the producer reloads that buffer only after
+  // the stores have read it (stg_free). At d = 128 rows are stored directly from
+  // registers.
   static constexpr bool kTmaStore = (D == 64);
   static constexpr int kOutWarpBytes = 2048;
-  static constexpr int kOffOut = ((kDqBytes > kKvBytes ? kDqBytes : kKvBytes) + 1023) / 1024 * 1024;
-  static constexpr int kOutBytes = kTmaStore ? 16 * kOutWarpBytes : 0;
-  static constexpr int kUsed = kOffOut + kOutBytes + 1024;
+  static_assert(!kTmaStore || (kNF == 2 && 16 * kOutWarpBytes <= kKvFixBytes && 16 * kOutWarpBytes <= kDqFixBytes),
+                "the staging regions fit in a fixed buffer");
+  __host__ __device__ static constexpr int stage_out(bool dkv, int f, int warp) {
+    return (dkv ? kKvOffK + f * kKvFixBytes : kDqOffQ + f * kDqFixBytes) + warp * kOutWarpBytes;
+  }
+  static constexpr int kUsed = (kDqBytes > kKvBytes ? kDqBytes : kKvBytes) + 1024;
   static constexpr int kSmemBytes = kUsed > kOneCtaPerSmSmem ? kUsed : kOneCtaPerSmSmem;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   // TMEM columns
@@ -264,9 +278,23 @@ __device__ __forceinline__ void write_aux_row(uint8_t* tile, int row, float x) {
   *reinterpret_cast<uint4*>(tile + aux_off(row, 1)) = make_uint4(0u, 0u, 0u, 0u);
 }
 
-__device__ __forceinline__ void write_ones_row(uint8_t* tile, int row) {
+// A row of a ONES operand: bf16 1.0 in columns 2*pair and 2*pair + 1, zeros elsewhere.
+__device__ __forceinline__ void write_ones_row(uint8_t* tile, int row, int pair = 0) {
   const uint32_t one2 = 0x3F803F80u;  // bf16 1.0 in both halves
-  *reinterpret_cast<uint4*>(tile + aux_off(row, 0)) = make_uint4(one2, 0u, 0u, 0u);
+  *reinterpret_cast<uint4*>(tile + aux_off(row, 0)) =
+      make_uint4(pair == 0 ? one2 : 0u, pair == 1 ? one2 : 0u, 0u, 0u);
+  *reinterpret_cast<uint4*>(tile + aux_off(row, 1)) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Two row terms in one row of a row-term operand: x in columns 0-1, y in 2-3 (each
+// as hi + lo), met by the ONES operand with pair 0 or pair 1.
+__device__ __forceinline__ void write_aux_row2(uint8_t* tile, int row, float x, float y) {
+  auto split = [](float v) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+    return static_cast<uint32_t>(__bfloat16_as_ushort(hi)) | (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
+  };
+  *reinterpret_cast<uint4*>(tile + aux_off(row, 0)) = make_uint4(split(x), split(y), 0u, 0u);
   *reinterpret_cast<uint4*>(tile + aux_off(row, 1)) = make_uint4(0u, 0u, 0u, 0u);
 }
 
@@ -342,6 +370,7 @@ __device__ __forceinline__ void score_chunk(const uint32_t (&s)[32], const uint3
 struct MainBars {
   uint64_t task_full[2], task_empty[2];   // producer <-> every other warp: next task index
   uint64_t fixed_full[2], fixed_free[2];   // per fixed buffer: operands loaded / no longer read
+  uint64_t stg_free[2];  // per fixed buffer (d = 64): the epilogue's TMA stores have read their rows there
   // dK/dV stage ring. d = 64: q_full/q_empty cover the whole stage (Q, dO and their
   // row terms). d = 128: q_* cover Q and -LSE2, do_* cover dO and -D, so the dO slot
   // is refilled once the dV MMAs are done while the dK MMAs still read Q.
@@ -448,7 +477,10 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
     tma_prefetch_desc(&p.tmap_v);
     tma_prefetch_desc(&p.tmap_do);
   }
-  for (int r = lane; r < kTile; r += 32) write_ones_row(smem + Cfg::kOffOnes, r);
+  for (int r = lane; r < kTile; r += 32) {
+    write_ones_row(smem + Cfg::kOffOnes, r);
+    if (Cfg::kCombAux) write_ones_row(smem + Cfg::kOffOnesP, r, 1);
+  }
   fence_proxy_async_smem();
   __syncwarp();
   int kv_used = 0, q_used = 0, n = 0, n_fixed = 0, prev_kind = -1;
@@ -495,6 +527,8 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
     // epilogue has read the accumulators, so they are).
     const int f = n % NF, fu = n / NF;
     if (fu > 0) ok = lane0_wait(&bars.fixed_free[f], (fu - 1) & 1, ctx, 42, lane);
+    // (its task's epilogue staged its output rows there: their stores must have read them)
+    if (Cfg::kTmaStore && ok && fu > 0) ok = lane0_wait(&bars.stg_free[f], (fu - 1) & 1, ctx, 45, lane);
     if (ok && n > 0 && t.dkv != prev_kind) ok = lane0_wait(&bars.acc_free, (n - 1) & 1, ctx, 43, lane);
     if (!ok) break;
     uint64_t* fbar = &bars.fixed_full[f];
@@ -565,8 +599,12 @@ __device__ __forceinline__ void producer_role(const BwdParams& p, uint8_t* smem,
           }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            write_aux_row(smem + Cfg::st_qx(st), lane + 32 * k, vnl[k] * inv_sl2);
-            write_aux_row(smem + Cfg::st_dx(st), lane + 32 * k, -vd[k]);
+            if constexpr (Cfg::kCombAux) {
+              write_aux_row2(smem + Cfg::st_qx(st), lane + 32 * k, vnl[k] * inv_sl2, -vd[k]);
+            } else {
+              write_aux_row(smem + Cfg::st_qx(st), lane + 32 * k, vnl[k] * inv_sl2);
+              write_aux_row(smem + Cfg::st_dx(st), lane + 32 * k, -vd[k]);
+            }
           }
         }
         if (++qt_n == p.nT) {
@@ -671,12 +709,13 @@ struct MmaCtx {
   uint64_t kvA_S, kvA_P, kvB_S, kvB_P, kvG1, kvG2, kvXB_S, kvXB_P;
   // dQ descriptors (fixed buffer 0, ring slot 0)
   uint64_t qA_S, qA_P, qB_S, qB_P, qG1;
-  uint64_t ones;
+  uint64_t ones, ones_p;  // ONES operands of the S and dP folds (the same at d = 128)
 
   __device__ __forceinline__ void init(uint8_t* smem, uint32_t tm) {
     tmem = tm;
     const uint32_t b = smem_u32(smem);
     ones = sdesc_noswz(b + Cfg::kOffOnes, 128, 256);
+    ones_p = sdesc_noswz(b + Cfg::kOffOnesP, 128, 256);
     kvA_S = sdesc_sw128(b + Cfg::kKvOffK, 16, 1024);  // K
     kvA_P = sdesc_sw128(b + Cfg::kKvOffV, 16, 1024);  // V
     kvB_S = sdesc_sw128(b + Cfg::st_q(0), 16, 1024);   // Q  (K-major)
@@ -724,7 +763,7 @@ struct MmaCtx {
       const uint64_t b0 = kvB_P + bslot * kStDO;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) mma_ss(dst, a + kmaj_step(kk), b0 + kmaj_step(kk), idesc_s, kk > 0 ? 1u : 0u);
-      mma_ss(dst, ones, kvXB_P + bslot * kStX, idesc_s, 1u);
+      mma_ss(dst, ones_p, kvXB_P + bslot * kStX, idesc_s, 1u);
     } else {
       const uint64_t fo = f * (Cfg::kDqFixBytes >> 4);
       const uint64_t b0 = qB_P + bslot * kTileD;
@@ -1136,7 +1175,7 @@ __device__ __forceinline__ bool compute_epilogue(const BwdParams& p, MainBars& b
     mbar_arrive(&bars.acc_free);
     if (unrot) unrotate_acc<NC>(r, t.tile * kTile + row, c0 / 2, p.rope_f);
     if constexpr (Cfg::kTmaStore) {
-      tma_store_rows<NC>(r, wg < 2 ? 1.f : p.scale, smem + Cfg::kOffOut + (warp - 2) * Cfg::kOutWarpBytes,
+      tma_store_rows<NC>(r, wg < 2 ? 1.f : p.scale, smem + Cfg::stage_out(true, n % Cfg::kNF, warp - 2),
                          wg < 2 ? &p.tmap_dv : &p.tmap_dk, part * NC, t.kvh, t.tile * kTile + quarter * 32, t.b,
                          p.T, lane);
       return true;
@@ -1155,7 +1194,7 @@ __device__ __forceinline__ bool compute_epilogue(const BwdParams& p, MainBars& b
     mbar_arrive(&bars.acc_free);
     if (unrot) unrotate_acc<NC>(r, t.tile * kTile + row, c0 / 2, p.rope_f);
     if constexpr (Cfg::kTmaStore) {
-      tma_store_rows<NC>(r, p.scale, smem + Cfg::kOffOut + (warp - 2) * Cfg::kOutWarpBytes, &p.tmap_dq, wg * NC,
+      tma_store_rows<NC>(r, p.scale, smem + Cfg::stage_out(false, n % Cfg::kNF, warp - 2), &p.tmap_dq, wg * NC,
                          t.h, t.tile * kTile + quarter * 32, t.b, p.T, lane);
       return true;
     }
@@ -1195,6 +1234,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.fixed_full[s], 2);  // TMA bytes + the producer warp's arrival once all are issued
       mbar_init(&bars.fixed_free[s], 2);  // one commit from each MMA issuer
+      mbar_init(&bars.stg_free[s], 16);   // lane 0 of each compute warp
     }
     for (int s = 0; s < kMaxKvStages; ++s) {
       mbar_init(&bars.q_full[s], 2);  // TMA bytes + the producer warp's aux operands
@@ -1266,6 +1306,11 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
       const bool early = prev_id >= 0 && (MainCfg<D>::kNF > 1 || (prev_id < p.n_dkv_tasks) != (t.dkv != 0));
       if (early) ok = epilogue(n - 1);
       if (ok) ok = tiles(t, 0, 1);
+      if (MainCfg<D>::kTmaStore && ok && prev_id >= 0 && lane == 0) {
+        // a tile after the epilogue of n-1: its stores have long read the staged rows
+        tma_store_wait_read();
+        mbar_arrive(&bars.stg_free[(n - 1) % MainCfg<D>::kNF]);
+      }
       if (ok && prev_id >= 0 && !early) ok = epilogue(n - 1);
       if (ok) ok = tiles(t, 1, t.n_it);
       if (!ok) break;
