@@ -195,11 +195,16 @@ struct MainCfg {
   // At d = 64 the rings take the room the dK/dV layout needs anyway (four K and
   // three V stages: 0.7-1.2% faster than three and two at T = 3000-4096).
   static constexpr int kDqKStages = (D == 64) ? 4 : 3;
-  static constexpr int kDqVStages = (D == 64) ? 3 : 1;
+  static constexpr int kDqVStages = (D == 64) ? 3 : 2;
   static constexpr int kDqFixBytes = 2 * kTileBytes;
-  static constexpr int kDqOffQ = kAuxRegion;  // buffer 0; buffer f adds f * kDqFixBytes
+  // A CTA takes its tasks in index order, every dK/dV task before any dQ task, so
+  // the dQ layout may reuse the ONES region, which only dK/dV tasks read: at d = 128
+  // that makes room for a second V stage. At d = 64 its fixed buffers stay where the
+  // dK/dV ones are, since an epilogue's output rows are staged in them.
+  static constexpr int kDqBase = (D == 64) ? kAuxRegion : 0;
+  static constexpr int kDqOffQ = kDqBase;  // buffer 0; buffer f adds f * kDqFixBytes
   static constexpr int kDqOffDO = kDqOffQ + kTileBytes;
-  static constexpr int kDqOffK = kAuxRegion + kNF * kDqFixBytes;
+  static constexpr int kDqOffK = kDqBase + kNF * kDqFixBytes;
   static constexpr int kDqOffV = kDqOffK + kDqKStages * kTileBytes;
   static constexpr int kDqBytes = kDqOffV + kDqVStages * kTileBytes;
   // dK/dV task: fixed buffers [K][V], then the ring of stages [Q][dO][QX][DX].
