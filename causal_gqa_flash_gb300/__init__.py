@@ -20,7 +20,7 @@ __all__ = [
     "NOALLOC_SCRATCH_BYTES",
     "attn_sync_status", "attn_selftest_timeout", "attn_set_wait_budget_ns", "attn_set_task_order", "attn_last_error", "attn_version",
     "GqaView", "view_of", "attn_rope_table", "attn_rope", "attn_fwd_rope", "attn_bwd_rope", "attn_fwd_naive", "attn_bwd_naive",
-    "attn_naive_workspace_bytes", "probe_rates", "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
+    "attn_naive_workspace_bytes", "probe_rates", "probe_tma", "EXPORTED_SYMBOLS", "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED_DEVICE", "GQA_ERR_LAUNCH",
     "GQA_ERR_TIMEOUT",
 ]
 
@@ -38,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "attn_rope_table", "attn_rope", "attn_fwd_rope", "attn_bwd_rope", "attn_naive_workspace_bytes", "attn_fwd_naive", "attn_bwd_naive",
     "attn_last_error", "attn_sync_status", "attn_selftest_timeout",
     "attn_set_wait_budget_ns", "attn_set_task_order", "attn_version", "attn_probe_mma", "attn_probe_ex2",
+    "attn_probe_tma",
 )
 
 _lib = None
@@ -118,6 +119,8 @@ def load():
     lib.attn_probe_mma.restype = i
     lib.attn_probe_ex2.argtypes = [i, vp, vp, vp]
     lib.attn_probe_ex2.restype = i
+    lib.attn_probe_tma.argtypes = [vp, ctypes.c_longlong, i, i, i, vp, vp]
+    lib.attn_probe_tma.restype = i
     _lib = lib
     return lib
 
@@ -536,4 +539,33 @@ def probe_rates(iters: int = 4096, device=None):
     res["sm_mhz_during_mma"] = statistics.median(clocks)
     best = max(res["mma"].values())
     res["mma_peak_tflops_at_probe_clock"] = best * sms * res["sm_mhz_during_mma"] * 1e6 / 1e12
+    return res
+
+
+def probe_tma(sizes_mb=(32, 2048), stages: int = 6, ctas_per_sm=(1, 2), iters: int = 2000, device=None):
+    """Measured rate of the TMA path that fills the kernels' operand rings
+    (attn_probe_tma): 16 KB tiles into shared memory, `stages` requests in flight per
+    CTA, one or two CTAs per SM, over a buffer of each size in MB (32 MB fits the L2,
+    2048 MB does not). Returns a list of dicts: TB/s over the slowest CTA and the
+    implied load latency in microseconds (bytes in flight per SM over the per-SM
+    rate)."""
+    import torch
+    lib = load()
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    res = []
+    for mb in sizes_mb:
+        buf = torch.zeros(int(mb) << 20, dtype=torch.uint8, device=dev)
+        for cps in ctas_per_sm:
+            st = min(stages, 8 if cps == 1 else 6)
+            out = torch.zeros(sms * cps, dtype=torch.int64, device=dev)
+            for _ in range(2):  # the first call warms the caches and the clocks
+                _check(lib.attn_probe_tma(_ptr(buf), buf.numel(), st, cps, iters, _ptr(out), _stream_handle(None)))
+                _check(attn_sync_status())
+            ns = max(out.cpu().tolist())
+            rate = sms * cps * iters * 16384 / ns * 1e9  # bytes/s
+            latency_us = st * cps * 16384 / (rate / sms) * 1e6
+            res.append({"buffer_mb": mb, "ctas_per_sm": cps, "stages": st, "tbps": rate / 1e12,
+                        "latency_us": latency_us})
+        del buf
     return res

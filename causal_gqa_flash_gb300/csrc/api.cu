@@ -877,6 +877,44 @@ gqa_status_t attn_probe_ex2(int iters, void* out, void* sink, void* stream) {
   return GQA_OK;
 }
 
+gqa_status_t attn_probe_tma(const void* buf, long long bytes, int stages, int ctas_per_sm, int iters, void* out,
+                            void* stream) {
+  const char* fn = "attn_probe_tma";
+  t_last_error.clear();
+  if (bytes < 16384 || bytes % 16384 != 0 || bytes / 16384 > 0x7fffffffLL)
+    return fail(GQA_ERR_INVALID_ARG, "%s: bytes must be a positive multiple of 16384 (got %lld)", fn, bytes);
+  if (ctas_per_sm != 1 && ctas_per_sm != 2)
+    return fail(GQA_ERR_INVALID_ARG, "%s: ctas_per_sm must be 1 or 2 (got %d)", fn, ctas_per_sm);
+  const int max_stages = ctas_per_sm == 1 ? 8 : 6;  // 16 KB slots a CTA, two CTAs sharing an SM's 228 KB
+  if (stages < 1 || stages > max_stages)
+    return fail(GQA_ERR_INVALID_ARG, "%s: stages must be in [1, %d] with %d CTA(s) per SM (got %d)", fn, max_stages,
+                ctas_per_sm, stages);
+  if (iters <= 0 || iters > (1 << 20)) return fail(GQA_ERR_INVALID_ARG, "%s: iters must be in [1, 2^20]", fn);
+  gqa_status_t s;
+  if ((s = check_ptr(fn, "buf", buf)) || (s = check_ptr(fn, "out", out))) return s;
+  DeviceState* ds = nullptr;
+  if ((s = device_state(fn, &ds))) return s;
+  // the buffer as bf16 rows of 64 (128 bytes), read in boxes of 128 rows
+  const cuuint64_t rows = static_cast<cuuint64_t>(bytes / 128);
+  CUtensorMap map;
+  cuuint64_t dims[4] = {64, 1, rows, 1};
+  cuuint64_t strides[3] = {128, 128, rows * 128};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(buf), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GQA_ERR_INVALID_ARG, "%s: cuTensorMapEncodeTiled failed (%d)", fn, (int)r);
+  int sms = 0;
+  cudaError_t e = sm_count(&sms);
+  if (e != cudaSuccess) return cuda_fail(fn, "cudaDeviceGetAttribute", e);
+  e = launch_tma_probe(map, static_cast<int>(bytes / 16384), stages, ctas_per_sm, iters,
+                       static_cast<unsigned long long*>(out), ds->status, g_budget_ns.load(), sms,
+                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(fn, "kernel launch", e);
+  return GQA_OK;
+}
+
 gqa_status_t attn_selftest_timeout(unsigned long long budget_ns, void* stream) {
   const char* fn = "attn_selftest_timeout";
   t_last_error.clear();

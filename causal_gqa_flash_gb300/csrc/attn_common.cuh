@@ -196,5 +196,8 @@ cudaError_t launch_selftest_timeout(DevStatusWord* status, unsigned long long bu
 cudaError_t launch_mma_probe(int n, int a_tmem, int chains, int iters, void* out, DevStatusWord* status,
                              unsigned long long budget_ns, int grid, cudaStream_t stream);
 cudaError_t launch_ex2_probe(int iters, unsigned long long* cycles, float* sink, int grid, cudaStream_t stream);
+cudaError_t launch_tma_probe(const CUtensorMap& map, int n_tiles, int stages, int ctas_per_sm, int iters,
+                             unsigned long long* out, DevStatusWord* status, unsigned long long budget_ns, int sms,
+                             cudaStream_t stream);
 
 }  // namespace gqa

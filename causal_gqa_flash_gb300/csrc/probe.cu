@@ -1,5 +1,6 @@
 // probe.cu — rate probes for the units the attention kernels lean on: the tcgen05
-// tensor core (bf16 x bf16 -> fp32 MMAs, M = 128) and the ex2 unit of the softmax.
+// tensor core (bf16 x bf16 -> fp32 MMAs, M = 128), the ex2 unit of the softmax, and
+// the TMA path that fills their operand rings (16 KB tiles into shared memory).
 //
 // "Talking to the GPU", §The real tensor core peak: the page measures its GPU's
 // real MMA peak with enough independent work per SM to keep the unit busy, over one
@@ -124,6 +125,56 @@ __global__ void __launch_bounds__(1024, 1) ex2_probe_kernel(int iters, unsigned 
   if (threadIdx.x == 0) cycles[blockIdx.x] = c1 - c0;
 }
 
+// TMA tile loads: each CTA keeps `stages` loads of one 128-row x 128-byte tile
+// (16 KB, the attention kernels' d = 64 operand tile) in flight, each into its own
+// shared-memory slot with its own mbarrier, for `iters` tiles picked by a per-CTA
+// linear congruential sequence over the tensor's n_tiles tiles. Record per CTA: the
+// global-timer nanoseconds from the first request to the last arrival. With the
+// tensor in the L2 the rate shows the load path; over a tensor far larger than the
+// L2, HBM. Bytes in flight per SM divided by the per-SM rate is the load latency
+// under that load.
+constexpr int kTmaProbeMaxStages = 8;
+constexpr int kTmaTileBytes = 16384;
+
+__global__ void __launch_bounds__(32) tma_probe_kernel(const __grid_constant__ CUtensorMap map, int n_tiles,
+                                                       int stages, int iters, unsigned long long* out,
+                                                       DevStatusWord* status, unsigned long long budget_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ uint64_t full[kTmaProbeMaxStages];
+  __shared__ int abort_sh;
+  if (threadIdx.x != 0) return;
+  for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
+  abort_sh = 0;
+  fence_mbar_init();
+  const WaitCtx ctx{&abort_sh, status, budget_ns, kKidProbe};
+  uint32_t seed = blockIdx.x * 2654435761u + 12345u;
+  const uint64_t t0 = globaltimer_ns();
+  int issued = 0;
+  bool ok = true;
+  for (int i = 0; i < iters + stages && ok; ++i) {
+    const int s = i % stages;
+    // slot s last held request i - stages: it must have landed before the slot is reused
+    if (i >= stages) ok = mbar_wait(&full[s], ((i / stages) - 1) & 1, ctx, 1);
+    if (ok && i < iters) {
+      seed = seed * 1664525u + 1013904223u;
+      const int tile = static_cast<int>((seed >> 8) % static_cast<uint32_t>(n_tiles));
+      mbar_arrive_expect_tx(&full[s], kTmaTileBytes);
+      tma_load_4d(smem + s * kTmaTileBytes, &map, &full[s], 0, 0, tile * 128, 0);
+      ++issued;
+    }
+  }
+  if (!ok) {
+    // let every request already made land before the CTA leaves
+    for (int s = 0; s < stages; ++s) {
+      const int uses = issued / stages + (s < issued % stages ? 1 : 0);
+      if (uses > 0) mbar_wait_drain(&full[s], (uses - 1) & 1, budget_ns);
+    }
+    return;
+  }
+  out[blockIdx.x] = globaltimer_ns() - t0;
+}
+
 }  // namespace
 
 // Both probes request more shared memory than two CTAs could share, so each SM
@@ -137,6 +188,16 @@ cudaError_t launch_mma_probe(int n, int a_tmem, int chains, int iters, void* out
   if (e != cudaSuccess) return e;
   mma_probe_kernel<<<grid, kProbeThreads, smem, stream>>>(n, a_tmem, chains, iters, static_cast<MmaProbeOut*>(out),
                                                           status, budget_ns);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tma_probe(const CUtensorMap& map, int n_tiles, int stages, int ctas_per_sm, int iters,
+                             unsigned long long* out, DevStatusWord* status, unsigned long long budget_ns, int sms,
+                             cudaStream_t stream) {
+  const int smem = stages * kTmaTileBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(tma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  tma_probe_kernel<<<sms * ctas_per_sm, 32, smem, stream>>>(map, n_tiles, stages, iters, out, status, budget_ns);
   return cudaGetLastError();
 }
 

@@ -4,10 +4,11 @@
 
 prints one JSON line: tcgen05 bf16 MMA FLOP per cycle per SM for N = 64, 128, 256
 with A in shared memory ("ss") or tensor memory ("ts"), ex2 lanes per cycle per SM,
-the SM clock seen during the MMA probes, and the best MMA rate at that clock over
-all SMs in TFLOP/s. "Talking to the GPU", §The real tensor core peak: measure the
+the SM clock seen during the MMA probes, the best MMA rate at that clock over
+all SMs in TFLOP/s, and the TMA tile-load rate from the L2 and from HBM with the
+load latency it implies ("tma"). "Talking to the GPU", §The real tensor core peak: measure the
 unit's real rate with enough independent work per SM instead of trusting the data
-sheet. The kernels are attn_probe_mma / attn_probe_ex2 of the library.
+sheet. The kernels are attn_probe_mma / attn_probe_ex2 / attn_probe_tma of the library.
 """
 from __future__ import annotations
 
@@ -22,6 +23,7 @@ def main() -> int:
     import causal_gqa_flash_gb300 as gqa
     gqa.build()
     res = gqa.probe_rates(iters=args.iters)
+    res["tma"] = gqa.probe_tma()
     print(json.dumps(res), flush=True)
     return 0
 

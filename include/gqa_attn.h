@@ -318,8 +318,24 @@ gqa_status_t attn_selftest_timeout(unsigned long long budget_ns, void* stream);
  *   lanes/cycle/SM = 1024 * 8 * iters / cycles. sink: 4 bytes of device memory
  *   (written only to keep the chains alive).
  */
+/*
+ * attn_probe_tma: the TMA path that feeds the attention kernels' operand rings.
+ *   ctas_per_sm (1 or 2) CTAs on every SM each keep `stages` (1..8 with one CTA per
+ *   SM, 1..6 with two) requests in flight for one 128-row x 128-byte tile (16 KB,
+ *   128-byte swizzle) of `buf`, each into its own shared-memory slot, `iters` tiles
+ *   in all, picked by a per-CTA linear congruential sequence over the buffer's
+ *   bytes / 16384 tiles. buf: caller-owned device memory, `bytes` a multiple of
+ *   16384, 16-byte aligned; its contents are only read. Record per CTA (SMs x
+ *   ctas_per_sm of them, 8 bytes each): u64 global-timer ns from the first request
+ *   to the last arrival. Rate = CTAs * iters * 16384 / ns; a buffer that fits the
+ *   L2 measures the load path from the L2, one far larger than it HBM; the bytes a
+ *   SM holds in flight divided by its share of the rate give the load latency.
+ *   iters in [1, 2^20].
+ */
 gqa_status_t attn_probe_mma(int n, int a_tmem, int chains, int iters, void* out, void* stream);
 gqa_status_t attn_probe_ex2(int iters, void* out, void* sink, void* stream);
+gqa_status_t attn_probe_tma(const void* buf, long long bytes, int stages, int ctas_per_sm, int iters, void* out,
+                            void* stream);
 
 /*
  * Time budget of every pipeline wait, in nanoseconds (default 2e9). Applies

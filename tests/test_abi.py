@@ -287,3 +287,22 @@ def test_task_order_argument_checks(lib):
     assert lib.attn_set_task_order(-1) == gqa.GQA_ERR_INVALID_ARG
     for order in (1, 2, 0):
         assert lib.attn_set_task_order(order) == gqa.GQA_OK
+
+
+def test_probe_tma_argument_checks(lib):
+    buf = ctypes.c_void_p(0x10000)  # never dereferenced: every call below is refused first
+    out = ctypes.c_void_p(0x20000)
+    cases = [
+        ((buf, 16384 + 128, 4, 1, 10, out), "multiple of 16384"),
+        ((buf, 0, 4, 1, 10, out), "multiple of 16384"),
+        ((buf, 1 << 20, 4, 3, 10, out), "ctas_per_sm must be 1 or 2"),
+        ((buf, 1 << 20, 0, 1, 10, out), "stages must be in [1, 8]"),
+        ((buf, 1 << 20, 9, 1, 10, out), "stages must be in [1, 8]"),
+        ((buf, 1 << 20, 7, 2, 10, out), "stages must be in [1, 6]"),
+        ((buf, 1 << 20, 4, 1, 0, out), "iters must be in"),
+        ((None, 1 << 20, 4, 1, 10, out), "buf is NULL"),
+        ((ctypes.c_void_p(0x10008), 1 << 20, 4, 1, 10, out), "not 16-byte aligned"),
+    ]
+    for args, needle in cases:
+        assert lib.attn_probe_tma(*args, None) == gqa.GQA_ERR_INVALID_ARG, needle
+        assert needle in gqa.attn_last_error(), (needle, gqa.attn_last_error())

@@ -20,3 +20,19 @@ def test_probe_rates():
     assert 4 <= r["ex2_lanes_per_clk"] <= 128
     assert 300 < r["sm_mhz_during_mma"] < 3000
     assert gqa.attn_sync_status() == gqa.GQA_OK
+
+
+def test_probe_tma():
+    """TMA tile loads: from a buffer that fits the L2 at least as fast as from one
+    that does not, HBM between 1 and 12 TB/s, and a load latency between 0.1 and 20
+    microseconds."""
+    gqa.build()
+    res = gqa.probe_tma(sizes_mb=(32, 1024), iters=500)
+    print(res)
+    by = {(r["buffer_mb"], r["ctas_per_sm"]): r for r in res}
+    for cps in (1, 2):
+        assert by[(32, cps)]["tbps"] >= 0.9 * by[(1024, cps)]["tbps"], by
+        assert 1.0 < by[(1024, cps)]["tbps"] < 12.0, by
+    for r in res:
+        assert 0.1 < r["latency_us"] < 20.0, r
+    assert gqa.attn_sync_status() == gqa.GQA_OK
