@@ -258,8 +258,13 @@ struct MainCfg {
   static constexpr bool kDqTsS = (D == 128);
   static constexpr uint32_t kDqColQA = 448;
   static constexpr bool kKvSepPdS = (D == 64);  // dK/dV: P/dS region of its own
-  static constexpr uint32_t kKvColP = kKvSepPdS ? 256 : 0;
-  static constexpr uint32_t kKvColDS = kKvSepPdS ? 320 : 64;
+  // d = 128 dK/dV: P and dS go over dP's columns, so S(G+1) can be computed as soon
+  // as every compute thread holds S(G); dP(G+1) follows the gradient MMAs of G
+  // (warp 18), and the compute warps start the exponentials of G+1 before dP(G+1)
+  // has landed.
+  static constexpr bool kLateDP = !kKvSepPdS;
+  static constexpr uint32_t kKvColP = kKvSepPdS ? 256 : kColDP;
+  static constexpr uint32_t kKvColDS = kKvSepPdS ? 320 : kColDP + 64;
   static constexpr uint32_t kKvColDV = kKvSepPdS ? 384 : 256;
   static constexpr uint32_t kKvColDK = kKvColDV + D;
   static_assert(kDqColAcc + D <= 512 && kKvColDK + D <= 512, "TMEM columns");
@@ -366,6 +371,42 @@ __device__ __forceinline__ void score_chunk(const uint32_t (&s)[32], const uint3
   }
 }
 
+// score_chunk<true, MASKED> in two halves, for d = 128 dK/dV tiles, whose dP lands
+// after S: P (fp32, kept for dS, and its bf16 pairs) from S alone, then dS from P
+// and dP. The same operations per element as score_chunk, so the same bits.
+template <bool MASKED>
+__device__ __forceinline__ void score_p(const uint32_t (&s)[32], float sl2, int lo, int hi, float (&pf)[32],
+                                        uint32_t (&pk)[16]) {
+  const uint64_t c2 = f2_make(sl2, sl2);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float x0, x1;
+    f2_split(f2_mul(f2_make(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2), x0, x1);
+    float p0 = ex2_approx(x0);
+    float p1 = ex2_approx(x1);
+    if (MASKED) {
+      p0 = (2 * i >= lo && 2 * i < hi) ? p0 : 0.f;
+      p1 = (2 * i + 1 >= lo && 2 * i + 1 < hi) ? p1 : 0.f;
+    }
+    pk[i] = pack_bf16x2(p0, p1);
+    pf[2 * i] = p0;
+    pf[2 * i + 1] = p1;
+  }
+}
+
+// dS of column pairs [8h, 8h + 8) from their 16 dP values.
+__device__ __forceinline__ void score_ds_half(const float (&pf)[32], const uint32_t (&dp)[16], int h,
+                                              uint32_t (&dk)[16]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float d0, d1;
+    f2_split(f2_mul(f2_make(pf[16 * h + 2 * i], pf[16 * h + 2 * i + 1]),
+                    f2_make(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1]))),
+             d0, d1);
+    dk[8 * h + i] = pack_bf16x2(d0, d1);
+  }
+}
+
 // Every barrier is at most one phase ahead of any waiter: sdp_full(G+1) is
 // committed only after sdp_free(G) completed, which needs every compute thread
 // to have passed sdp_full(G); pds_full(G+1) needs pds_free(G), which is committed
@@ -384,7 +425,9 @@ struct MainBars {
   uint64_t k_full[kMaxDqKStages], k_empty[kMaxDqKStages];  // dQ K and V rings
   uint64_t v_full[kMaxDqVStages], v_empty[kMaxDqVStages];
   uint64_t sdp_full;  // MMA -> compute: S(G) and dP(G) are in TMEM
-  uint64_t sdp_free;  // compute -> MMA: every thread has S(G), dP(G) in registers
+  uint64_t sdp_free;  // compute -> MMA: every thread has S(G), dP(G) in registers (d = 128 dK/dV: S(G))
+  uint64_t dp_full;   // d = 128 dK/dV: MMA (warp 18) -> compute: dP(G) is in TMEM
+  uint64_t dp_free;   // d = 128 dK/dV: compute -> compute: every thread has dP(G) in registers
   uint64_t pds_full;  // compute -> MMA: bf16 P/dS of G are in TMEM
   uint64_t pds_free;  // MMA -> compute: the gradient MMAs of G have completed
   uint64_t acc_full;  // MMA -> compute (and producer): every MMA of the task is done
@@ -839,15 +882,16 @@ struct RingPos {
   }
 };
 
-// Warp 1, one task: S and dP of every tile (only dP of dK/dV tiles at d = 128,
-// where the S MMA must follow the gradient MMAs of the previous tile and warp 18
+// Warp 1, one task: S and dP of every tile (only S of dK/dV tiles at d = 128,
+// where the dP MMA must follow the gradient MMAs of the previous tile and warp 18
 // issues it). sdp_full and fixed_free expect two arrivals per phase: warp 1 gives
-// both when it issued both S and dP, otherwise one each with warp 18.
+// both when it issued both S and dP; for a d = 128 dK/dV tile sdp_full reports S
+// alone (two commits after it) and fixed_free gets one arrival from each warp.
 template <int D, bool DKV>
 __device__ __forceinline__ bool sdp_task(const MmaCtx<D>& m, MainBars& bars, const WaitCtx& ctx, int n_it, int f,
                                          int& G, int used, bool& issued) {
   using Cfg = MainCfg<D>;
-  constexpr bool s_too = !DKV || Cfg::kKvSepPdS;  // this warp issues S as well
+  constexpr bool dp_here = !DKV || !Cfg::kLateDP;  // this warp issues dP as well as S
   RingPos<DKV ? Cfg::kKvStages : Cfg::kDqKStages> rb(used);
   RingPos<Cfg::kDqVStages> rv(used);
   bool ok = true;
@@ -856,20 +900,18 @@ __device__ __forceinline__ bool sdp_task(const MmaCtx<D>& m, MainBars& bars, con
     // Q/dO stage) operand is waited for first; in dQ tasks V only before dP, so
     // a late V tile (its ring is refilled only when dP(G-1) completes) does not
     // hold up S.
-    // dK/dV: the dP MMA needs dO (d = 128: its own barrier) and, at d = 64, the S MMA Q
-    ok = warp_wait(DKV ? (Cfg::kSplitStage ? &bars.do_full[rb.slot] : &bars.q_full[rb.slot]) : &bars.k_full[rb.slot],
-                   rb.phase, ctx, 11);
+    // dK/dV: the S MMA needs Q and its row term (d = 128: their own barrier), at d = 64 the
+    // dP MMA dO as well (one barrier for the stage)
+    ok = warp_wait(DKV ? &bars.q_full[rb.slot] : &bars.k_full[rb.slot], rb.phase, ctx, 11);
     if (ok && G > 0) ok = warp_wait(&bars.sdp_free, (G - 1) & 1, ctx, 14);
     if (!ok) break;
     tc_fence_after();
     if (elect_one()) {
-      if (s_too) {
-        m.template s_mmas<DKV>(f, rb.slot);
-        mma_commit(&bars.sdp_full);
-      }
+      m.template s_mmas<DKV>(f, rb.slot);
+      mma_commit(&bars.sdp_full);
       if (DKV) {
-        m.template dp_mmas<DKV>(f, rb.slot);
-        mma_commit(&bars.sdp_full);
+        if (dp_here) m.template dp_mmas<DKV>(f, rb.slot);
+        mma_commit(&bars.sdp_full);  // (d = 128: the phase's second arrival, S alone)
       }
     }
     __syncwarp();
@@ -891,7 +933,7 @@ __device__ __forceinline__ bool sdp_task(const MmaCtx<D>& m, MainBars& bars, con
   // free once they complete
   if (elect_one()) {
     mma_commit(&bars.fixed_free[f]);
-    if (s_too) mma_commit(&bars.fixed_free[f]);
+    if (dp_here) mma_commit(&bars.fixed_free[f]);
   }
   __syncwarp();
   return true;
@@ -933,19 +975,19 @@ __device__ __forceinline__ void sdp_issuer_role(const BwdParams& p, uint8_t* sme
   }
 }
 
-// Warp 18, one task: the gradient MMAs of every tile, and at d = 128 the S MMAs
+// Warp 18, one task: the gradient MMAs of every tile, and at d = 128 the dP MMAs
 // of dK/dV tiles, issued right after the gradient MMAs of the previous tile that
 // read P and dS from the same TMEM columns. Steps it = 0..n_it: gradient MMAs of
-// tile it-1, then (S here) S of tile it.
+// tile it-1, then (dP here) dP of tile it.
 template <int D, bool DKV>
 __device__ __forceinline__ bool grad_task(const MmaCtx<D>& m, MainBars& bars, const WaitCtx& ctx, int n_it, int f,
                                           int n, int G, int used, bool& issued) {
   using Cfg = MainCfg<D>;
-  constexpr bool s_here = DKV && !Cfg::kKvSepPdS;
+  constexpr bool dp_here = DKV && Cfg::kLateDP;
   RingPos<DKV ? Cfg::kKvStages : Cfg::kDqKStages> rg(used);  // stage of tile it-1 (gradient operands)
-  RingPos<Cfg::kKvStages> rs(used);                          // stage of tile it (S operands)
+  RingPos<Cfg::kKvStages> rs(used);                          // stage of tile it (dP operands)
   bool ok = true;
-  if (s_here) {
+  if (dp_here) {
     ok = warp_wait(&bars.fixed_full[f], (n / Cfg::kNF) & 1, ctx, 17);
     if (!ok) return false;
   }
@@ -969,14 +1011,14 @@ __device__ __forceinline__ bool grad_task(const MmaCtx<D>& m, MainBars& bars, co
       issued = true;
       rg.next();
     }
-    if (ok && s_here && it < n_it) {
-      // S(it) overwrites the columns the gradient MMAs above read: same thread, in order
-      ok = warp_wait(&bars.q_full[rs.slot], rs.phase, ctx, 18);
+    if (ok && dp_here && it < n_it) {
+      // dP(it) overwrites the columns the gradient MMAs above read: same thread, in order
+      ok = warp_wait(&bars.do_full[rs.slot], rs.phase, ctx, 18);
       if (!ok) break;
       tc_fence_after();
       if (elect_one()) {
-        m.template s_mmas<true>(f, rs.slot);
-        mma_commit(&bars.sdp_full);
+        m.template dp_mmas<true>(f, rs.slot);
+        mma_commit(&bars.dp_full);
         if (it + 1 == n_it) mma_commit(&bars.fixed_free[f]);
       }
       __syncwarp();
@@ -1044,6 +1086,45 @@ __device__ __forceinline__ bool compute_tiles(const BwdParams& p, MainBars& bars
   }
   // One tile: S, dP -> registers -> sdp_free; P, dS -> TMEM -> pds_full.
   auto tile = [&](int g, bool masked, int lo, int hi) -> bool {
+    if constexpr (DKV && Cfg::kLateDP) {
+      // S -> registers -> sdp_free (S(g+1) may start); P; dP -> registers -> dp_free;
+      // dS; once every thread holds dP(g), P and dS over its columns -> pds_full.
+      if (!warp_wait(&bars.sdp_full, g & 1, ctx, 20)) return false;
+      tc_fence_after();
+      uint32_t sv[32];
+      tmem_ld32(tS, sv);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars.sdp_free);
+      float pf[32];
+      uint32_t pk[16], dk[16];
+      if (masked)
+        score_p<true>(sv, sl2, lo, hi, pf, pk);
+      else
+        score_p<false>(sv, sl2, lo, hi, pf, pk);
+      if (!warp_wait(&bars.dp_full, g & 1, ctx, 24)) return false;
+      tc_fence_after();
+      // dP in two halves of 16 columns: fewer live registers next to P's 48
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t dp[16];
+        tmem_ld16(tDP + 16 * h, dp);
+        tmem_wait_ld();
+        if (h == 1) {
+          tc_fence_before();
+          mbar_arrive(&bars.dp_free);
+        }
+        score_ds_half(pf, dp, h, dk);
+      }
+      if (!warp_wait(&bars.dp_free, g & 1, ctx, 25)) return false;
+      tc_fence_after();
+      tmem_st16(tP, pk);
+      tmem_st16(tDS, dk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars.pds_full);
+      return true;
+    }
     if (!warp_wait(&bars.sdp_full, g & 1, ctx, 20)) return false;
     tc_fence_after();
     uint32_t s[32], dp[32];
@@ -1257,6 +1338,8 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
     }
     mbar_init(&bars.sdp_full, 2);  // one commit from each MMA issuer (or two from warp 1)
     mbar_init(&bars.sdp_free, kComputeThreads);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.dp_free, kComputeThreads);
     mbar_init(&bars.pds_full, kComputeThreads);
     mbar_init(&bars.pds_free, 1);
     mbar_init(&bars.acc_full, 1);
