@@ -144,7 +144,11 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const BwdPreParams
 //   MMA:     S(G+1), dP(G+1) as soon as sdp_free(G) | gradient MMAs of G on
 //            pds_full(G).
 // so the tensor core computes the scores of G+1 while the compute warps work on
-// G. Across a task boundary the next task is published (and its operands start
+// G. d = 128 dK/dV tiles have no TMEM room for a P/dS region of their own: P and
+// dS go over dP's columns, S(G+1) still follows sdp_free(G) (which there means
+// "every thread holds S(G)"), dP(G+1) follows the gradient MMAs of G on warp 18,
+// and the compute warps form P from S before they wait for dP (dp_full) and,
+// once every thread holds dP (dp_free), write P and dS over it. Across a task boundary the next task is published (and its operands start
 // loading) while this task's last tiles run; its first scores follow its fixed
 // operands and first K (or Q/dO) tile.
 // Per task: fixed_full (its fixed operands are in shared memory), fixed_free
@@ -162,9 +166,9 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const BwdPreParams
 //   dQ:        S [0,128) dP [128,256) dS [256,320) dQ [320,320+D)
 //   dK/dV 64:  S [0,128) dP [128,256) P [256,320) dS [320,384) dV [384,448) dK [448,512)
 //   dK/dV 128: S [0,128) dP [128,256) dV [256,384) dK [384,512); no room for a separate
-//              P/dS region, so P goes to S columns [0,64) and dS to [64,128) once every
-//              warpgroup has read S (sdp_free), and S(G+1) follows the gradient MMAs
-//              of G (warp 18 issues it right after them; warp 1 issues dP).
+//              P/dS region, so P goes to dP columns [128,192) and dS to [192,256) once
+//              every warpgroup has read dP (dp_free), and dP(G+1) follows the gradient
+//              MMAs of G (warp 18 issues it right after them; warp 1 issues S).
 // Warpgroup g writes the bf16 pairs of its score columns [32g, 32g+32) to columns
 // [16g, 16g+16) of the P (dS) region, so the A operand of K-step kk is at 8*kk.
 // ============================================================================
@@ -412,7 +416,10 @@ __device__ __forceinline__ void score_ds_half(const float (&pf)[32], const uint3
 // to have passed sdp_full(G); pds_full(G+1) needs pds_free(G), which is committed
 // only after pds_full(G) was seen; fixed_full of a buffer is produced again only
 // after its fixed_free was seen, which needs that fixed_full; acc_free(n) needs acc_full(n)
-// and acc_full(n+1) needs acc_free(n); task_full(n+2) needs task_empty(n).
+// and acc_full(n+1) needs acc_free(n); task_full(n+2) needs task_empty(n); dp_full(G+1)
+// follows the gradient MMAs of G, which need pds_full(G), given only after dp_free(G)
+// was seen; stg_free(n+2) needs task n+2's fixed operands, loaded only after
+// stg_free(n) was seen.
 struct MainBars {
   uint64_t task_full[2], task_empty[2];   // producer <-> every other warp: next task index
   uint64_t fixed_full[2], fixed_free[2];   // per fixed buffer: operands loaded / no longer read
