@@ -148,8 +148,9 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const BwdPreParams
 // dS go over dP's columns, S(G+1) still follows sdp_free(G) (which there means
 // "every thread holds S(G)"), dP(G+1) follows the gradient MMAs of G on warp 18,
 // and the compute warps form P from S before they wait for dP (dp_full) and,
-// once every thread holds dP (dp_free), write P and dS over it. Across a task boundary the next task is published (and its operands start
-// loading) while this task's last tiles run; its first scores follow its fixed
+// once every thread holds dP (dp_free), write P and dS over it. Across a task
+// boundary the next task is published (and its operands start loading) while this
+// task's last tiles run; its first scores follow its fixed
 // operands and first K (or Q/dO) tile.
 // Per task: fixed_full (its fixed operands are in shared memory), fixed_free
 // (its last S/dP MMAs are done, the fixed operands may be replaced), acc_full
@@ -215,9 +216,10 @@ struct MainCfg {
   // The two gradient chains (dV += P^T dO, dK += dS^T Q) are separate N = D MMAs:
   // at d = 64 a single N = 128 chain over block-diagonal operands (half of it
   // multiplying zeros) measured 8-10% slower overall.
-  // Q/dO stages. At d = 64 a stage is busy from its load (~1 us from the L2) until
-  // the tile's gradient MMAs finish, about two tile periods later: two stages
-  // measured 18% slower than three, and the fourth gained 2-3% more.
+  // Q/dO stages. At d = 64 a stage is busy from its load (~1.6 us from the L2 under
+  // load, attn_probe_tma) until the tile's gradient MMAs finish, about two tile
+  // periods later: two stages measured 18% slower than three, and the fourth (room
+  // made by the shared row-term tile and the staging in the fixed buffers) 6% faster.
   static constexpr int kKvStages = (D == 64) ? 4 : 2;
   // d = 128: each stage's dO and Q have their own barriers (see MainBars)
   static constexpr bool kSplitStage = (D == 128);
