@@ -457,7 +457,8 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
       const int qt = p.nT - 1 - fdiv(id, p.fd_bh);
       const int n_kv = p.causal ? qt + 1 : p.nT;
       float m_used = -INFINITY;  // running max in log2 units (possibly stale by <= 8)
-      float l = 0.f;
+      float l = 0.f;   // row sum of the fp32 probabilities (for the LSE)
+      float lo = 0.f;  // the same less each tile's top term's bf16 rounding (for O, see below)
       for (int j = 0; j < n_kv; ++j, ++g) {
         ok = warp_wait(&bar_s, g & 1, ctx, 20);
         if (!ok) break;
@@ -505,6 +506,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
           alpha = ex2_approx(m_used - m_tile);
           m_used = m_tile;
           l *= alpha;
+          lo *= alpha;
         }
         // p = 2^(s*c - m) two columns at a time (packed fp32 FMA and add), bf16 pairs kept
         // in registers until the P columns are free.
@@ -523,6 +525,14 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
           float a0, a1;
           f2_split(f2_add(f2_add(lsum[0], lsum[1]), f2_add(lsum[2], lsum[3])), a0, a1);
           l += a0 + a1;
+          // The PV MMA weighs each key by its bf16-rounded probability. With m_used up to
+          // 2^8 stale the largest term of a tile is not a power of two, and in a row one
+          // key dominates its rounding (up to 2^-9 relative) would move O by that much of
+          // the key's value when O is divided by the fp32 sum: O's divisor therefore
+          // counts each tile's largest term as the MMA sees it (the same FMA and ex2 as
+          // in the loop above, then the same rounding).
+          const float ptop = ex2_approx(fmaf(mx, sl2, -m_used));
+          lo += (a0 + a1) - (ptop - __bfloat162float(__float2bfloat16_rn(ptop)));
         }
         // d = 64: P(g-1) (possibly of the previous item) must no longer be read by PV(g-1).
         if (kSepP && g > 0) {
@@ -556,7 +566,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdCtasPerSm) attn_fwd_kernel(co
       tc_fence_after();
       const FwdItem it = decode_item(p, id);
       const int q_idx = qt * kTile + row;
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lo;
       const bool valid = q_idx < p.T;
       if constexpr (Cfg::kTmaStore) {
         // O / l as bf16 pairs, then O's columns are free; 32 rows x 128 bytes per
