@@ -1,8 +1,10 @@
 """GPU parity at the full benchmark sizes, in the launch configuration the
 benchmark times. The whole problem runs on the GPU; the oracle then checks
 whole (batch, kv-head) groups — each an independent slice of the problem with
-all of its query heads — element by element, and every output is checked for
-finiteness, guard bytes and bit-identical repeat runs.
+all of its query heads — element by element: O and LSE of every group against the
+oracle's forward, and the gradients of the first and last group against its
+backward. Every output is checked for finiteness, guard bytes and bit-identical
+repeat runs.
 """
 import numpy as np
 import pytest
@@ -54,6 +56,16 @@ def test_fullsize_groups(name):
         assert torch.equal(a.view(torch.uint8), g.tensor.view(torch.uint8))
 
     o, lse, dq, dk, dv = outs
+    worst_o = worst_l = 0.0
+    for b in range(B):
+        for kv in range(Hkv):
+            hs = slice(kv * G, (kv + 1) * G)
+            ro, rl = oracle.fwd(q[b:b + 1, :, hs], k[b:b + 1, :, kv:kv + 1], v[b:b + 1, :, kv:kv + 1],
+                                causal=w.causal)
+            worst_o = max(worst_o, o_err(f64(o[b:b + 1, :, hs]), ro))
+            worst_l = max(worst_l, max_abs(f64(lse[b:b + 1, hs]), rl))
+    print(f"{name} every group: O {worst_o:.2e} beyond the bf16 half-ulp, LSE {worst_l:.2e}")
+    assert worst_o <= TOL_O and worst_l <= TOL_LSE, (worst_o, worst_l)
     for b, kv in ((0, 0), (B - 1, Hkv - 1)):
         hs = slice(kv * G, (kv + 1) * G)
         ref = oracle.bwd(q[b:b + 1, :, hs], k[b:b + 1, :, kv:kv + 1], v[b:b + 1, :, kv:kv + 1],
