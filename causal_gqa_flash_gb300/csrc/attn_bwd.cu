@@ -147,8 +147,9 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const BwdPreParams
 // G. d = 128 dK/dV tiles have no TMEM room for a P/dS region of their own: P and
 // dS go over dP's columns, S(G+1) still follows sdp_free(G) (which there means
 // "every thread holds S(G)"), dP(G+1) follows the gradient MMAs of G on warp 18,
-// and the compute warps form P from S before they wait for dP (dp_full) and,
-// once every thread holds dP (dp_free), write P and dS over it. Across a task
+// and the compute warps form P from S before they wait for dP (dp_full), then write
+// P and dS over their warpgroup's own dP columns (no wait: each thread overwrites
+// only the cells it has just read). Across a task
 // boundary the next task is published (and its operands start loading) while this
 // task's last tiles run; its first scores follow its fixed
 // operands and first K (or Q/dO) tile.
@@ -167,11 +168,12 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const BwdPreParams
 //   dQ:        S [0,128) dP [128,256) dS [256,320) dQ [320,320+D)
 //   dK/dV 64:  S [0,128) dP [128,256) P [256,320) dS [320,384) dV [384,448) dK [448,512)
 //   dK/dV 128: S [0,128) dP [128,256) dV [256,384) dK [384,512); no room for a separate
-//              P/dS region, so P goes to dP columns [128,192) and dS to [192,256) once
-//              every warpgroup has read dP (dp_free), and dP(G+1) follows the gradient
-//              MMAs of G (warp 18 issues it right after them; warp 1 issues S).
-// Warpgroup g writes the bf16 pairs of its score columns [32g, 32g+32) to columns
-// [16g, 16g+16) of the P (dS) region, so the A operand of K-step kk is at 8*kk.
+//              P/dS region, so warpgroup g puts its P pairs in dP columns
+//              [128+32g, 128+32g+16) and its dS pairs in the next 16 (its own dP
+//              columns), and dP(G+1) follows the gradient MMAs of G (warp 18 issues it
+//              right after them; warp 1 issues S).
+// Elsewhere warpgroup g writes the bf16 pairs of its score columns [32g, 32g+32) to
+// columns [16g, 16g+16) of the P (dS) region, so the A operand of K-step kk is at 8*kk.
 // ============================================================================
 constexpr int kMainThreads = 608;
 constexpr int kComputeThreads = 512;
@@ -269,6 +271,8 @@ struct MainCfg {
   // (warp 18), and the compute warps start the exponentials of G+1 before dP(G+1)
   // has landed.
   static constexpr bool kLateDP = !kKvSepPdS;
+  // (d = 128: P and dS are interleaved per warpgroup over the dP columns, see
+  // grad_mmas_split; these two name the region for the other paths)
   static constexpr uint32_t kKvColP = kKvSepPdS ? 256 : kColDP;
   static constexpr uint32_t kKvColDS = kKvSepPdS ? 320 : kColDP + 64;
   static constexpr uint32_t kKvColDV = kKvSepPdS ? 384 : 256;
@@ -419,10 +423,10 @@ __device__ __forceinline__ void score_ds_half(const float (&pf)[32], const uint3
 // only after pds_full(G) was seen; fixed_full of a buffer is produced again only
 // after its fixed_free was seen, which needs that fixed_full; acc_free(n) needs acc_full(n)
 // and acc_full(n+1) needs acc_free(n); task_full(n+2) needs task_empty(n); dp_full(G+1)
-// follows the gradient MMAs of G, which need pds_full(G), given only after dp_free(G)
+// follows the gradient MMAs of G, which need pds_full(G), given only after dp_full(G)
 // was seen; stg_free(n+2) needs task n+2's fixed operands, loaded only after
 // stg_free(n) was seen.
-struct MainBars {
+struct alignas(16) MainBars {
   uint64_t task_full[2], task_empty[2];   // producer <-> every other warp: next task index
   uint64_t fixed_full[2], fixed_free[2];   // per fixed buffer: operands loaded / no longer read
   uint64_t stg_free[2];  // per fixed buffer (d = 64): the epilogue's TMA stores have read their rows there
@@ -436,7 +440,6 @@ struct MainBars {
   uint64_t sdp_full;  // MMA -> compute: S(G) and dP(G) are in TMEM
   uint64_t sdp_free;  // compute -> MMA: every thread has S(G), dP(G) in registers (d = 128 dK/dV: S(G))
   uint64_t dp_full;   // d = 128 dK/dV: MMA (warp 18) -> compute: dP(G) is in TMEM
-  uint64_t dp_free;   // d = 128 dK/dV: compute -> compute: every thread has dP(G) in registers
   uint64_t pds_full;  // compute -> MMA: bf16 P/dS of G are in TMEM
   uint64_t pds_free;  // MMA -> compute: the gradient MMAs of G have completed
   uint64_t acc_full;  // MMA -> compute (and producer): every MMA of the task is done
@@ -840,16 +843,21 @@ struct MmaCtx {
   }
   // dK/dV gradient MMAs as two chains, dV first, with a commit on `do_free` between
   // them so that the dO slot is refilled while the dK chain still reads Q.
+  // d = 128: warpgroup g's P pairs (query columns [32g, 32g+32)) sit in dP columns
+  // [32g, 32g+16) and its dS pairs in [32g+16, 32g+32), so K-step kk reads warpgroup kk/2.
   __device__ __forceinline__ void grad_mmas_split(int bslot, bool first, uint64_t* do_free) const {
-    const uint32_t tP = tmem + Cfg::kKvColP, tDS = tmem + Cfg::kKvColDS;
+    static_assert(Cfg::kLateDP, "P and dS over dP's columns");
+    const uint32_t tBase = tmem + Cfg::kColDP;
     const uint64_t g1 = kvG1 + bslot * kStG1, g2 = kvG2 + bslot * kStG2;
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk)
-      mma_ts(tmem + Cfg::kKvColDV, tP + kk * 8, g1 + kk * 128, idesc_g, (!first || kk > 0) ? 1u : 0u);
+      mma_ts(tmem + Cfg::kKvColDV, tBase + 32 * (kk >> 1) + 8 * (kk & 1), g1 + kk * 128, idesc_g,
+             (!first || kk > 0) ? 1u : 0u);
     mma_commit(do_free);
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk)
-      mma_ts(tmem + Cfg::kKvColDK, tDS + kk * 8, g2 + kk * 128, idesc_g, (!first || kk > 0) ? 1u : 0u);
+      mma_ts(tmem + Cfg::kKvColDK, tBase + 32 * (kk >> 1) + 16 + 8 * (kk & 1), g2 + kk * 128, idesc_g,
+             (!first || kk > 0) ? 1u : 0u);
   }
   // Gradient MMAs of one tile; `first` starts the task's accumulators.
   template <bool DKV>
@@ -1008,7 +1016,7 @@ __device__ __forceinline__ bool grad_task(const MmaCtx<D>& m, MainBars& bars, co
       if (!ok) break;
       tc_fence_after();
       if (elect_one()) {
-        if (DKV && Cfg::kSplitStage)
+        if constexpr (DKV && Cfg::kSplitStage)
           m.grad_mmas_split(rg.slot, it == 1, &bars.do_empty[rg.slot]);
         else
           m.template grad_mmas<DKV>(rg.slot, it == 1);
@@ -1096,8 +1104,8 @@ __device__ __forceinline__ bool compute_tiles(const BwdParams& p, MainBars& bars
   // One tile: S, dP -> registers -> sdp_free; P, dS -> TMEM -> pds_full.
   auto tile = [&](int g, bool masked, int lo, int hi) -> bool {
     if constexpr (DKV && Cfg::kLateDP) {
-      // S -> registers -> sdp_free (S(g+1) may start); P; dP -> registers -> dp_free;
-      // dS; once every thread holds dP(g), P and dS over its columns -> pds_full.
+      // S -> registers -> sdp_free (S(g+1) may start); P; dP -> registers; dS; P and
+      // dS over the warpgroup's own dP columns -> pds_full.
       if (!warp_wait(&bars.sdp_full, g & 1, ctx, 20)) return false;
       tc_fence_after();
       uint32_t sv[32];
@@ -1119,16 +1127,12 @@ __device__ __forceinline__ bool compute_tiles(const BwdParams& p, MainBars& bars
         uint32_t dp[16];
         tmem_ld16(tDP + 16 * h, dp);
         tmem_wait_ld();
-        if (h == 1) {
-          tc_fence_before();
-          mbar_arrive(&bars.dp_free);
-        }
         score_ds_half(pf, dp, h, dk);
       }
-      if (!warp_wait(&bars.dp_free, g & 1, ctx, 25)) return false;
-      tc_fence_after();
-      tmem_st16(tP, pk);
-      tmem_st16(tDS, dk);
+      // P and dS over this warpgroup's own 32 dP columns, which this thread has just
+      // read in its own lane: no other thread's data is overwritten, so no barrier
+      tmem_st16(tDP, pk);
+      tmem_st16(tDP + 16, dk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars.pds_full);
@@ -1348,7 +1352,6 @@ __global__ void __launch_bounds__(kMainThreads, 1) bwd_main_kernel(const __grid_
     mbar_init(&bars.sdp_full, 2);  // one commit from each MMA issuer (or two from warp 1)
     mbar_init(&bars.sdp_free, kComputeThreads);
     mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.dp_free, kComputeThreads);
     mbar_init(&bars.pds_full, kComputeThreads);
     mbar_init(&bars.pds_free, 1);
     mbar_init(&bars.acc_full, 1);
